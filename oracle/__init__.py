@@ -1,0 +1,324 @@
+"""CPU oracle for the routed MoE FFN over NVFP4 weights.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference legs of ``bench.py`` may import this package.  The
+product library never loads it, and it shares no code with the CUDA path.
+
+Two halves:
+  * ``moe_oracle.c`` (compiled here into ``_build/liboracle.so``): the parts whose
+    result must be bit-exact -- E2M1/E4M3 codecs, the NVFP4 quantiser in fp32,
+    the router logits in a fixed fp32 order, top-k and the stable grouping.
+  * this module: ctypes wrappers and the FFN in FP64 with numpy (a matmul is
+    the only library step), following the definition
+
+        out[t] = sum_j w[t][j] * FFN_{id[t][j]}(x_t)  (+ FFN_shared(x_t))
+        FFN_e(v) = Wd_e ( silu(Wg_e v) * (Wu_e v) ),   silu(z) = z / (1 + e^-z)
+
+    with every weight dequantised as E2M1(code) * E4M3(scale) * tensor_scale.
+
+Sources (page title, section): "NVIDIA FP4-Local checkpoints on DGX Spark ...
+#565", section 4 Round 1 -- gate, up and SwiGLU of the routed experts (#766),
+one FP32 tensor scale per expert weight (#517, #545), activations rounded to
+FP4 in the W4A4 GEMM (#687), the SwiGLU output quantised before the down GEMM
+(#760), down rows in BF16 rounded to nearest even (#914), the card sum folded
+into the combine (#701), the shared expert added beside the routed ones (#686);
+"bloomery 0.3.9", New: an f64 oracle with a band for sums whose order is the
+hardware's.
+
+Parity status: the codecs, quantiser, router, top-k, grouping and the FFN are
+pinned by the tests in ``tests/test_oracle_*.py`` (tables, library
+conversions, brute force, identities, a hand-worked example, a dense-MLP
+special case).  Nothing here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "liboracle.so")
+_SRC = os.path.join(_HERE, "moe_oracle.c")
+_lock = threading.Lock()
+_lib = None
+
+ROUTER_SOFTMAX = 0
+ROUTER_SIGMOID = 1
+MODE_W4A16 = 0
+MODE_W4A4 = 1
+
+
+def build_library(force: bool = False) -> str:
+    """Compile moe_oracle.c with gcc (no fused multiply-add contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_SO) and os.path.getmtime(_SO) >= os.path.getmtime(_SRC):
+        return _SO
+    base = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+            _SRC, "-o", _SO + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_SO + ".tmp", _SO)
+    return _SO
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build_library()
+            L = ctypes.CDLL(_SO)
+            c = ctypes
+            P = c.c_void_p
+            L.oracle_e2m1_value.argtypes = [c.c_int]
+            L.oracle_e2m1_value.restype = c.c_double
+            L.oracle_e4m3_value.argtypes = [c.c_int]
+            L.oracle_e4m3_value.restype = c.c_double
+            L.oracle_e2m1_table.argtypes = [P]
+            L.oracle_e4m3_table.argtypes = [P]
+            L.oracle_e4m3_from_f32.argtypes = [c.c_float]
+            L.oracle_e4m3_from_f32.restype = c.c_uint8
+            L.oracle_e2m1_from_f32.argtypes = [c.c_float]
+            L.oracle_e2m1_from_f32.restype = c.c_uint8
+            L.oracle_e4m3_from_f32_array.argtypes = [P, c.c_int64, P]
+            L.oracle_e2m1_from_f32_array.argtypes = [P, c.c_int64, P]
+            L.oracle_f64_to_bf16.argtypes = [c.c_double]
+            L.oracle_f64_to_bf16.restype = c.c_uint16
+            L.oracle_f64_to_bf16_array.argtypes = [P, c.c_int64, P]
+            L.oracle_nvfp4_tensor_scale.argtypes = [P, c.c_int64]
+            L.oracle_nvfp4_tensor_scale.restype = c.c_float
+            L.oracle_nvfp4_quantize.argtypes = [P, c.c_int64, c.c_int64, c.c_float, P, P]
+            L.oracle_router_logits.argtypes = [P, c.c_int32, c.c_int32, P, c.c_int32, P, P]
+            L.oracle_topk.argtypes = [P, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, P, P]
+            L.oracle_group.argtypes = [P, c.c_int64, c.c_int32, P, P]
+            _lib = L
+    return _lib
+
+
+def _p(a: np.ndarray):
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+# ------------------------------------------------------------------ codecs
+
+def e2m1_table() -> np.ndarray:
+    out = np.zeros(16, np.float64)
+    lib().oracle_e2m1_table(_p(out))
+    return out
+
+
+def e4m3_table() -> np.ndarray:
+    out = np.zeros(256, np.float64)
+    lib().oracle_e4m3_table(_p(out))
+    return out
+
+
+def e4m3_from_f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.zeros(x.shape, np.uint8)
+    lib().oracle_e4m3_from_f32_array(_p(x), x.size, _p(out))
+    return out
+
+
+def e2m1_from_f32(x) -> np.ndarray:
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    out = np.zeros(x.shape, np.uint8)
+    lib().oracle_e2m1_from_f32_array(_p(x), x.size, _p(out))
+    return out
+
+
+def f64_to_bf16(x) -> np.ndarray:
+    """FP64 -> bf16 bit patterns (uint16), one round-to-nearest-even."""
+    x = np.ascontiguousarray(np.asarray(x, np.float64))
+    out = np.zeros(x.shape, np.uint16)
+    lib().oracle_f64_to_bf16_array(_p(x), x.size, _p(out))
+    return out
+
+
+def bf16_to_f64(b) -> np.ndarray:
+    b = np.asarray(b, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_to_f32(b) -> np.ndarray:
+    b = np.asarray(b, np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# ------------------------------------------------------------------ NVFP4
+
+def tensor_scale(x) -> float:
+    """amax / (6*448) of the whole tensor, in fp32."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    return float(np.float32(lib().oracle_nvfp4_tensor_scale(_p(x), x.size)))
+
+
+def quantize(x, ts: float | None = None):
+    """NVFP4-quantise a [rows][cols] fp32 matrix.  Returns (codes, scales, ts)."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    assert x.ndim == 2 and x.shape[1] % 16 == 0
+    if ts is None:
+        ts = tensor_scale(x)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 16), np.uint8)
+    lib().oracle_nvfp4_quantize(_p(x), rows, cols, ctypes.c_float(ts), _p(codes), _p(scales))
+    return codes, scales, float(np.float32(ts))
+
+
+def unpack_codes(codes: np.ndarray) -> np.ndarray:
+    """[.., K/2] bytes -> [.., K] 4-bit codes, element 2i from the low nibble."""
+    codes = np.asarray(codes, np.uint8)
+    q = np.empty(codes.shape[:-1] + (codes.shape[-1] * 2,), np.uint8)
+    q[..., 0::2] = codes & 0x0F
+    q[..., 1::2] = codes >> 4
+    return q
+
+
+def dequantize(codes, scales, ts) -> np.ndarray:
+    """NVFP4 -> FP64: E2M1(code) * E4M3(scale) * tensor_scale."""
+    q = unpack_codes(codes)
+    s = np.repeat(e4m3_table()[np.asarray(scales, np.uint8)], 16, axis=-1)
+    return e2m1_table()[q] * s * float(ts)
+
+
+# ------------------------------------------------------------------ router
+
+def router_logits(x_bf16: np.ndarray, router_w: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    x = np.ascontiguousarray(x_bf16, np.uint16)
+    w = np.ascontiguousarray(router_w, np.float32)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H and H % 8 == 0
+    out = np.zeros((T, E), np.float32)
+    b = None if bias is None else np.ascontiguousarray(bias, np.float32)
+    lib().oracle_router_logits(_p(x), T, H, _p(w), E, None if b is None else _p(b), _p(out))
+    return out
+
+
+def topk(logits: np.ndarray, k: int, kind: int, renormalize: bool = True):
+    lg = np.ascontiguousarray(logits, np.float32)
+    T, E = lg.shape
+    assert 1 <= k <= min(E, 64)
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    lib().oracle_topk(_p(lg), T, E, k, kind, int(bool(renormalize)), _p(ids), _p(w))
+    return ids, w
+
+
+def group(ids: np.ndarray, E: int):
+    flat = np.ascontiguousarray(ids, np.int32).ravel()
+    offsets = np.zeros(E + 1, np.int32)
+    rows = np.zeros(flat.size, np.int32)
+    lib().oracle_group(_p(flat), flat.size, E, _p(offsets), _p(rows))
+    return offsets, rows
+
+
+# ------------------------------------------------------------------ FFN
+
+def silu(z: np.ndarray) -> np.ndarray:
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def route(x_bf16, router_w, router_bias, k, kind, renormalize=True):
+    """Router + grouping.  Returns a dict of logits, ids, weights, offsets, rows."""
+    E = router_w.shape[0]
+    lg = router_logits(x_bf16, router_w, router_bias)
+    ids, w = topk(lg, k, kind, renormalize)
+    offsets, rows = group(ids, E)
+    return dict(logits=lg, ids=ids, weights=w, offsets=offsets, sorted_rows=rows)
+
+
+def quantize_activations(x_bf16: np.ndarray):
+    """W4A4 activation quantisation: tensor scale from the batch amax."""
+    xf = bf16_to_f32(x_bf16)
+    return quantize(xf)
+
+
+def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormalize=True,
+            mode=MODE_W4A16, shared=None, keep=False):
+    """The whole MoE FFN in FP64.
+
+    expert(e) -> ((gc, gs, gts), (uc, us, uts), (dc, ds, dts)): expert e's packed
+    NVFP4 gate [I][H], up [I][H] and down [H][I] (the oracle's own quantisation).
+    shared: None or the same triple for the shared expert (weight 1, every token).
+    Returns a dict with the route, the FP64 output and its bf16 bit patterns.
+    """
+    x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
+    T, H = x_bf16.shape
+    E = router_w.shape[0]
+    r = route(x_bf16, router_w, router_bias, k, router_kind, renormalize)
+    res = dict(r)
+    if mode == MODE_W4A4:
+        xc, xs, xts = quantize_activations(x_bf16)
+        xin = dequantize(xc, xs, xts)
+        res.update(x_codes=xc, x_scales=xs, x_ts=xts)
+    else:
+        xin = bf16_to_f64(x_bf16)
+
+    offsets, rows = r["offsets"], r["sorted_rows"]
+    wflat = r["weights"].ravel()
+    out = np.zeros((T, H), np.float64)
+
+    def up_part(weights, X):
+        (gc, gs, gts), (uc, us, uts), _ = weights
+        g = X @ dequantize(gc, gs, gts).T
+        u = X @ dequantize(uc, us, uts).T
+        return silu(g) * u
+
+    def down_part(weights, h):
+        _, _, (dc, ds, dts) = weights
+        return h @ dequantize(dc, ds, dts).T
+
+    def quant_h(h_all):
+        """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax."""
+        h32 = [h.astype(np.float32) for h in h_all]
+        amax = max((float(np.max(np.abs(h))) for h in h32 if h.size), default=0.0)
+        ts = float(np.float32(np.float32(amax) / np.float32(2688.0)))
+        return [dequantize(*quantize(h, ts)[:2], ts) if h.size else h.astype(np.float64)
+                for h in h32], ts
+
+    active = [e for e in range(E) if offsets[e + 1] > offsets[e]]
+    hs = {}
+    for e in active:
+        pr = rows[offsets[e]:offsets[e + 1]]
+        hs[e] = up_part(expert(e), xin[pr // k])
+    if mode == MODE_W4A4:
+        qh, ts_h = quant_h([hs[e] for e in active])
+        hs = dict(zip(active, qh))
+        res["h_ts"] = ts_h
+    if keep:
+        res["h"] = hs
+    for e in active:
+        pr = rows[offsets[e]:offsets[e + 1]]
+        y = down_part(expert(e), hs[e])
+        np.add.at(out, pr // k, wflat[pr][:, None] * y)
+
+    if shared is not None:
+        hsh = up_part(shared, xin)
+        if mode == MODE_W4A4:
+            (hsh,), ts_s = quant_h([hsh])
+            res["shared_h_ts"] = ts_s
+        out += down_part(shared, hsh)
+
+    res["out"] = out
+    res["out_bf16"] = f64_to_bf16(out)
+    return res
+
+
+def compare_output(got_bf16: np.ndarray, ref_f64: np.ndarray):
+    """Output tolerance: max|d| <= 2e-2 * RMS(ref) and ||d||_2 / ||ref||_2 <= 5e-3."""
+    got = bf16_to_f64(got_bf16)
+    d = got - ref_f64
+    rms = float(np.sqrt(np.mean(ref_f64 ** 2)))
+    max_abs = float(np.max(np.abs(d)))
+    rel_l2 = float(np.linalg.norm(d) / max(np.linalg.norm(ref_f64), 1e-300))
+    ok = (max_abs <= 2e-2 * rms) and (rel_l2 <= 5e-3) and bool(np.all(np.isfinite(got)))
+    return ok, dict(max_abs=max_abs, rms=rms, max_abs_over_rms=max_abs / max(rms, 1e-300), rel_l2=rel_l2)

@@ -1,0 +1,110 @@
+"""Pins of the oracle's router logits, top-k, routing weights and grouping
+(no GPU)."""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _bf16(a):
+    return oracle.f64_to_bf16(np.asarray(a, np.float64))
+
+
+def test_logit_order_hand_worked():
+    # H = 256: position h belongs to lane (h // 8) % 32.  One large term in lane 0
+    # and two ones; the butterfly (offsets 16, 8, 4, 2, 1) decides the rounding.
+    H = 256
+    x = np.zeros((2, H))
+    w = np.zeros((1, H), np.float32)
+    w[0, 0] = 2.0 ** 24
+    w[0, 8] = w[0, 16] = w[0, 24] = 1.0
+    x[0, [0, 8, 16]] = 1.0   # ones in lanes 1 and 2: lane0+=lane2 then +=lane1, each 2^24+1 -> 2^24
+    x[1, [0, 8, 24]] = 1.0   # ones in lanes 1 and 3: lane1+=lane3 gives 2, then 2^24+2 exactly
+    lg = oracle.router_logits(_bf16(x), w, None)
+    assert lg[0, 0] == 2.0 ** 24
+    assert lg[1, 0] == 2.0 ** 24 + 2
+    # within a lane the sum runs in increasing h with one rounding per step
+    x2 = np.zeros((1, H)); w2 = np.zeros((1, H), np.float32)
+    x2[0, [0, 1, 2]] = 1.0
+    w2[0, 0] = 2.0 ** 24; w2[0, 1] = 1.0; w2[0, 2] = 1.0   # (2^24 + 1) + 1 -> 2^24
+    assert oracle.router_logits(_bf16(x2), w2, None)[0, 0] == 2.0 ** 24
+    b = np.array([0.5], np.float32)
+    assert oracle.router_logits(_bf16(x2), w2, b)[0, 0] == 2.0 ** 24  # bias added last in fp32
+
+
+def test_logits_within_fp32_error_bound_of_exact_dot():
+    rng = np.random.default_rng(6)
+    T, H, E = 5, 1024, 12
+    x = _bf16(rng.normal(0, 1, (T, H)))
+    w = rng.normal(0, H ** -0.5, (E, H)).astype(np.float32)
+    bias = rng.normal(0, 1, E).astype(np.float32)
+    lg = oracle.router_logits(x, w, bias).astype(np.float64)
+    xf = oracle.bf16_to_f64(x)
+    exact = xf @ w.astype(np.float64).T + bias
+    absdot = np.abs(xf) @ np.abs(w.astype(np.float64)).T + np.abs(bias)
+    n = H // 32 + 5 + 1
+    gamma = n * 2.0 ** -24 / (1 - n * 2.0 ** -24)
+    assert np.all(np.abs(lg - exact) <= gamma * absdot)
+
+
+def _brute_topk(lg_row, k):
+    order = sorted(range(len(lg_row)), key=lambda e: (-float(lg_row[e]), e))
+    return order[:k]
+
+
+@pytest.mark.parametrize("E,k", [(4, 1), (6, 2), (8, 3), (5, 5)])
+def test_topk_brute_force_with_ties(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    lg = rng.integers(-2, 3, (200, E)).astype(np.float32)  # many exact ties
+    ids, w = oracle.topk(lg, k, oracle.ROUTER_SOFTMAX)
+    for t in range(lg.shape[0]):
+        assert list(ids[t]) == _brute_topk(lg[t], k)
+
+
+def test_softmax_weights_identity_and_sum():
+    rng = np.random.default_rng(7)
+    lg = rng.normal(0, 2, (50, 16)).astype(np.float32)
+    ids, w = oracle.topk(lg, 4, oracle.ROUTER_SOFTMAX, True)
+    full = np.exp(lg.astype(np.float64))
+    full /= full.sum(axis=1, keepdims=True)            # softmax over all experts
+    sel = np.take_along_axis(full, ids, axis=1)
+    np.testing.assert_allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-12)
+    ids2, w2 = oracle.topk(lg, 4, oracle.ROUTER_SOFTMAX, False)
+    np.testing.assert_allclose(w2, sel, rtol=1e-12)   # no renormalisation: plain softmax probs
+
+
+def test_sigmoid_weights():
+    rng = np.random.default_rng(8)
+    lg = rng.normal(0, 3, (50, 32)).astype(np.float32)
+    ids, w = oracle.topk(lg, 8, oracle.ROUTER_SIGMOID, True)
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg, ids, axis=1).astype(np.float64)))
+    np.testing.assert_allclose(w, s / s.sum(axis=1, keepdims=True), rtol=1e-12)
+    np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=1e-12)
+    _, w2 = oracle.topk(lg, 8, oracle.ROUTER_SIGMOID, False)
+    np.testing.assert_allclose(w2, s, rtol=1e-12)
+
+
+def test_group_is_a_stable_sort():
+    rng = np.random.default_rng(9)
+    for T, k, E in [(1, 1, 1), (7, 2, 5), (64, 8, 32), (300, 4, 7)]:
+        ids = np.stack([rng.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+        offsets, rows = oracle.group(ids, E)
+        flat = ids.ravel()
+        assert np.array_equal(rows, np.argsort(flat, kind="stable"))
+        assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(np.bincount(flat, minlength=E))]))
+
+
+def test_route_permutation_covers_every_pair_once():
+    rng = np.random.default_rng(10)
+    T, H, E, k = 33, 256, 9, 3
+    x = _bf16(rng.normal(0, 1, (T, H)))
+    w = rng.normal(0, H ** -0.5, (E, H)).astype(np.float32)
+    r = oracle.route(x, w, None, k, oracle.ROUTER_SOFTMAX)
+    assert sorted(r["sorted_rows"].tolist()) == list(range(T * k))
+    for e in range(E):
+        seg = r["sorted_rows"][r["offsets"][e]:r["offsets"][e + 1]]
+        assert np.all(r["ids"].ravel()[seg] == e)
+        assert np.all(np.diff(seg) > 0)
