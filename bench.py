@@ -1,0 +1,421 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE NVFP4 expert FFN (moe_forward) on GB300.
+
+One step = one moe_forward (route, group, [quantise], gate/up + SwiGLU, down +
+combine) over one batch of seeded synthetic input, inputs resident in HBM.
+Default workload: decode, 4 tokens, H 4096, 128 experts, I 1536, top-8, shared
+expert, W4A16, over the 10 seeded instances (seeds 0-9, each with its own
+weights); step i runs instance i mod 10, so consecutive steps never share
+weights and the touched weights (~0.3 GB a step, 13.6 GB in all) exceed L2.
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle instead.
+Multi-GPU: one process per GPU (torchrun), independent replicas, no collective
+on the data path; value = tokens of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import shutil
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np
+import torch
+
+import synth
+
+METRIC = "MoE NVFP4 expert-FFN tokens/s; decode HBM GB/s & prefill FP4 TFLOP/s % peak"
+PROJ = ("gate", "up", "down")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"], source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        if shutil.which("nvidia-smi") is None:
+            return
+        sel = str(device_index)
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            pass
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        self.f = open(self.path, "w")
+        self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
+                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                     stdout=self.f, stderr=subprocess.DEVNULL)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = [l.split(",") for l in open(self.path).read().strip().splitlines() if l.strip()]
+        os.unlink(self.path)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [c.strip() for c in r]
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- inputs
+
+class Instance:
+    """One seeded problem: device activations, router, NVFP4 weights."""
+
+    def __init__(self, moe, w, seed, batch=0):
+        self.seed, self.batch = seed, batch
+        self.x = synth.activations(w, seed, batch, device="cuda")
+        self.rw = synth.router_weight(w, seed, device="cuda")
+        self.bias = synth.router_bias(w, seed, device="cuda")
+
+
+def build_weights(moe, w, seed):
+    E, I, H = w.experts, w.inter, w.hidden
+    def alloc(n, rows, cols):
+        return moe.NvfpTensor(torch.empty(n, rows, cols // 2, dtype=torch.uint8, device="cuda"),
+                              torch.empty(n, rows, cols // 16, dtype=torch.uint8, device="cuda"),
+                              torch.empty(n, dtype=torch.float32, device="cuda"))
+    shapes = {"gate": (I, H), "up": (I, H), "down": (H, I)}
+    ts = {p: alloc(E, *shapes[p]) for p in PROJ}
+    for e in range(E):
+        for p in PROJ:
+            t = ts[p]
+            moe.quantize_nvfp4(synth.expert_weight(w, seed, e, p, device="cuda"),
+                               out=moe.NvfpTensor(t.codes[e:e + 1], t.scales[e:e + 1], t.ts[e:e + 1]))
+    routed = moe.ExpertSet(ts["gate"], ts["up"], ts["down"])
+    shared = None
+    if w.shared_inter:
+        shared = moe.ExpertSet(*[moe.quantize_nvfp4(synth.expert_weight(w, seed, "shared", p, device="cuda"))
+                                 for p in PROJ])
+    return routed, shared
+
+
+def algorithmic(w, ids_list):
+    """Per-step algorithmic bytes of the gate/up and down kernels and flops,
+    averaged over the instances (distinct experts touched come from routing)."""
+    H, I, Is, T, k = w.hidden, w.inter, w.shared_inter, w.tokens, w.top_k
+    wb = 9.0 / 16.0                                   # bytes per NVFP4 value (code nibble + 1/16 scale byte)
+    act = 2.0 if w.mode == "w4a16" else wb            # activation bytes per value
+    hb = 2.0 if w.mode == "w4a16" else 4.0            # SwiGLU output element as written
+    gu, dn, fl = [], [], []
+    for ids in ids_list:
+        d = len(np.unique(ids))
+        P = ids.size
+        rows_s = T if Is else 0
+        gu.append(d * 2 * I * H * wb + (2 * Is * H * wb if Is else 0) + T * H * act + (P * I + rows_s * Is) * hb)
+        dn.append(d * H * I * wb + (H * Is * wb if Is else 0) + (P * I + rows_s * Is) * (2.0 if w.mode == "w4a16" else wb)
+                  + T * H * 4)
+        fl.append(2.0 * 3 * H * (P * I + rows_s * Is))
+    return float(np.mean(gu)), float(np.mean(dn)), float(np.mean(fl)), float(np.mean([len(np.unique(i)) for i in ids_list]))
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+
+class OraclePrep:
+    """Host copies of one instance and the oracle's own quantisation of every
+    expert it touches (untimed preparation)."""
+
+    def __init__(self, w, inst):
+        import oracle
+        self.oracle, self.w = oracle, w
+        self.xb = inst.x.cpu().view(torch.int16).numpy().view(np.uint16)
+        self.rw = inst.rw.cpu().numpy()
+        self.bias = None if inst.bias is None else inst.bias.cpu().numpy()
+        self.kind = oracle.ROUTER_SIGMOID if w.router == "sigmoid" else oracle.ROUTER_SOFTMAX
+        self.mode = oracle.MODE_W4A4 if w.mode == "w4a4" else oracle.MODE_W4A16
+        self.route = oracle.route(self.xb, self.rw, self.bias, w.top_k, self.kind, w.renormalize)
+        need = sorted(set(int(e) for e in np.unique(self.route["ids"])))
+        self.packed = {e: tuple(oracle.quantize(synth.expert_weight(w, inst.seed, e, p, device="cuda").cpu().numpy())
+                                for p in PROJ) for e in need}
+        self.shared = None
+        if w.shared_inter:
+            self.shared = tuple(oracle.quantize(
+                synth.expert_weight(w, inst.seed, "shared", p, device="cuda").cpu().numpy()) for p in PROJ)
+        self.threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    def full(self):
+        """One complete oracle moe_forward of the batch."""
+        w = self.w
+        self.oracle.forward(self.xb, self.rw, self.bias, lambda e: self.packed[e], k=w.top_k,
+                            router_kind=self.kind, renormalize=w.renormalize, mode=self.mode, shared=self.shared)
+
+    def pairs(self):
+        """The (token, expert) pairs of the batch, then the shared expert's tokens."""
+        ids = self.route["ids"]
+        out = [(t, int(ids[t, j])) for t in range(ids.shape[0]) for j in range(ids.shape[1])]
+        if self.shared is not None:
+            out += [(t, "shared") for t in range(ids.shape[0])]
+        return out
+
+    def pair(self, t, e):
+        """One complete oracle call on a one-token, one-expert problem: FFN_e(x_t)."""
+        w = self.w
+        packed = self.shared if e == "shared" else self.packed[e]
+        self.oracle.forward(self.xb[t:t + 1], self.rw[:1], None, lambda _: packed, k=1, router_kind=self.kind,
+                            renormalize=w.renormalize, mode=self.mode)
+
+
+def oracle_baseline(w, inst, budget_s=15.0):
+    """CPU oracle on a bounded sample: repeated full moe_forward of one batch
+    (router, grouping, FP64 FFN of every touched expert), weights prepared."""
+    prep = OraclePrep(w, inst)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        prep.full()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el * (n + 1) / n > 2 * budget_s:
+            break
+    desc = (f"{n} complete oracle moe_forward(s) of seed {inst.seed} ({w.tokens} tokens, "
+            f"{len(prep.packed)} experts touched; FP64 numpy matmul, C router), {el:.1f} s")
+    return n * w.tokens / el, desc, prep.threads
+
+
+# ---------------------------------------------------------------- main arms
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world):
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_ours(args, w, world, rank, local):
+    import moe_routed_expert_router_gb300 as moe
+    moe.lib()
+    pk = peaks()
+    n_inst = len(w.seeds) if w.batches == 1 else 1
+    weights = {}
+    insts = []
+    if w.batches > 1:
+        weights[w.seeds[0]] = build_weights(moe, w, w.seeds[0])
+        insts = [Instance(moe, w, w.seeds[0], b) for b in range(w.batches)]
+    else:
+        for s in w.seeds:
+            weights[s] = build_weights(moe, w, s)
+            insts.append(Instance(moe, w, s))
+    plan = moe.Plan(w.hidden, w.inter, w.experts, w.top_k, w.tokens,
+                    router=moe.ROUTER_SIGMOID if w.router == "sigmoid" else moe.ROUTER_SOFTMAX,
+                    renormalize=w.renormalize, mode=moe.W4A4 if w.mode == "w4a4" else moe.W4A16,
+                    has_shared=w.shared_inter > 0, shared_inter=w.shared_inter)
+    ids_list = [plan.route(i.x, i.rw, i.bias)["topk_ids"].cpu().numpy() for i in insts]
+    gu_bytes, dn_bytes, flops, distinct = algorithmic(w, ids_list)
+    outs = [torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda") for _ in insts]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        j = i % len(insts)
+        r, s = weights[insts[j].seed]
+        plan.forward(insts[j].x, insts[j].rw, insts[j].bias, r, s, out=outs[j])
+
+    clk = ClockSampler(local)
+    for i in range(args.warmup):
+        step(i)
+    st = plan.sync_status()
+    if st != moe.OK:
+        raise SystemExit(f"moe_forward failed: {moe.STATUS[st]}")
+    plan.read_profile()
+    plan.set_profiling(True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = t0.elapsed_time(t1)
+    prof = plan.read_profile()
+    plan.set_profiling(False)
+    st = plan.sync_status()
+    if st != moe.OK:
+        raise SystemExit(f"moe_forward failed: {moe.STATUS[st]}")
+    ms = max_over_ranks(ms, world)
+
+    # end to end through the host-buffer entry point: H2D of x + D2H of out each step
+    xh = [i.x.cpu().pin_memory() for i in insts]
+    oh = torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16).pin_memory()
+
+    def step_host(i):
+        j = i % len(insts)
+        r, s = weights[insts[j].seed]
+        plan.forward_host(xh[j], insts[j].rw, insts[j].bias, r, s, oh)
+
+    for i in range(args.warmup):
+        step_host(i)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step_host(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    clocks = clk.stop()
+
+    tokens = world * args.steps * w.tokens
+    value = tokens / (ms / 1e3)
+    # dominant kernel by measured stage time
+    stage_ms = {k: v[0] for k, v in prof.items() if v[2] > 0}
+    dom = max(stage_ms, key=stage_ms.get)
+    per_launch = {k: prof[k][0] / prof[k][2] for k in stage_ms}
+    alg = {"gate_up": gu_bytes, "down": dn_bytes}
+    roof = None
+    if dom in alg:
+        ach = alg[dom] / (per_launch[dom] / 1e3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+                "peak_source": pk["source"], "algorithmic_bytes_per_launch": round(alg[dom]),
+                "avg_launch_us": round(per_launch[dom] * 1e3, 2)}
+    launches = sum(v[1] for v in prof.values())
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp32" if w.mode == "w4a16" else "fp4xfp4->fp32",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to NVFP4 on device)",
+        "config": {"workload": w.name, "description": w.description, "tokens": w.tokens, "hidden": w.hidden,
+                   "experts": w.experts, "inter": w.inter, "top_k": w.top_k, "shared_inter": w.shared_inter,
+                   "mode": w.mode, "router": w.router, "instances": len(insts),
+                   "l2": "inputs larger than L2: step i runs instance i mod %d with its own weights" % len(insts),
+                   "parallelism": f"replicas x{world}", "distinct_experts_per_step": distinct},
+        "e2e": {"value": round(tokens / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": w.tokens * w.hidden * 2, "d2h_bytes_per_step": w.tokens * w.hidden * 2},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "stages_us_per_step": {k: round(v * 1e3 / args.steps, 2) for k, v in stage_ms.items()},
+        "hbm_gbs_whole_step": round((gu_bytes + dn_bytes) / (ms / args.steps / 1e3) / 1e9, 1),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, desc, thr = oracle_baseline(w, insts[0], args.cpu_budget)
+        res["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                               "sample": desc}
+    plan.close()
+    return res
+
+
+def run_reference(args, w, world, rank):
+    """The oracle as it stands, on the host cores.  One step = one complete
+    oracle call on one (token, expert) pair of the workload's first batch
+    (cycling through the batch's routed pairs and shared-expert rows);
+    tokens/s = steps / pairs-per-token / time."""
+    if rank != 0:
+        return None
+    inst = Instance(None, w, w.seeds[0])
+    prep = OraclePrep(w, inst)
+    pairs = prep.pairs()
+    for i in range(args.warmup):
+        prep.pair(*pairs[i % len(pairs)])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        prep.pair(*pairs[i % len(pairs)])
+    el = time.perf_counter() - t0
+    per_token = w.top_k + (1 if w.shared_inter else 0)
+    v = args.steps / per_token / el
+    desc = (f"each step one oracle FFN call on one (token, expert) pair of seed {w.seeds[0]} "
+            f"({per_token} pairs a token); {args.steps} steps in {el:.1f} s")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name, "tokens": w.tokens},
+            "cpu_baseline": {"value": round(v, 4), "unit": "tokens/s", "cores": prep.threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            torch.cuda.set_device(0) if torch.cuda.is_available() else None
+            res = run_reference(args, w, world, rank)
+            print(json.dumps(res), flush=True)
+        return
+    world, rank, local = dist_init()
+    res = run_ours(args, w, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

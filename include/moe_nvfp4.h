@@ -1,0 +1,215 @@
+/*
+ * moe_nvfp4.h -- C ABI of the routed mixture-of-experts FFN over NVFP4
+ * weights, for one NVIDIA GB300 (sm_103a).
+ *
+ * What it computes, for every token t of a batch x[T][H]:
+ *
+ *   out[t] = sum_{j<k} w[t][j] * FFN_{id[t][j]}(x_t)   (+ FFN_shared(x_t))
+ *   FFN_e(v) = Wd_e ( silu(Wg_e v) * (Wu_e v) ),   silu(z) = z / (1 + e^-z)
+ *
+ * with the router choosing id[t][*] and w[t][*] (softmax or sigmoid, top-k,
+ * renormalised) and every weight W = E2M1(code) * E4M3(block scale) *
+ * tensor_scale.  Sources (page title, section):
+ *   "NVIDIA FP4-Local checkpoints on DGX Spark (TP=1, TP=2) ... #565",
+ *   section 4 Round 1: NVFP4 weights as U8 codes and F8_E4M3 scales held as
+ *   stored (#489); routed experts with a gate, up and down product and one
+ *   tensor scale an expert (#517, #545); a whole batch routed in one run so
+ *   each expert is read once (#740); gate, up and SwiGLU in one launch (#766);
+ *   W4A16 / W4A4 activation formats (#687, list of formats at the end of the
+ *   section); the SwiGLU output quantised for the down product (#760); down
+ *   rows in BF16 rounded to nearest even (#914); the combine folded into the
+ *   card sum (#701); the shared expert beside the routed ones (#686);
+ *   router logits in fp32 (#763).  "bloomery 0.3.9", From our contributors:
+ *   the router's normalisation policy is a named value (#772).
+ *
+ * Formats (the pages name them; the bit layouts are the OCP Microscaling ones):
+ *   - NVFP4 tensor W[N][K]: codes uint8[N][K/2], element 2i in bits 0..3 and
+ *     element 2i+1 in bits 4..7; scales uint8[N][K/16], one E4M3 byte per 16
+ *     consecutive K values, row-major; one fp32 tensor scale.
+ *   - E2M1: sign bit 3, magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6}.
+ *   - E4M3 ("FN"): bias 7, max 448, 0x7F/0xFF NaN, no infinities.
+ *   - NVFP4 quantiser (weights and W4A4 activations), fp32 arithmetic:
+ *       ts = amax / 2688;  s = E4M3_rne_sat((block_amax / 6) / ts);
+ *       code = E2M1_rne_sat(x / (E4M3(s) * ts)).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is DEVICE memory unless its comment says host;
+ *     the caller owns it.  Pointers must be 16-byte aligned
+ *     (MOE_ERR_MISALIGNED otherwise).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream).  No call below allocates or synchronises
+ *     except moe_plan_create / moe_plan_destroy / moe_plan_sync_status.
+ *   - Host-side checks return an error at once and launch nothing.  Errors
+ *     found on the device (a non-finite activation, a wait that ran out) set
+ *     the plan's error word, which moe_plan_sync_status returns; outputs are
+ *     unspecified after a device error.
+ *   - A plan is used by one stream at a time.
+ */
+#ifndef MOE_NVFP4_H
+#define MOE_NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, T > max_tokens ... */
+    MOE_ERR_UNSUPPORTED_SHAPE = 2, /* H or I not a multiple of 256/128, k > E ... */
+    MOE_ERR_MISALIGNED = 3,        /* a pointer not 16-byte aligned */
+    MOE_ERR_NONFINITE = 4,         /* device: an activation is NaN or infinite */
+    MOE_ERR_TIMEOUT = 5,           /* device: a bounded wait ran out */
+    MOE_ERR_CUDA = 6,              /* a CUDA runtime call failed */
+    MOE_ERR_OOM = 7,               /* moe_plan_create could not allocate */
+    MOE_ERR_DEVICE = 8             /* device: an internal check failed */
+} moe_status;
+
+typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router_kind;
+
+/* W4A16: activations stay bf16; the SwiGLU output is rounded to bf16 (RNE)
+ *        before the down product.
+ * W4A4:  activations are NVFP4-quantised (tensor scale from the batch amax);
+ *        the SwiGLU output of all routed rows is rounded to fp32 and
+ *        NVFP4-quantised with the tensor scale from its own batch amax (the
+ *        shared expert's with its own). */
+typedef enum { MOE_W4A16 = 0, MOE_W4A4 = 1 } moe_mode;
+
+typedef struct {
+    int32_t hidden;       /* H: multiple of 256, at most 8192 */
+    int32_t inter;        /* I: per-expert intermediate, multiple of 128, at most 8192 */
+    int32_t num_experts;  /* E: 1..1024 */
+    int32_t top_k;        /* k: 1..min(E, 32) */
+    int32_t max_tokens;   /* largest T a call may pass (sizes the workspace) */
+    int32_t router;       /* moe_router_kind */
+    int32_t renormalize;  /* 1: weights renormalised over the top-k; 0: not */
+    int32_t mode;         /* moe_mode */
+    int32_t has_shared;   /* 1: a shared expert is added to every token */
+    int32_t shared_inter; /* shared expert's intermediate (multiple of 128, at most 8192) */
+} moe_config;
+
+/* One NVFP4 weight stacked over `count` experts: codes [count][N][K/2],
+ * scales [count][N][K/16], tensor_scale [count] (all device memory). */
+typedef struct {
+    const uint8_t *codes;
+    const uint8_t *scales;
+    const float *tensor_scale;
+} moe_nvfp4;
+
+/* gate and up are [I][H]; down is [H][I].  For the routed set count = E; for
+ * the shared expert count = 1 and I = shared_inter. */
+typedef struct {
+    moe_nvfp4 gate, up, down;
+} moe_expert_set;
+
+typedef struct moe_plan_s *moe_plan;
+
+/* Validate `cfg` (host memory), then allocate the plan and its device
+ * workspace on the current device for cfg->max_tokens tokens.  *out receives
+ * the plan (NULL on error).  This and moe_plan_set_profiling are the only
+ * calls that allocate. */
+moe_status moe_plan_create(const moe_config *cfg, moe_plan *out);
+
+/* Free the plan and its workspace (synchronises the device first). */
+moe_status moe_plan_destroy(moe_plan plan);
+
+/* Router + grouping only (the steps "route" and "group by expert").
+ *   x_bf16      [T][H] bf16 activations
+ *   router_w    [E][H] fp32
+ *   router_bias [E] fp32 or NULL; added to the logits, so it moves both the
+ *               selection and the weights
+ * Outputs (device, caller-owned):
+ *   topk_ids       [T][k] int32, experts by decreasing logit, ties -> lower id
+ *   topk_w         [T][k] fp32 routing weights
+ *   expert_offsets [E+1] int32, exclusive prefix of per-expert pair counts
+ *   sorted_rows    [T*k] int32, pair indices t*k+j grouped by expert, each
+ *                  expert's pairs in increasing t*k+j
+ * Logits are fp32 with a fixed order: position h of the H dimension belongs to
+ * lane (h/8) mod 32, each lane sums fmaf in increasing h from +0, the 32 lane
+ * sums are combined by an xor butterfly over offsets 16, 8, 4, 2, 1, and the
+ * bias is added last.  Indices and offsets are therefore reproducible bit for
+ * bit. */
+moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w,
+                     const float *router_bias, int32_t *topk_ids, float *topk_w,
+                     int32_t *expert_offsets, int32_t *sorted_rows, void *stream);
+
+/* The whole MoE FFN: route, group, [W4A4: quantise x], permute, gate/up +
+ * SwiGLU, down with the routing weight, combine, [+ shared expert], bf16 out.
+ *   routed: E experts' NVFP4 gate/up/down (host struct of device pointers)
+ *   shared: NULL, or the shared expert (count 1) when cfg.has_shared
+ *   out_bf16 [T][H] bf16, written with one round-to-nearest-even of the fp32
+ *            sum.  T = 0 is a no-op. */
+moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w,
+                       const float *router_bias, const moe_expert_set *routed,
+                       const moe_expert_set *shared, void *out_bf16, void *stream);
+
+/* moe_forward with HOST activations and output: copies x (host, ideally
+ * pinned) to the plan's device staging buffer, runs moe_forward, and copies
+ * the result back to out_bf16_host.  The weights stay device pointers.
+ * The copies are ordered on `stream`; the call returns before they finish
+ * (synchronise the stream before reading out_bf16_host). */
+moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, const float *router_w,
+                            const float *router_bias, const moe_expert_set *routed,
+                            const moe_expert_set *shared, void *out_bf16_host, void *stream);
+
+/* W4A4 activation quantisation on its own (the step moe_forward runs first in
+ * W4A4): tensor scale from the amax of all of x[T][H], then per 16-block
+ * E4M3 scales and E2M1 codes.
+ *   codes [T][H/2], scales [T][H/16], tensor_scale [1] fp32 (device). */
+moe_status moe_quantize_act(moe_plan plan, const void *x_bf16, int32_t T, uint8_t *codes,
+                            uint8_t *scales, float *tensor_scale, void *stream);
+
+/* NVFP4 quantisation of fp32 weights w[batch][rows][cols] (device), one
+ * tensor scale per batch item (amax of that item / 2688).  Writes codes
+ * [batch][rows][cols/2], scales [batch][rows][cols/16], tensor_scale [batch].
+ * cols must be a multiple of 16.  Needs no plan and no workspace:
+ * tensor_scale doubles as the amax accumulator while the call runs. */
+moe_status moe_quantize_nvfp4(const float *w, int32_t batch, int32_t rows, int32_t cols,
+                              uint8_t *codes, uint8_t *scales, float *tensor_scale, void *stream);
+
+/* Synchronise `stream`, then return and clear the plan's device error word
+ * (MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE). */
+moe_status moe_plan_sync_status(moe_plan plan, void *stream);
+
+/* Device address and size of a plan workspace buffer, for tests that check a
+ * step in isolation.  name: "h_codes", "h_scales", "h_ts", "x_ts", "acc",
+ * "counts", "padded_offsets".  Returns MOE_ERR_INVALID_ARG for an unknown name. */
+moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
+
+/* Stages of moe_forward, for moe_plan_read_profile. */
+typedef enum {
+    MOE_STAGE_ROUTE = 0,      /* logits + top-k (2 kernels) */
+    MOE_STAGE_GROUP = 1,      /* histogram scan, stable placement, work lists */
+    MOE_STAGE_QUANT_X = 2,    /* W4A4 activation quantisation */
+    MOE_STAGE_PERMUTE = 3,    /* gather of activations into per-expert tiles */
+    MOE_STAGE_GATE_UP = 4,    /* gate + up + SwiGLU */
+    MOE_STAGE_QUANT_H = 5,    /* W4A4 quantisation of the SwiGLU output */
+    MOE_STAGE_DOWN = 6,       /* down + routing weight + scatter-add */
+    MOE_STAGE_FINALIZE = 7,   /* bf16 write of the combine */
+    MOE_NUM_STAGES = 8
+} moe_stage;
+
+/* Turn per-stage timing on (1) or off (0).  While on, moe_forward records a
+ * CUDA event pair on its stream around every stage (events come from a pool
+ * the plan allocates here) and counts the kernels it launches. */
+moe_status moe_plan_set_profiling(moe_plan plan, int32_t enable);
+
+/* Synchronise the device, then add into ms[MOE_NUM_STAGES] the summed event
+ * time of every stage recorded since the last read, and into
+ * launches[MOE_NUM_STAGES] / calls[MOE_NUM_STAGES] the kernels launched and
+ * the stage executions; clears the record.  Host arrays; any may be NULL. */
+moe_status moe_plan_read_profile(moe_plan plan, float *ms, int64_t *launches, int64_t *calls);
+
+/* Text of a status code (static storage). */
+const char *moe_status_string(moe_status s);
+
+/* Library version string (static storage). */
+const char *moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_NVFP4_H */

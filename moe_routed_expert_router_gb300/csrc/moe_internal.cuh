@@ -1,0 +1,192 @@
+// Internal declarations of the GB300 MoE NVFP4 library (device side and plan).
+// Nothing here is part of the C ABI; see include/moe_nvfp4.h.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_nvfp4.h"
+
+namespace moe {
+
+// Rows of every expert's segment in the permuted activation / SwiGLU buffers
+// are padded to this multiple, so a 128-row tensor-core tile never mixes experts.
+constexpr int kTileRows = 128;
+// Tokens of one expert handled together by the CUDA-core (decode-shaped) kernels.
+constexpr int kChunkRows = 4;
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopK = 32;
+
+// Device error bits (plan error word).
+constexpr int kErrNonFinite = 1;
+constexpr int kErrTimeout = 2;
+constexpr int kErrDevice = 4;
+
+// Per-call scratch words, cleared by one memset at the start of every call.
+struct CallScratch {
+    unsigned int x_amax;        // fp32 bits of amax|x| (W4A4)
+    unsigned int h_amax;        // fp32 bits of amax|h| over routed rows (W4A4)
+    unsigned int hs_amax;       // same for the shared expert's rows
+    int n_chunks;               // CUDA-core work chunks
+    int n_tiles;                // tensor-core tiles (gate/up)
+    int n_active;               // experts with at least one pair
+    int pad[2];
+};
+
+struct Plan {
+    moe_config cfg;
+    int device = 0;
+    int num_sms = 0;
+    int64_t pairs_max = 0;      // max_tokens * k
+    int64_t rows_pad_max = 0;   // padded permuted rows (routed + shared)
+    int64_t chunks_max = 0;
+
+    void *ws = nullptr;
+    size_t ws_bytes = 0;
+
+    float *logits = nullptr;        // [Tmax][E]
+    int32_t *ids = nullptr;         // [P]
+    float *wts = nullptr;           // [P]
+    int32_t *counts = nullptr;      // [E]
+    int32_t *offsets = nullptr;     // [E+2]
+    int32_t *poff = nullptr;        // [E+2] padded offsets; index E = shared segment
+    int32_t *sorted = nullptr;      // [P]
+    int32_t *inv = nullptr;         // [P] pair -> padded row
+    int32_t *pad_pair = nullptr;    // [rows_pad] pair at a padded row (-1 pad, >= P shared token)
+    int4 *chunks = nullptr;         // [chunks_max] {expert, first padded row, rows, 0}
+    CallScratch *scratch = nullptr;
+    float *xts = nullptr;           // [2] x tensor scale, spare
+    uint8_t *xq = nullptr;          // [Tmax][H/2]
+    uint8_t *xsc = nullptr;         // [Tmax][H/16]
+    float *hbuf = nullptr;          // [rows_pad][Imax] fp32 (W4A4) or bf16 (W4A16)
+    uint8_t *hq = nullptr;          // [rows_pad][Imax/2]
+    uint8_t *hsc = nullptr;         // [rows_pad][Imax/16]
+    float *hts = nullptr;           // [2] h tensor scales (routed, shared)
+    float *acc = nullptr;           // [Tmax][H] fp32 combine accumulator, kept zero between calls
+    int *err = nullptr;             // device error word
+    void *x_stage = nullptr;        // [Tmax][H] bf16 (moe_forward_host)
+    void *out_stage = nullptr;      // [Tmax][H] bf16
+};
+
+// ------------------------------------------------------------- conversions
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Two E2M1 codes (one byte; element 0 in the low nibble) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n\t}" : "=r"(out) : "r"(byte));
+    return out;
+}
+
+// Four E2M1x2 bytes of a word -> four f16x2 words (exact).
+__device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// Two E4M3 bytes (low byte = first) -> f16x2 (exact: E4M3 fits f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 h;\n\tcvt.u16.u32 h, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;\n\t}" : "=r"(out) : "r"(two_bytes));
+    return out;
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint32_t byte) {
+    uint32_t h2 = e4m3x2_to_f16x2(byte & 0xFFu);
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+}
+
+// fp32 >= 0 -> E4M3 byte, round to nearest even, saturating at 448.
+__device__ __forceinline__ uint32_t f32_to_e4m3_sat(float v) {
+    uint32_t out;
+    asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
+        : "=r"(out) : "f"(v), "f"(0.0f));
+    return out & 0xFFu;
+}
+
+// Two fp32 -> one byte of two E2M1 codes (lo -> bits 0..3, hi -> bits 4..7),
+// round to nearest even, saturating at +-6.
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float lo, float hi) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b;\n\tcvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\tcvt.u32.u8 %0, b;\n\t}"
+        : "=r"(out) : "f"(lo), "f"(hi));
+    return out & 0xFFu;
+}
+
+// NVFP4 quantisation of one 16-value block with tensor scale ts, in the
+// fixed fp32 order: s = E4M3((amax/6)/ts); den = E4M3(s)*ts; code = E2M1(v/den).
+__device__ __forceinline__ void quant_block16(const float (&v)[16], float ts, uint2 &codes, uint32_t &scale) {
+    float bamax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) bamax = fmaxf(bamax, fabsf(v[i]));
+    uint32_t s = 0;
+    if (ts != 0.0f) s = f32_to_e4m3_sat(__fdiv_rn(__fdiv_rn(bamax, 6.0f), ts));
+    const float den = __fmul_rn(e4m3_to_f32(s), ts);
+    uint32_t b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        b[i] = (den == 0.0f) ? 0u : f32x2_to_e2m1x2(__fdiv_rn(v[2 * i], den), __fdiv_rn(v[2 * i + 1], den));
+    }
+    codes.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+    codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+    scale = s;
+}
+
+__device__ __forceinline__ void atomic_max_nonneg(unsigned int *addr, float v) {
+    atomicMax(addr, __float_as_uint(v));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+
+// ------------------------------------------------------------ launchers
+
+struct ExpertPtrs {
+    const uint8_t *gc, *gs, *uc, *us, *dc, *ds;
+    const float *gts, *uts, *dts;
+};
+
+cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias,
+                          int32_t *ids, float *wts, cudaStream_t st);
+cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out,
+                         int32_t *sorted_out, bool build_work, cudaStream_t st);
+cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes, uint8_t *scales,
+                             float *ts_out, bool amax_ready, cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const float *w, int batch, int rows, int cols, uint8_t *codes, uint8_t *scales,
+                               float *ts, cudaStream_t st);
+// part 0: gate + up + SwiGLU; part 1: down + routing weight + scatter-add.
+cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtrs &routed,
+                            const ExpertPtrs *shared, int part, cudaStream_t st);
+cudaError_t launch_quant_h(const Plan &p, cudaStream_t st);
+cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st);
+
+}  // namespace moe

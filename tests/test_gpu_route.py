@@ -1,0 +1,81 @@
+"""moe_route against the oracle: top-k ids, expert offsets and the grouped
+order bit for bit, routing weights within a few fp32 ulps (expf vs exp)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import moe_routed_expert_router_gb300 as moe
+from helpers import plan_for
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(w, x, rw, bias):
+    with plan_for(w, max_tokens=max(1, x.shape[0])) as plan:
+        r = plan.route(x, rw, bias)
+        assert plan.sync_status() == moe.OK
+    xb = x.cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.route(xb, rw.cpu().numpy(), None if bias is None else bias.cpu().numpy(), w.top_k,
+                       oracle.ROUTER_SIGMOID if w.router == "sigmoid" else oracle.ROUTER_SOFTMAX, w.renormalize)
+    np.testing.assert_array_equal(r["topk_ids"].cpu().numpy(), ref["ids"])
+    np.testing.assert_array_equal(r["expert_offsets"].cpu().numpy(), ref["offsets"])
+    np.testing.assert_array_equal(r["sorted_rows"].cpu().numpy()[:ref["sorted_rows"].size], ref["sorted_rows"])
+    np.testing.assert_allclose(r["topk_w"].cpu().numpy(), ref["weights"], rtol=2e-6, atol=1e-7)
+    return ref
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_route_full_size(name):
+    w = synth.WORKLOADS[name]
+    for seed in w.seeds[:2]:
+        ref = _check(w, synth.activations(w, seed, device="cuda"), synth.router_weight(w, seed, "cuda"),
+                     synth.router_bias(w, seed, "cuda"))
+        assert np.all(np.diff(ref["offsets"]) >= 0)
+
+
+@pytest.mark.parametrize("T", [1, 3, 37, 130])
+def test_route_ragged_token_counts(T):
+    w = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=T, hidden=1024, experts=64)
+    _check(w, synth.activations(w, 7, device="cuda"), synth.router_weight(w, 7, "cuda"), synth.router_bias(w, 7, "cuda"))
+
+
+def test_route_ties_go_to_the_lower_expert():
+    w = synth.scaled(synth.WORKLOADS["tiny_w4a16"], tokens=40, experts=16, top_k=4)
+    rw = synth.router_weight(w, 1, "cuda")
+    rw[5] = rw[2]; rw[9] = rw[2]; rw[14] = rw[3]       # identical rows -> exactly equal logits
+    ref = _check(w, synth.activations(w, 1, device="cuda"), rw, None)
+    ids = ref["ids"]
+    for t in range(ids.shape[0]):
+        pos = {e: j for j, e in enumerate(ids[t])}
+        for lo, hi in ((2, 5), (5, 9), (3, 14)):
+            if lo in pos and hi in pos:
+                assert pos[lo] < pos[hi]
+
+
+@pytest.mark.parametrize("kind,renorm", [("softmax", False), ("sigmoid", False), ("sigmoid", True)])
+def test_route_normalisation_policies(kind, renorm):
+    w = synth.scaled(synth.WORKLOADS["decode4_w4a16"], tokens=20, router=kind, renormalize=renorm)
+    _check(w, synth.activations(w, 2, device="cuda"), synth.router_weight(w, 2, "cuda"), None)
+
+
+def test_route_k_equals_e_and_single_expert():
+    for E, k in ((8, 8), (1, 1)):
+        w = synth.scaled(synth.WORKLOADS["tiny_w4a16"], experts=E, top_k=k)
+        _check(w, synth.activations(w, 3, device="cuda"), synth.router_weight(w, 3, "cuda"), None)
+
+
+def test_nonfinite_activation_is_refused():
+    w = synth.WORKLOADS["tiny_w4a16"]
+    x = synth.activations(w, 0, device="cuda")
+    x[3, 17] = float("nan")
+    with plan_for(w) as plan:
+        plan.route(x, synth.router_weight(w, 0, "cuda"))
+        assert plan.sync_status() == moe.ERR_NONFINITE
+        x[3, 17] = float("inf")
+        plan.route(x, synth.router_weight(w, 0, "cuda"))
+        assert plan.sync_status() == moe.ERR_NONFINITE
+        x[3, 17] = 0.0
+        plan.route(x, synth.router_weight(w, 0, "cuda"))
+        assert plan.sync_status() == moe.OK
