@@ -15,6 +15,8 @@ Two halves:
         FFN_e(v) = Wd_e ( silu(Wg_e v) * (Wu_e v) ),   silu(z) = z / (1 + e^-z)
 
     with every weight dequantised as E2M1(code) * E4M3(scale) * tensor_scale.
+    The SwiGLU output enters the down product rounded as the mode says: to
+    bf16 (W4A16) or NVFP4 with its batch tensor scale (W4A4).
 
 Sources (page title, section): "NVIDIA FP4-Local checkpoints on DGX Spark ...
 #565", section 4 Round 1 -- gate, up and SwiGLU of the routed experts (#766),
@@ -277,6 +279,12 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         _, _, (dc, ds, dts) = weights
         return h @ dequantize(dc, ds, dts).T
 
+    def round_h_bf16(h):
+        """W4A16: the SwiGLU output is rounded to bf16 (nearest even) before the
+        down product ("down rows in BF16, the product rounding each to nearest
+        even", page 3 section 4, #914)."""
+        return bf16_to_f64(f64_to_bf16(h))
+
     def quant_h(h_all):
         """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax."""
         h32 = [h.astype(np.float32) for h in h_all]
@@ -294,6 +302,8 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         qh, ts_h = quant_h([hs[e] for e in active])
         hs = dict(zip(active, qh))
         res["h_ts"] = ts_h
+    else:
+        hs = {e: round_h_bf16(h) for e, h in hs.items()}
     if keep:
         res["h"] = hs
     for e in active:
@@ -306,6 +316,8 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         if mode == MODE_W4A4:
             (hsh,), ts_s = quant_h([hsh])
             res["shared_h_ts"] = ts_s
+        else:
+            hsh = round_h_bf16(hsh)
         out += down_part(shared, hsh)
 
     res["out"] = out

@@ -6,6 +6,13 @@ import math
 import numpy as np
 
 import oracle
+from test_oracle_codecs import _bf16_brute
+
+
+def _bf16(v):
+    """bf16 value nearest to v (exact rational rounding, ties to even)."""
+    b = _bf16_brute(float(v))
+    return float(np.array([b << 16], np.uint32).view(np.float32)[0])
 
 
 def _packed(rows, cols, entries, scale=0x38, ts=1.0, block_scales=None):
@@ -38,8 +45,8 @@ def test_hand_worked_one_token_two_experts():
     e1 = math.e / (1 + math.e)
     e0 = 1 / (1 + math.e)
     np.testing.assert_allclose(r["weights"][0], [e1, e0], rtol=1e-15)
-    h0 = 3 * 2 / (1 + math.exp(-2))
-    h1 = 2 * (-1) / (1 + math.exp(1))
+    h0 = _bf16(3 * 2 / (1 + math.exp(-2)))      # W4A16: SwiGLU output rounded to bf16
+    h1 = _bf16(2 * (-1) / (1 + math.exp(1)))
     want = np.zeros(H)
     want[0] = e0 * 2 * h0
     want[1] = e0 * -1 * h0
@@ -67,7 +74,7 @@ def test_single_expert_is_a_dense_swiglu_mlp():
         for i in range(I):
             g = sum(Wg[i][j] * xs[t][j] for j in range(H))
             u = sum(Wu[i][j] * xs[t][j] for j in range(H))
-            h.append(g / (1 + math.exp(-g)) * u)
+            h.append(_bf16(g / (1 + math.exp(-g)) * u))
         for j in range(H):
             y = sum(Wd[j][i] * h[i] for i in range(I))
             assert abs(r["out"][t][j] - y) <= 1e-12 * (1 + abs(y))
