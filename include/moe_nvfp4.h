@@ -178,6 +178,17 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream);
  * "counts", "padded_offsets".  Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 
+/* Expert-FFN implementation moe_forward uses: AUTO picks the tensor-core
+ * grouped GEMMs (tcgen05) for W4A4 batches of 64 or more (token, expert)
+ * pairs when the shapes allow (H, I multiples of 256) and the CUDA-core
+ * weight-streaming kernels otherwise.  Both compute the same function. */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_CUDA_CORE = 1, MOE_PATH_TENSOR_CORE = 2 } moe_path;
+
+/* Select the expert-FFN implementation for later calls on this plan.
+ * MOE_ERR_UNSUPPORTED_SHAPE if MOE_PATH_TENSOR_CORE is asked for a plan whose
+ * mode or shapes it does not cover. */
+moe_status moe_plan_set_path(moe_plan plan, int32_t path);
+
 /* Stages of moe_forward, for moe_plan_read_profile. */
 typedef enum {
     MOE_STAGE_ROUTE = 0,      /* logits + top-k (2 kernels) */

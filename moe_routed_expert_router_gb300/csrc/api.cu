@@ -10,7 +10,6 @@
 #include "moe_internal.cuh"
 
 namespace moe {
-cudaError_t launch_quant_h(const Plan &p, cudaStream_t st);
 size_t group_smem_bytes(int E);
 cudaError_t configure_group_kernel(int E);
 cudaError_t configure_tc(const Plan &p);
@@ -23,6 +22,7 @@ using moe::Plan;
 
 struct moe_plan_s {
     Plan p;
+    int path = MOE_PATH_AUTO;
     // per-stage timing (moe_plan_set_profiling)
     bool prof = false;
     std::vector<cudaEvent_t> pool;
@@ -103,6 +103,10 @@ void carve(Plan &p, Carver &c) {
     p.inv = c.take<int32_t>(sizeof(int32_t) * p.pairs_max);
     p.pad_pair = c.take<int32_t>(sizeof(int32_t) * p.rows_pad_max);
     p.chunks = c.take<int4>(sizeof(int4) * p.chunks_max);
+    p.tiles = c.take<int4>(sizeof(int4) * p.tiles_max);
+    p.xp = c.take<uint8_t>(p.rows_pad_max * H / 2);
+    p.xp_atoms = c.take<uint8_t>(p.rows_pad_max * H / 16);
+    p.hq_atoms = c.take<uint8_t>(p.rows_pad_max * Imax / 16);
     p.xts = c.take<float>(64);
     p.xq = c.take<uint8_t>(T * H / 2);
     p.xsc = c.take<uint8_t>(T * H / 16);
@@ -170,15 +174,16 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     moe::ExpertPtrs r = ptrs(*routed), sh{};
     if (shared) sh = ptrs(*shared);
     const moe::ExpertPtrs *shp = shared ? &sh : nullptr;
-    const bool tc = moe::tc_supported(p) && T * p.cfg.top_k >= 64;
+    const bool tc = plan->path == MOE_PATH_TENSOR_CORE ||
+                    (plan->path == MOE_PATH_AUTO && moe::tc_supported(p) && T * p.cfg.top_k >= 64);
     {
         Stage s(plan, MOE_STAGE_GATE_UP, st);
         e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
-        if (s.done(e, 1) != cudaSuccess) return MOE_ERR_CUDA;
+        if (s.done(e, tc ? 2 : 1) != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (p.cfg.mode == MOE_W4A4) {
         Stage s(plan, MOE_STAGE_QUANT_H, st);
-        if (s.done(moe::launch_quant_h(p, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
+        if (s.done(moe::launch_quant_h(p, tc, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
     }
     {
         Stage s(plan, MOE_STAGE_DOWN, st);
@@ -228,7 +233,9 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
     p.pairs_max = T * cfg->top_k;
     p.rows_pad_max = p.pairs_max + std::min<int64_t>(E, p.pairs_max) * (moe::kTileRows - 1) +
                      (cfg->has_shared ? (T + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows : 0);
+    p.rows_pad_max = (p.rows_pad_max + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows;
     p.chunks_max = p.pairs_max / moe::kChunkRows + E + 2 + (cfg->has_shared ? T / moe::kChunkRows + 1 : 0);
+    p.tiles_max = p.pairs_max / moe::kTileRows + E + 2 + (cfg->has_shared ? T / moe::kTileRows + 1 : 0);
     Carver dry;
     carve(p, dry);
     p.ws_bytes = dry.off + 256;
@@ -250,6 +257,13 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
         return MOE_ERR_CUDA;
     }
     *out = plan;
+    return MOE_OK;
+}
+
+moe_status moe_plan_set_path(moe_plan plan, int32_t path) {
+    if (!plan || path < MOE_PATH_AUTO || path > MOE_PATH_TENSOR_CORE) return MOE_ERR_INVALID_ARG;
+    if (path == MOE_PATH_TENSOR_CORE && !moe::tc_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    plan->path = path;
     return MOE_OK;
 }
 
@@ -348,10 +362,10 @@ moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, c
 
 moe_status moe_quantize_act(moe_plan plan, const void *x_bf16, int32_t T, uint8_t *codes, uint8_t *scales,
                             float *tensor_scale, void *stream) {
-    moe_status st = check_call(plan, x_bf16, T, nullptr, nullptr);
-    if (st != MOE_OK) return st;
+    if (!plan || T < 0 || T > plan->p.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
-    if (!codes || !scales || !tensor_scale) return MOE_ERR_INVALID_ARG;
+    if (!x_bf16 || !codes || !scales || !tensor_scale) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x_bf16)) return MOE_ERR_MISALIGNED;
     if (!aligned16(codes) || !aligned4(tensor_scale)) return MOE_ERR_MISALIGNED;
     Plan &p = plan->p;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

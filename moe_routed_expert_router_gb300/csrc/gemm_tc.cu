@@ -1,12 +1,568 @@
-// Tensor-core (tcgen05) grouped expert GEMMs.
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05), NVFP4 x
+// NVFP4 with E4M3 block scales (kind::mxf4nvf4, 16-value scale blocks), fp32
+// accumulators in tensor memory, operands brought in by TMA.
+//
+// "NVIDIA FP4-Local checkpoints on DGX Spark ... #565", section 4 Round 1:
+// the routed NVFP4 prompt GEMM runs on the FP4 tensor cores with 4-bit
+// activations (#687); gate, up and SwiGLU run as one launch (#766); the GEMM
+// store scales each slot by its expert's tensor scale (#545); the operands are
+// copied through a multi-stage pipeline in K steps (#822); the combine is folded
+// into the down product's store (#701).
+//
+// Layout (swap-AB): A = expert weight rows (M = 128 features per MMA), B = the
+// expert's token rows (N = 128), K along the hidden / intermediate dimension.
+// One work item = (tile of 128 padded token rows of one expert, 256 weight
+// rows): gate+up (two 128-row MMAs sharing B, SwiGLU epilogue) or down (two
+// 128-row MMAs, weighted scatter-add epilogue).
+//
+// Warp roles (192 threads, one CTA per SM, persistent over the items):
+//   warp 0   TMA producer (one lane)
+//   warp 1   TMEM owner; re-lays the weight scale tiles into the tensor-core
+//            scale-factor layout, then one lane issues tcgen05.cp + tcgen05.mma
+//   warps 2-5 epilogue (tcgen05.ld of their 32-lane quadrant of the accumulators)
+// Every mbarrier wait is bounded (about one second); on expiry the kernel sets
+// the plan's timeout bit and every role leaves its loop.
+#include <cuda.h>
+
+#include <algorithm>
+
 #include "moe_internal.cuh"
 
 namespace moe {
+namespace {
 
-bool tc_supported(const Plan &) { return false; }
-cudaError_t configure_tc(const Plan &) { return cudaSuccess; }
-cudaError_t launch_ffn_tc(const Plan &, const void *, int, const ExpertPtrs &, const ExpertPtrs *, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int kStages = 3;
+constexpr int kBK = 256;                  // K values per pipeline stage
+constexpr int kRowBytes = kBK / 2;        // 128 code bytes per row per stage
+constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
+constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
+constexpr int kStageBytes = 3 * kTile + 5 * kSf;
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single wait
+
+enum Epi { kSwiGLU = 0, kScatter = 1 };
+
+struct TcArgs {
+    CUtensorMap a0[2];      // [routed, shared]: gate codes (G1) / down codes (G2)
+    CUtensorMap a1[2];      // up codes (G1) / unused (G2: second half of down rows from a0)
+    CUtensorMap s0[2];      // plain scale tiles matching a0
+    CUtensorMap s1[2];      // matching a1
+    CUtensorMap b;          // token rows: Xp codes (G1) / SwiGLU codes (G2), [rows][Kb]
+    const uint8_t *b_atoms; // token-row scales in the tensor-core layout
+    int b_atoms_per_block;  // 512-byte atoms per 128-row block (= row length / 64)
+    const int4 *tiles;      // {expert (E = shared), first padded row, valid rows, 0}
+    const CallScratch *scratch;
+    int E, H, I, Is;
+    int nf;                 // 256-row weight groups per item row (G1: Imax/128, G2: H/256)
+    // epilogue
+    const float *ts_a0[2], *ts_a1[2];  // tensor scales of the A operands
+    const float *b_ts;      // SwiGLU tensor scales [routed, shared] (G2)
+    float *hbuf;            // G1 output [rows][hstride] fp32
+    int hstride;
+    unsigned int *h_amax, *hs_amax;
+    const int32_t *pad_pair;
+    const float *wts;
+    int P, k;
+    float *acc;             // G2 output [T][H]
+    int *err;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t now_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity; false (and the timeout
+// bit set) if it has not completed within kWaitNs.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = now_ns();
+    while (!mbar_test(bar, parity)) {
+        if (now_ns() - t0 > kWaitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Descriptor of one 512-byte scale-factor atom (32 rows x 16 bytes, no swizzle)
+// for tcgen05.cp .32x128b.
+__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor, kind::mxf4nvf4: A and B E2M1, UE4M3 scales, K-major,
+// M = 128, N = 128.
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+__device__ __forceinline__ void sf_copy(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+struct Item {
+    int e, row0, valid, f, sh, K;
+};
+
+__device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, Item &it) {
+    const int4 t = a.tiles[item / a.nf];
+    it.f = item % a.nf;
+    it.e = t.x;
+    it.row0 = t.y;
+    it.valid = t.z;
+    it.sh = (t.x == a.E);
+    const int I = it.sh ? a.Is : a.I;
+    if (epi == kSwiGLU) {
+        it.K = a.H;
+        return it.f * 128 < I;
+    }
+    it.K = I;
+    return true;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;
+    uint64_t *acc_empty = acc_full + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = a.scratch->n_tiles * a.nf;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item(a, item, EPI, it)) continue;
+                const int m = it.sh ? 1 : 0;
+                int r0, r1;
+                if (EPI == kSwiGLU) {
+                    r0 = r1 = (it.sh ? 0 : it.e * a.I) + it.f * 128;
+                } else {
+                    r0 = (it.sh ? 0 : it.e * a.H) + it.f * 256;
+                    r1 = r0 + 128;
+                }
+                const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
+                const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
+                const uint8_t *batoms = a.b_atoms + (size_t)(it.row0 / 128) * a.b_atoms_per_block * 512;
+                const int ks_n = it.K / kBK;
+                for (int ks = 0; ks < ks_n; ++ks) {
+                    if (!mbar_wait(empty + s, ph ^ 1, a.err)) { ok = false; break; }
+                    uint8_t *st = smem + s * kStageBytes;
+                    mbar_expect_tx(full + s, 3 * kTile + 3 * kSf);
+                    tma_2d(st, &a.a0[m], full + s, ks * kRowBytes, r0);
+                    tma_2d(st + kTile, A1, full + s, ks * kRowBytes, r1);
+                    tma_2d(st + 2 * kTile, &a.b, full + s, ks * kRowBytes, it.row0);
+                    tma_2d(st + 3 * kTile, &a.s0[m], full + s, ks * 16, r0);
+                    tma_2d(st + 3 * kTile + kSf, S1, full + s, ks * 16, r1);
+                    bulk_copy(st + 3 * kTile + 4 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
+                    if (++s == kStages) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ scale re-layout + MMA issue
+        int s = 0;
+        uint32_t ph = 0, aph = 0;
+        bool ok = true;
+        const uint32_t d0 = tmem, d1 = tmem + 128;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item(a, item, EPI, it)) continue;
+            if (!mbar_wait(acc_empty, aph ^ 1, a.err)) break;
+            aph ^= 1;
+            tc_fence_after();
+            const int ks_n = it.K / kBK;
+            for (int ks = 0; ks < ks_n; ++ks) {
+                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                uint8_t *st = smem + s * kStageBytes;
+                // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each: the
+                // 4 scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
+#pragma unroll
+                for (int op = 0; op < 2; ++op) {
+                    const uint4 *src = reinterpret_cast<const uint4 *>(st + 3 * kTile + op * kSf);
+                    uint4 *dst = reinterpret_cast<uint4 *>(st + 3 * kTile + 2 * kSf + op * kSf);
+                    uint4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+                    dst[0 * 32 + lane] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                    dst[1 * 32 + lane] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+                    dst[2 * 32 + lane] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+                    dst[3 * 32 + lane] = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t base = smem_u32(st);
+                    const uint32_t at0 = base + 3 * kTile + 2 * kSf, at1 = at0 + kSf, atb = at0 + 2 * kSf;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        sf_copy(tmem + 256 + 4 * kk, desc_sf(at0 + 512 * kk));
+                        sf_copy(tmem + 272 + 4 * kk, desc_sf(at1 + 512 * kk));
+                        sf_copy(tmem + 288 + 4 * kk, desc_sf(atb + 512 * kk));
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t accum = (ks | kk) ? 1u : 0u;
+                        const uint64_t bd = desc_sw128(base + 2 * kTile + 32 * kk);
+                        mma_fp4(d0, desc_sw128(base + 32 * kk), bd, tmem + 256 + 4 * kk, tmem + 288 + 4 * kk, accum);
+                        mma_fp4(d1, desc_sw128(base + kTile + 32 * kk), bd, tmem + 272 + 4 * kk, tmem + 288 + 4 * kk,
+                                accum);
+                    }
+                    mma_commit(empty + s);
+                }
+                __syncwarp();
+                if (++s == kStages) { s = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(acc_full);
+            __syncwarp();
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2..5)
+        const int quad = warp & 3;
+        uint32_t aph = 0;
+        float lmax = 0.0f, lmax_s = 0.0f;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item(a, item, EPI, it)) continue;
+            if (!mbar_wait(acc_full, aph, a.err)) break;
+            aph ^= 1;
+            tc_fence_after();
+            const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+            const int m = it.sh ? 1 : 0;
+            const int e = it.sh ? 0 : it.e;
+            if (EPI == kSwiGLU) {
+                const float xts = __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
+                const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
+                const int feat = it.f * 128 + quad * 32 + lane;
+                float mx = 0.0f;
+                for (int n0 = 0; n0 < 128 && n0 < it.valid; n0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16(lane_base + n0, g);
+                    tmem_ld16(lane_base + 128 + n0, u);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (n0 + j < it.valid) {
+                            const float gv = g[j] * sg, uv = u[j] * su;
+                            const float h = gv / (1.0f + expf(-gv)) * uv;
+                            a.hbuf[(size_t)(it.row0 + n0 + j) * a.hstride + feat] = h;
+                            mx = fmaxf(mx, fabsf(h));
+                        }
+                    }
+                }
+                if (it.sh) lmax_s = fmaxf(lmax_s, mx);
+                else lmax = fmaxf(lmax, mx);
+            } else {
+                const float ds = a.ts_a0[m][e] * a.b_ts[m];
+                // column n's token and routing weight, spread over the lanes
+                int tok[4];
+                float wgt[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int n = lane + 32 * q;
+                    tok[q] = 0;
+                    wgt[q] = 0.0f;
+                    if (n < it.valid) {
+                        const int pair = a.pad_pair[it.row0 + n];
+                        tok[q] = pair >= a.P ? pair - a.P : pair / a.k;
+                        wgt[q] = pair >= a.P ? 1.0f : a.wts[pair];
+                    }
+                }
+                const int j0 = it.f * 256 + quad * 32 + lane;
+                for (int n0 = 0; n0 < 128 && n0 < it.valid; n0 += 16) {
+                    float y0[16], y1[16];
+                    tmem_ld16(lane_base + n0, y0);
+                    tmem_ld16(lane_base + 128 + n0, y1);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int n = n0 + j;
+                        const int t = __shfl_sync(0xffffffffu, tok[n >> 5], n & 31);
+                        const float wv = __shfl_sync(0xffffffffu, wgt[n >> 5], n & 31);
+                        if (n < it.valid) {
+                            float *dst = a.acc + (size_t)t * a.H + j0;
+                            atomicAdd(dst, y0[j] * ds * wv);
+                            atomicAdd(dst + 128, y1[j] * ds * wv);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+        }
+        if (EPI == kSwiGLU) {
+            lmax = warp_max(lmax);
+            lmax_s = warp_max(lmax_s);
+            if (lane == 0) {
+                if (lmax > 0.0f) atomic_max_nonneg(a.h_amax, lmax);
+                if (lmax_s > 0.0f) atomic_max_nonneg(a.hs_amax, lmax_s);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    }
+}
+
+// Gather x's NVFP4 codes into the padded per-expert rows and its scales into
+// the tensor-core scale layout (512-byte atoms of 128 rows x 4 scale bytes:
+// byte (r % 32) * 16 + (r / 32 % 4) * 4 + j of atom (r / 128, c)).
+__global__ void __launch_bounds__(256) k_permute_fp4(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xsc,
+                                                     const int32_t *__restrict__ pad_pair,
+                                                     const int32_t *__restrict__ poff, int E, int H, int P, int k,
+                                                     uint8_t *__restrict__ xp, uint8_t *__restrict__ xp_atoms) {
+    const int rows = poff[E + 1];
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const int cb = H / 2 / 16;    // uint4 per code row
+    const int sw = H / 16 / 4;    // scale words per row
+    for (int r = warp; r < rows; r += nwarps) {
+        const int pair = pad_pair[r];
+        if (pair < 0) continue;
+        const int t = pair >= P ? pair - P : pair / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * (H / 2));
+        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * (H / 2));
+        for (int i = lane; i < cb; i += 32) dst[i] = src[i];
+        const uint32_t *ss = reinterpret_cast<const uint32_t *>(xsc + (size_t)t * (H / 16));
+        const int rb = r >> 7, rr = r & 127;
+        uint8_t *ab = xp_atoms + (size_t)rb * (H / 64) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+        for (int c = lane; c < sw; c += 32) *reinterpret_cast<uint32_t *>(ab + (size_t)c * 512) = ss[c];
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D uint8 tensor map: `rows` rows of `row_bytes` bytes (row stride
+// `stride`), box = box_bytes x box_rows.
+bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint64_t stride,
+              uint32_t box_bytes, uint32_t box_rows, bool swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {stride};
+    cuuint32_t box[2] = {box_bytes, box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = kStages * kStageBytes + 256 + 1024;
+
+}  // namespace
+
+// Shapes the tensor-core path takes: W4A4, H a multiple of 256, I (and the
+// shared I) multiples of 256, scale rows 16-byte aligned.
+bool tc_supported(const Plan &p) {
+    const moe_config &c = p.cfg;
+    if (c.mode != MOE_W4A4) return false;
+    if (c.hidden % 256 || c.inter % 256) return false;
+    if (c.has_shared && c.shared_inter % 256) return false;
+    return encode_fn() != nullptr;
+}
+
+cudaError_t configure_tc(const Plan &) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_gemm_fp4<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+}
+
+cudaError_t launch_ffn_tc(const Plan &p, const void *, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
+                          cudaStream_t st) {
+    const moe_config &c = p.cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts;
+    const int Is = c.has_shared ? c.shared_inter : 0;
+    const int Imax = std::max(I, Is);
+    const ExpertPtrs &sp = s ? *s : r;
+    const int Is_ = s ? Is : I;
+    TcArgs a{};
+    a.tiles = p.tiles;
+    a.scratch = p.scratch;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.Is = Is;
+    a.hbuf = p.hbuf;
+    a.hstride = Imax;
+    a.h_amax = &p.scratch->h_amax;
+    a.hs_amax = &p.scratch->hs_amax;
+    a.pad_pair = p.pad_pair;
+    a.wts = p.wts;
+    a.P = T * c.top_k;
+    a.k = c.top_k;
+    a.acc = p.acc;
+    a.err = p.err;
+    a.b_ts = p.hts;
+    bool ok = true;
+    if (part == 0) {
+        // permute x codes/scales into the padded rows first
+        k_permute_fp4<<<p.num_sms * 4, 256, 0, st>>>(p.xq, p.xsc, p.pad_pair, p.poff, E, H, a.P, c.top_k, p.xp,
+                                                     p.xp_atoms);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
+        ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
+        ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.s1[0], r.us, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 128, 128, true);
+        ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
+        ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
+        ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
+        ok &= make_map(&a.b, p.xp, H / 2, p.rows_pad_max, H / 2, 128, 128, true);
+        a.b_atoms = p.xp_atoms;
+        a.b_atoms_per_block = H / 64;
+        a.nf = Imax / 128;
+        a.ts_a0[0] = r.gts;
+        a.ts_a1[0] = r.uts;
+        a.ts_a0[1] = sp.gts;
+        a.ts_a1[1] = sp.uts;
+        if (!ok) return cudaErrorInvalidValue;
+        k_gemm_fp4<kSwiGLU><<<p.num_sms, kThreads, kSmemBytes, st>>>(a);
+        return cudaGetLastError();
+    }
+    ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
+    ok &= make_map(&a.s0[0], r.ds, I / 16, (uint64_t)E * H, I / 16, 16, 128, false);
+    ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 128, 128, true);
+    ok &= make_map(&a.s0[1], sp.ds, Is_ / 16, H, Is_ / 16, 16, 128, false);
+    a.a1[0] = a.a0[0];
+    a.a1[1] = a.a0[1];
+    a.s1[0] = a.s0[0];
+    a.s1[1] = a.s0[1];
+    ok &= make_map(&a.b, p.hq, Imax / 2, p.rows_pad_max, Imax / 2, 128, 128, true);
+    a.b_atoms = p.hq_atoms;
+    a.b_atoms_per_block = Imax / 64;
+    a.nf = H / 256;
+    a.ts_a0[0] = r.dts;
+    a.ts_a0[1] = sp.dts;
+    a.ts_a1[0] = r.dts;
+    a.ts_a1[1] = sp.dts;
+    if (!ok) return cudaErrorInvalidValue;
+    k_gemm_fp4<kScatter><<<p.num_sms, kThreads, kSmemBytes, st>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace moe

@@ -56,6 +56,11 @@ struct Plan {
     int32_t *inv = nullptr;         // [P] pair -> padded row
     int32_t *pad_pair = nullptr;    // [rows_pad] pair at a padded row (-1 pad, >= P shared token)
     int4 *chunks = nullptr;         // [chunks_max] {expert, first padded row, rows, 0}
+    int4 *tiles = nullptr;          // [tiles_max] {expert, first padded row, valid rows, 0}, 128-row tiles
+    int64_t tiles_max = 0;
+    uint8_t *xp = nullptr;          // [rows_pad][H/2] permuted x codes (tensor-core path)
+    uint8_t *xp_atoms = nullptr;    // [rows_pad/128][H/64][512] their scales, tensor-core layout
+    uint8_t *hq_atoms = nullptr;    // [rows_pad/128][Imax/64][512] SwiGLU scales, tensor-core layout
     CallScratch *scratch = nullptr;
     float *xts = nullptr;           // [2] x tensor scale, spare
     uint8_t *xq = nullptr;          // [Tmax][H/2]
@@ -186,7 +191,7 @@ cudaError_t launch_quant_nvfp4(const float *w, int batch, int rows, int cols, ui
 // part 0: gate + up + SwiGLU; part 1: down + routing weight + scatter-add.
 cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtrs &routed,
                             const ExpertPtrs *shared, int part, cudaStream_t st);
-cudaError_t launch_quant_h(const Plan &p, cudaStream_t st);
+cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st);
 cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st);
 
 }  // namespace moe

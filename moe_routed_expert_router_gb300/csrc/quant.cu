@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_h(const float *__restrict__ 
                                                      const int32_t *__restrict__ poff, int E, int I, int Is,
                                                      const int32_t *__restrict__ pad_pair,
                                                      const CallScratch *__restrict__ sc, uint2 *__restrict__ codes,
-                                                     uint8_t *__restrict__ scales, float *hts) {
+                                                     uint8_t *__restrict__ scales, uint8_t *__restrict__ atoms,
+                                                     float *hts) {
     const float ts_r = __fdiv_rn(__uint_as_float(sc->h_amax), 2688.0f);
     const float ts_s = __fdiv_rn(__uint_as_float(sc->hs_amax), 2688.0f);
     if (blockIdx.x == 0 && threadIdx.x == 0) { hts[0] = ts_r; hts[1] = ts_s; }
@@ -138,7 +139,13 @@ __global__ void __launch_bounds__(kThreads) k_quant_h(const float *__restrict__ 
         uint32_t s;
         quant_block16(v, sh ? ts_s : ts_r, c, s);
         codes[(int64_t)row * (stride / 16) + blk] = c;
-        scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+        if (atoms) {  // tensor-core scale layout: 512-byte atoms of 128 rows x 4 scales
+            const int rr = row & 127;
+            atoms[((int64_t)(row >> 7) * (stride / 64) + (blk >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (blk & 3)] =
+                (uint8_t)s;
+        } else {
+            scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+        }
     }
 }
 
@@ -184,11 +191,12 @@ cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_h(const Plan &p, cudaStream_t st) {
+cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st) {
     const int Imax = p.cfg.has_shared ? max(p.cfg.inter, p.cfg.shared_inter) : p.cfg.inter;
     k_quant_h<<<p.num_sms * 8, kThreads, 0, st>>>(p.hbuf, Imax, p.poff, p.cfg.num_experts, p.cfg.inter,
                                                   p.cfg.shared_inter, p.pad_pair, p.scratch,
-                                                  reinterpret_cast<uint2 *>(p.hq), p.hsc, p.hts);
+                                                  reinterpret_cast<uint2 *>(p.hq), p.hsc,
+                                                  tc_layout ? p.hq_atoms : nullptr, p.hts);
     return cudaGetLastError();
 }
 

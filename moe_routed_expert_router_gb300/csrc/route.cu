@@ -183,6 +183,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
                                                 int32_t *__restrict__ offsets, int32_t *__restrict__ poff,
                                                 int32_t *__restrict__ sorted, int32_t *__restrict__ inv,
                                                 int32_t *__restrict__ pad_pair, int4 *__restrict__ chunks,
+                                                int4 *__restrict__ tiles,
                                                 CallScratch *scratch, int32_t *__restrict__ offsets_out,
                                                 int32_t *__restrict__ sorted_out, int build_work, int rows_cap,
                                                 int *err) {
@@ -191,6 +192,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
     int *s_off = smem + 32 * E;            // [E+1]
     int *s_poff = s_off + (E + 1);         // [E+2]
     int *s_cb = s_poff + (E + 2);          // [E+2] chunk bases
+    int *s_tb = s_cb + (E + 2);            // [E+2] tile bases
     __shared__ int s_warp[32][3];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -228,6 +230,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         s_off[tid] = ba + a - c;
         s_poff[tid] = bb + b - pc;
         s_cb[tid] = bd + d - nc;
+        s_tb[tid] = (bb + b - pc) / kTileRows;   // a padded segment holds count/128 (rounded up) tiles
     }
     if (tid == 0) {
         int tot_a = s_warp[31][0], tot_b = s_warp[31][1], tot_d = s_warp[31][2];
@@ -236,6 +239,8 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         s_poff[E + 1] = tot_b + (has_shared ? (T + kTileRows - 1) / kTileRows * kTileRows : 0);
         s_cb[E] = tot_d;
         s_cb[E + 1] = tot_d + (has_shared ? (T + kChunkRows - 1) / kChunkRows : 0);
+        s_tb[E] = tot_b / kTileRows;
+        s_tb[E + 1] = s_poff[E + 1] / kTileRows;
         if (tot_a != P) atomicOr(err, kErrDevice);
     }
     __syncthreads();
@@ -311,7 +316,15 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         for (int q = 0; q * kChunkRows < cnt; ++q)
             chunks[cb + q] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
     }
+    // tensor-core tiles: 128 padded rows of one expert each
+    for (int e = tid; e <= E; e += 1024) {
+        int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (has_shared ? T : 0);
+        int tb = s_tb[e];
+        for (int q = 0; q * kTileRows < cnt; ++q)
+            tiles[tb + q] = make_int4(e, s_poff[e] + q * kTileRows, min(kTileRows, cnt - q * kTileRows), 0);
+    }
     if (tid == 0) {
+        scratch->n_tiles = s_tb[E + 1];
         scratch->n_chunks = s_cb[E + 1];
         int na = 0;
         for (int e = 0; e < E; ++e) na += (s_off[e + 1] > s_off[e]);
@@ -352,7 +365,7 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     return cudaGetLastError();
 }
 
-size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 3 * (size_t)E + 5); }
+size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (size_t)E + 8); }
 
 cudaError_t configure_group_kernel(int E) {
     return cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(E));
@@ -363,7 +376,7 @@ cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offs
     const int E = p.cfg.num_experts, k = p.cfg.top_k;
     size_t smem = group_smem_bytes(E);
     k_group<<<1, 1024, smem, st>>>(ids, T * k, E, T, k, p.cfg.has_shared, p.counts, p.offsets, p.poff, p.sorted,
-                                   p.inv, p.pad_pair, p.chunks, p.scratch, offsets_out, sorted_out,
+                                   p.inv, p.pad_pair, p.chunks, p.tiles, p.scratch, offsets_out, sorted_out,
                                    build_work ? 1 : 0, (int)p.rows_pad_max, p.err);
     return cudaGetLastError();
 }

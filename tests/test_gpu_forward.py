@@ -46,6 +46,31 @@ def test_prompt512_w4a16_full():
     _parity(Case(synth.WORKLOADS["prompt512_w4a16"], 0))
 
 
+@pytest.mark.parametrize("path", ["cuda_core", "tensor_core"])
+def test_w4a4_paths_against_oracle(path):
+    w = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=200, hidden=1024, experts=16, inter=512,
+                     shared_inter=256)
+    case = Case(w, 1)
+    plan = plan_for(w)
+    plan.set_path(moe.PATH_CUDA_CORE if path == "cuda_core" else moe.PATH_TENSOR_CORE)
+    _parity(case, plan)
+
+
+def test_tensor_core_path_matches_cuda_core_path():
+    w = synth.scaled(synth.WORKLOADS["verify16_w4a4"], hidden=2048, experts=32, inter=768, shared_inter=512)
+    w = synth.scaled(w, inter=512)
+    case = Case(w, 2)
+    p1, p2 = plan_for(w), plan_for(w)
+    p1.set_path(moe.PATH_CUDA_CORE)
+    p2.set_path(moe.PATH_TENSOR_CORE)
+    a, st1, _ = case.gpu_forward(p1)
+    b, st2, _ = case.gpu_forward(p2)
+    assert st1 == moe.OK and st2 == moe.OK
+    d = (a.float() - b.float()).abs()
+    rms = a.float().pow(2).mean().sqrt()
+    assert (d.max() / rms).item() < 2e-2 and (d.norm() / a.float().norm()).item() < 5e-3
+
+
 def test_prompt4096_w4a4_reduced():
     # several 128-row tiles for the heavy experts and a ragged tail
     w = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=300, hidden=1024, experts=32, inter=512)
