@@ -15,7 +15,7 @@ namespace moe {
 namespace {
 
 constexpr int kWarps = 8;
-constexpr int kFeatGroup = 64;  // features (gate/up) or output rows (down) per work item
+constexpr int kFeatGroup = 128;  // features (gate/up) or output rows (down) per work item
 
 // Row-major [kChunkRows][K] fp32 tile in shared memory with 16-byte chunks
 // xor-swizzled inside each group of 8, so a warp reading one 32-value unit per
@@ -47,42 +47,47 @@ struct FfnArgs {
 
 __device__ __forceinline__ int token_of(int pair, int P, int k) { return pair >= P ? pair - P : pair / k; }
 
-// Dot of one 32-value unit (16 code bytes + 2 scale bytes) with kChunkRows
-// activation rows held in shared memory (swizzled), accumulated into acc[].
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
+// Dot of one 32-value unit (16 code bytes + 2 scale bytes) with NR activation
+// rows held in shared memory (swizzled), accumulated into acc[].  The unit is
+// decoded once (E2M1 -> f16x2 -> fp32 pairs) and used for all NR rows; the 16
+// products of a scale block are summed in fp32 pairs, then scaled.
+template <int NR>
 __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const float *xs, int K, int u,
                                          float (&acc)[kChunkRows]) {
-    const uint32_t sc2 = e4m3x2_to_f16x2(sp);
-    const float2 scf = f16x2_to_f32x2(sc2);
+    const float2 scf = f16x2_to_f32x2(e4m3x2_to_f16x2(sp));
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
-        float w[16];
+        float2 w[8];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             uint32_t h[4];
             e2m1x8_to_f16x8(words[blk * 2 + q], h);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                float2 f = f16x2_to_f32x2(h[j]);
-                w[q * 8 + 2 * j] = f.x;
-                w[q * 8 + 2 * j + 1] = f.y;
-            }
+            for (int j = 0; j < 4; ++j) w[q * 4 + j] = f16x2_to_f32x2(h[j]);
         }
         const float sc = blk ? scf.y : scf.x;
         const int kbase = u * 32 + blk * 16;
 #pragma unroll
-        for (int r = 0; r < kChunkRows; ++r) {
+        for (int r = 0; r < NR; ++r) {
             const float *row = xs + r * K;
-            float p = 0.0f;
+            float2 p = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float4 xv = *reinterpret_cast<const float4 *>(row + swz(kbase + 4 * j));
-                p = fmaf(w[4 * j], xv.x, p);
-                p = fmaf(w[4 * j + 1], xv.y, p);
-                p = fmaf(w[4 * j + 2], xv.z, p);
-                p = fmaf(w[4 * j + 3], xv.w, p);
+                const float4 xv = *reinterpret_cast<const float4 *>(row + swz(kbase + 4 * j));
+                p = ffma2(w[2 * j], make_float2(xv.x, xv.y), p);
+                p = ffma2(w[2 * j + 1], make_float2(xv.z, xv.w), p);
             }
-            acc[r] = fmaf(p, sc, acc[r]);
+            acc[r] = fmaf(p.x + p.y, sc, acc[r]);
         }
     }
 }
@@ -90,10 +95,10 @@ __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const floa
 template <int MODE>
 __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
     const int H = a.H;
-    for (int idx = threadIdx.x; idx < kChunkRows * (H / 16); idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < ch.z * (H / 16); idx += blockDim.x) {
         const int r = idx / (H / 16), b = idx % (H / 16);
         float v[16];
-        if (r < ch.z) {
+        {
             const int tok = token_of(a.pad_pair[ch.y + r], a.P, a.k);
             if (MODE == MOE_W4A16) {
                 const uint4 *p = reinterpret_cast<const uint4 *>(a.x + (size_t)tok * H + b * 16);
@@ -117,9 +122,6 @@ __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
                     v[2 * j + 1] = f.y * sc;
                 }
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
         }
         float *row = xs + r * H;
 #pragma unroll
@@ -128,13 +130,77 @@ __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
     }
 }
 
-// Gate + up + SwiGLU.  Item = (chunk, group of 64 features); a warp does 8
-// features one after another, each as one gate row and one up row.
+// Rows of one weight-row pair (gate i, up i) for FPW features at a time: all
+// loads of the wave are issued before any arithmetic.
+template <int MODE, int UPL, int FPW, int NR>
+__device__ __forceinline__ void gateup_rows(const FfnArgs &a, const ExpertPtrs &W, int e, int I, int i0, int i_end,
+                                            const int4 &ch, const float *xs, float tsg, float tsu, float &lmax) {
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, units = H / 32;
+    for (int i = i0; i < i_end; i += FPW) {
+        uint4 cg[FPW][UPL], cu[FPW][UPL];
+        uint32_t sg[FPW][UPL], su[FPW][UPL];
+#pragma unroll
+        for (int f = 0; f < FPW; ++f) {
+            const size_t row = (size_t)e * I + i + f;
+            const uint8_t *gc = W.gc + row * (H / 2), *uc = W.uc + row * (H / 2);
+            const uint8_t *gs = W.gs + row * (H / 16), *us = W.us + row * (H / 16);
+#pragma unroll
+            for (int m = 0; m < UPL; ++m) {
+                const int u = lane + 32 * m;
+                if (u < units) {
+                    cg[f][m] = ldg_stream(gc + u * 16);
+                    cu[f][m] = ldg_stream(uc + u * 16);
+                    sg[f][m] = __ldg(reinterpret_cast<const unsigned short *>(gs + u * 2));
+                    su[f][m] = __ldg(reinterpret_cast<const unsigned short *>(us + u * 2));
+                }
+            }
+        }
+#pragma unroll
+        for (int f = 0; f < FPW; ++f) {
+            float ag[kChunkRows], au[kChunkRows];
+#pragma unroll
+            for (int r = 0; r < kChunkRows; ++r) ag[r] = au[r] = 0.0f;
+#pragma unroll
+            for (int m = 0; m < UPL; ++m) {
+                const int u = lane + 32 * m;
+                if (u < units) {
+                    unit_dot<NR>(cg[f][m], sg[f][m], xs, H, u, ag);
+                    unit_dot<NR>(cu[f][m], su[f][m], xs, H, u, au);
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                ag[r] = warp_sum(ag[r]);
+                au[r] = warp_sum(au[r]);
+            }
+            if (lane < NR) {
+                float g = 0.f, uu = 0.f;
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (r == lane) { g = ag[r]; uu = au[r]; }
+                g *= tsg;
+                uu *= tsu;
+                const float h = g / (1.0f + expf(-g)) * uu;
+                const size_t hrow = (size_t)(ch.y + lane) * a.hstride + i + f;
+                if (MODE == MOE_W4A16) {
+                    static_cast<__nv_bfloat16 *>(a.hbuf)[hrow] = __float2bfloat16_rn(h);
+                } else {
+                    static_cast<float *>(a.hbuf)[hrow] = h;
+                    lmax = fmaxf(lmax, fabsf(h));
+                }
+            }
+        }
+    }
+}
+
+// Gate + up + SwiGLU.  Item = (chunk, group of kFeatGroup features); each warp
+// takes kFeatGroup / kWarps consecutive features.
 template <int MODE, int UPL>
 __global__ void __launch_bounds__(kWarps * 32) k_gateup_simt(FfnArgs a) {
     extern __shared__ float xs[];
+    constexpr int FPW = UPL <= 4 ? 2 : 1;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int H = a.H, units = H / 32;
     const int Imax = max(a.I, a.Is);
     const int groups = (Imax + kFeatGroup - 1) / kFeatGroup;
     const int n_items = a.scratch->n_chunks * groups;
@@ -152,56 +218,13 @@ __global__ void __launch_bounds__(kWarps * 32) k_gateup_simt(FfnArgs a) {
         const int e = sh ? 0 : ch.x;
         const float tsg = W.gts[e] * xscale, tsu = W.uts[e] * xscale;
         float lmax = 0.0f;
-        for (int q = 0; q < kFeatGroup / kWarps; ++q) {
-            const int i = fg * kFeatGroup + warp * (kFeatGroup / kWarps) + q;
-            if (i >= I) break;
-            const size_t row = (size_t)e * I + i;
-            const uint8_t *gc = W.gc + row * (H / 2), *uc = W.uc + row * (H / 2);
-            const uint8_t *gs = W.gs + row * (H / 16), *us = W.us + row * (H / 16);
-            uint4 cg[UPL], cu[UPL];
-            uint32_t sg[UPL], su[UPL];
-#pragma unroll
-            for (int m = 0; m < UPL; ++m) {
-                const int u = lane + 32 * m;
-                if (u < units) {
-                    cg[m] = ldg_stream(gc + u * 16);
-                    cu[m] = ldg_stream(uc + u * 16);
-                    sg[m] = __ldg(reinterpret_cast<const unsigned short *>(gs + u * 2));
-                    su[m] = __ldg(reinterpret_cast<const unsigned short *>(us + u * 2));
-                }
-            }
-            float ag[kChunkRows], au[kChunkRows];
-#pragma unroll
-            for (int r = 0; r < kChunkRows; ++r) ag[r] = au[r] = 0.0f;
-#pragma unroll
-            for (int m = 0; m < UPL; ++m) {
-                const int u = lane + 32 * m;
-                if (u < units) {
-                    unit_dot(cg[m], sg[m], xs, H, u, ag);
-                    unit_dot(cu[m], su[m], xs, H, u, au);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < kChunkRows; ++r) {
-                ag[r] = warp_sum(ag[r]);
-                au[r] = warp_sum(au[r]);
-            }
-            if (lane < ch.z) {
-                float g = 0.f, uu = 0.f;
-#pragma unroll
-                for (int r = 0; r < kChunkRows; ++r)
-                    if (r == lane) { g = ag[r]; uu = au[r]; }
-                g *= tsg;
-                uu *= tsu;
-                const float h = g / (1.0f + expf(-g)) * uu;
-                const size_t hrow = (size_t)(ch.y + lane) * a.hstride + i;
-                if (MODE == MOE_W4A16) {
-                    static_cast<__nv_bfloat16 *>(a.hbuf)[hrow] = __float2bfloat16_rn(h);
-                } else {
-                    static_cast<float *>(a.hbuf)[hrow] = h;
-                    lmax = fmaxf(lmax, fabsf(h));
-                }
-            }
+        const int i0 = fg * kFeatGroup + warp * (kFeatGroup / kWarps);
+        const int i_end = min(i0 + kFeatGroup / kWarps, I);
+        switch (ch.z) {
+            case 1: gateup_rows<MODE, UPL, FPW, 1>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
+            case 2: gateup_rows<MODE, UPL, FPW, 2>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
+            case 3: gateup_rows<MODE, UPL, FPW, 3>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
+            default: gateup_rows<MODE, UPL, FPW, 4>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
         }
         if (MODE == MOE_W4A4) {
             lmax = warp_max(lmax);
@@ -212,10 +235,10 @@ __global__ void __launch_bounds__(kWarps * 32) k_gateup_simt(FfnArgs a) {
 
 template <int MODE>
 __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
-    for (int idx = threadIdx.x; idx < kChunkRows * (I / 16); idx += blockDim.x) {
+    for (int idx = threadIdx.x; idx < ch.z * (I / 16); idx += blockDim.x) {
         const int r = idx / (I / 16), b = idx % (I / 16);
         float v[16];
-        if (r < ch.z) {
+        {
             const size_t row = (size_t)(ch.y + r);
             if (MODE == MOE_W4A16) {
                 const uint4 *p = reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(a.hbuf) +
@@ -240,9 +263,6 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
                     v[2 * j + 1] = f.y * sc;
                 }
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[j] = 0.0f;
         }
         float *rowp = hs + r * I;
 #pragma unroll
@@ -251,11 +271,63 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
     }
 }
 
-// Down + routing weight + scatter-add.  Item = (chunk, group of 64 output
-// rows); a warp does 8 rows, 4 at a time.
+// Down rows j0 .. j0+RPW-1 for NR tokens: loads first, then arithmetic, then one
+// atomic add per (row, token) of y * tensor scales * routing weight.
+template <int UPL, int RPW, int NR>
+__device__ __forceinline__ void down_rows(const FfnArgs &a, const ExpertPtrs &W, int e, int I, int j0,
+                                          const float *hs, float scale, float wrow, int tok) {
+    const int lane = threadIdx.x & 31;
+    const int H = a.H, units = I / 32;
+    uint4 c[RPW][UPL];
+    uint32_t s[RPW][UPL];
+#pragma unroll
+    for (int q = 0; q < RPW; ++q) {
+        const size_t row = (size_t)e * H + j0 + q;
+        const uint8_t *dc = W.dc + row * (I / 2), *ds = W.ds + row * (I / 16);
+#pragma unroll
+        for (int m = 0; m < UPL; ++m) {
+            const int u = lane + 32 * m;
+            if (u < units) {
+                c[q][m] = ldg_stream(dc + u * 16);
+                s[q][m] = __ldg(reinterpret_cast<const unsigned short *>(ds + u * 2));
+            }
+        }
+    }
+    float acc[RPW][kChunkRows];
+#pragma unroll
+    for (int q = 0; q < RPW; ++q)
+#pragma unroll
+        for (int r = 0; r < kChunkRows; ++r) acc[q][r] = 0.0f;
+#pragma unroll
+    for (int q = 0; q < RPW; ++q)
+#pragma unroll
+        for (int m = 0; m < UPL; ++m) {
+            const int u = lane + 32 * m;
+            if (u < units) unit_dot<NR>(c[q][m], s[q][m], hs, I, u, acc[q]);
+        }
+#pragma unroll
+    for (int q = 0; q < RPW; ++q)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) acc[q][r] = warp_sum(acc[q][r]);
+    // lane (q * NR + r) adds one value
+    const int q = lane / NR, r = lane % NR;
+    float y = 0.f;
+#pragma unroll
+    for (int qq = 0; qq < RPW; ++qq)
+#pragma unroll
+        for (int rr = 0; rr < NR; ++rr)
+            if (qq == q && rr == r) y = acc[qq][rr];
+    const float wr = __shfl_sync(0xffffffffu, wrow, r);
+    const int tk = __shfl_sync(0xffffffffu, tok, r);
+    if (q < RPW) atomicAdd(a.acc + (size_t)tk * H + j0 + q, y * scale * wr);
+}
+
+// Down + routing weight + scatter-add.  Item = (chunk, group of kFeatGroup
+// output rows); a warp takes kFeatGroup / kWarps rows, RPW at a time.
 template <int MODE, int UPL>
 __global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
     extern __shared__ float hs[];
+    constexpr int RPW = UPL <= 2 ? 8 : 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int H = a.H;
     const int groups = H / kFeatGroup;
@@ -265,7 +337,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
         const int og = item % groups;
         const bool sh = (ch.x == a.E);
         const int I = sh ? a.Is : a.I;
-        const int units = I / 32;
         __syncthreads();
         stage_h<MODE>(a, ch, I, hs);
         __syncthreads();
@@ -273,7 +344,6 @@ __global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
         const int e = sh ? 0 : ch.x;
         float scale = W.dts[e];
         if (MODE == MOE_W4A4) scale *= a.hts[sh ? 1 : 0];
-        // per-row routing weight and token of this chunk
         float wrow = 0.f;
         int tok = 0;
         if (lane < ch.z) {
@@ -281,50 +351,14 @@ __global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
             tok = token_of(pair, a.P, a.k);
             wrow = sh ? 1.0f : a.wts[pair];
         }
-        for (int q0 = 0; q0 < kFeatGroup / kWarps; q0 += 4) {
+        for (int q0 = 0; q0 < kFeatGroup / kWarps; q0 += RPW) {
             const int j0 = og * kFeatGroup + warp * (kFeatGroup / kWarps) + q0;
-            uint4 c[4][UPL];
-            uint32_t s[4][UPL];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const size_t row = (size_t)e * H + j0 + q;
-                const uint8_t *dc = W.dc + row * (I / 2), *ds = W.ds + row * (I / 16);
-#pragma unroll
-                for (int m = 0; m < UPL; ++m) {
-                    const int u = lane + 32 * m;
-                    if (u < units) {
-                        c[q][m] = ldg_stream(dc + u * 16);
-                        s[q][m] = __ldg(reinterpret_cast<const unsigned short *>(ds + u * 2));
-                    }
-                }
+            switch (ch.z) {
+                case 1: down_rows<UPL, RPW, 1>(a, W, e, I, j0, hs, scale, wrow, tok); break;
+                case 2: down_rows<UPL, RPW, 2>(a, W, e, I, j0, hs, scale, wrow, tok); break;
+                case 3: down_rows<UPL, RPW, 3>(a, W, e, I, j0, hs, scale, wrow, tok); break;
+                default: down_rows<UPL, RPW, 4>(a, W, e, I, j0, hs, scale, wrow, tok); break;
             }
-            float acc[4][kChunkRows];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int r = 0; r < kChunkRows; ++r) acc[q][r] = 0.0f;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int m = 0; m < UPL; ++m) {
-                    const int u = lane + 32 * m;
-                    if (u < units) unit_dot(c[q][m], s[q][m], hs, I, u, acc[q]);
-                }
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int r = 0; r < kChunkRows; ++r) acc[q][r] = warp_sum(acc[q][r]);
-            // lane (q * kChunkRows + r) adds one value
-            const int q = lane / kChunkRows, r = lane % kChunkRows;
-            float y = 0.f;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq)
-#pragma unroll
-                for (int rr = 0; rr < kChunkRows; ++rr)
-                    if (qq == q && rr == r) y = acc[qq][rr];
-            const float wr = __shfl_sync(0xffffffffu, wrow, r);
-            const int tk = __shfl_sync(0xffffffffu, tok, r);
-            if (q < 4 && r < ch.z) atomicAdd(a.acc + (size_t)tk * H + j0 + q, y * scale * wr);
         }
     }
 }
