@@ -246,14 +246,13 @@ def run_ours(args, w, world, rank, local):
     import moe_routed_expert_router_gb300 as moe
     moe.lib()
     pk = peaks()
-    n_inst = len(w.seeds) if w.batches == 1 else 1
     weights = {}
     insts = []
     if w.batches > 1:
         weights[w.seeds[0]] = build_weights(moe, w, w.seeds[0])
-        insts = [Instance(moe, w, w.seeds[0], b) for b in range(w.batches)]
+        insts = [Instance(moe, w, w.seeds[0], b) for b in range(args.instances or w.batches)]
     else:
-        for s in w.seeds:
+        for s in w.seeds[:args.instances or len(w.seeds)]:
             weights[s] = build_weights(moe, w, s)
             insts.append(Instance(moe, w, s))
     plan = moe.Plan(w.hidden, w.inter, w.experts, w.top_k, w.tokens,
@@ -397,6 +396,8 @@ def main():
     ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--instances", type=int, default=0,
+                    help="use only the first N seeded instances / batches (0 = all; for small profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

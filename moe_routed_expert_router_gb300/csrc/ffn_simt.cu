@@ -42,6 +42,7 @@ struct FfnArgs {
     const float *hts;           // [2] h tensor scales
     unsigned int *h_amax, *hs_amax;
     float *acc;                 // [T][H]
+    int *err;                   // plan error word (bounded waits)
     ExpertPtrs r, s;
 };
 
@@ -130,107 +131,161 @@ __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
     }
 }
 
-// Rows of one weight-row pair (gate i, up i) for FPW features at a time: all
-// loads of the wave are issued before any arithmetic.
-template <int MODE, int UPL, int FPW, int NR>
-__device__ __forceinline__ void gateup_rows(const FfnArgs &a, const ExpertPtrs &W, int e, int I, int i0, int i_end,
-                                            const int4 &ch, const float *xs, float tsg, float tsu, float &lmax) {
+// Each warp streams its own contiguous weight rows into a ring of `slots`
+// shared-memory slots with bulk copies (one mbarrier per slot, bounded
+// waits); lanes then read one 32-value unit at a time from shared memory, so
+// the bytes in flight do not depend on registers.
+struct Ring {
+    uint8_t *base;      // this warp's slots
+    uint64_t *bars;     // this warp's slot barriers
+    int slot_bytes, slots;
+    __device__ __forceinline__ uint8_t *slot(int q) const { return base + (size_t)(q % slots) * slot_bytes; }
+    __device__ __forceinline__ uint64_t *bar(int q) const { return bars + q % slots; }
+    __device__ __forceinline__ uint32_t parity(int q) const { return (uint32_t)((q / slots) & 1); }
+};
+
+// Item of the gate/up kernel: (chunk, group of 128 features).  Routed chunks
+// come first (I/128 groups each), then the shared expert's (Is/128 groups).
+__device__ __forceinline__ int4 gateup_item(const FfnArgs &a, int item, int &fg) {
+    const int nr = a.scratch->n_chunks_routed, gi = a.I / 128;
+    if (item < nr * gi) {
+        fg = item % gi;
+        return a.chunks[item / gi];
+    }
+    const int j = item - nr * gi, gs = a.Is / 128;
+    fg = j % gs;
+    return a.chunks[nr + j / gs];
+}
+
+__device__ __forceinline__ int gateup_items(const FfnArgs &a) {
+    const int nr = a.scratch->n_chunks_routed, ns = a.scratch->n_chunks - nr;
+    return nr * (a.I / 128) + (a.Is ? ns * (a.Is / 128) : 0);
+}
+
+// Issue step q of a warp's gate/up stream (lane 0): feature
+// fg*128 + warp*16 + (q % 16) of item q / 16's chunk, i.e. one gate row and one
+// up row (codes + scales) into slot q.  Returns false past the last item.
+__device__ __forceinline__ bool gateup_issue(const FfnArgs &a, const Ring &rg, int q, int n_items, int nw, int warp) {
+    const int per_warp = 128 / nw;
+    const int item = blockIdx.x + (q / per_warp) * gridDim.x;
+    if (item >= n_items) return false;
+    int fg;
+    const int4 ch = gateup_item(a, item, fg);
+    const bool sh = (ch.x == a.E);
+    const ExpertPtrs &W = sh ? a.s : a.r;
+    const int I = sh ? a.Is : a.I, e = sh ? 0 : ch.x, H = a.H;
+    const size_t row = (size_t)e * I + fg * 128 + warp * per_warp + q % per_warp;
+    uint8_t *dst = rg.slot(q);
+    uint64_t *bar = rg.bar(q);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, 2 * (H / 2) + 2 * (H / 16));
+    bulk_copy(dst, W.gc + row * (H / 2), H / 2, bar);
+    bulk_copy(dst + H / 2, W.uc + row * (H / 2), H / 2, bar);
+    bulk_copy(dst + H, W.gs + row * (H / 16), H / 16, bar);
+    bulk_copy(dst + H + H / 16, W.us + row * (H / 16), H / 16, bar);
+    return true;
+}
+
+template <int MODE, int NR>
+__device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *slot, const int4 &ch, int i,
+                                               const float *xs, float tsg, float tsu, float &lmax) {
     const int lane = threadIdx.x & 31;
     const int H = a.H, units = H / 32;
-    for (int i = i0; i < i_end; i += FPW) {
-        uint4 cg[FPW][UPL], cu[FPW][UPL];
-        uint32_t sg[FPW][UPL], su[FPW][UPL];
+    float ag[kChunkRows], au[kChunkRows];
 #pragma unroll
-        for (int f = 0; f < FPW; ++f) {
-            const size_t row = (size_t)e * I + i + f;
-            const uint8_t *gc = W.gc + row * (H / 2), *uc = W.uc + row * (H / 2);
-            const uint8_t *gs = W.gs + row * (H / 16), *us = W.us + row * (H / 16);
+    for (int r = 0; r < kChunkRows; ++r) ag[r] = au[r] = 0.0f;
+    for (int u = lane; u < units; u += 32) {
+        const uint4 cg = *reinterpret_cast<const uint4 *>(slot + u * 16);
+        const uint4 cu = *reinterpret_cast<const uint4 *>(slot + H / 2 + u * 16);
+        const uint32_t sg = *reinterpret_cast<const unsigned short *>(slot + H + u * 2);
+        const uint32_t su = *reinterpret_cast<const unsigned short *>(slot + H + H / 16 + u * 2);
+        unit_dot<NR>(cg, sg, xs, H, u, ag);
+        unit_dot<NR>(cu, su, xs, H, u, au);
+    }
 #pragma unroll
-            for (int m = 0; m < UPL; ++m) {
-                const int u = lane + 32 * m;
-                if (u < units) {
-                    cg[f][m] = ldg_stream(gc + u * 16);
-                    cu[f][m] = ldg_stream(uc + u * 16);
-                    sg[f][m] = __ldg(reinterpret_cast<const unsigned short *>(gs + u * 2));
-                    su[f][m] = __ldg(reinterpret_cast<const unsigned short *>(us + u * 2));
-                }
-            }
-        }
+    for (int r = 0; r < NR; ++r) {
+        ag[r] = warp_sum(ag[r]);
+        au[r] = warp_sum(au[r]);
+    }
+    if (lane < NR) {
+        float g = 0.f, uu = 0.f;
 #pragma unroll
-        for (int f = 0; f < FPW; ++f) {
-            float ag[kChunkRows], au[kChunkRows];
-#pragma unroll
-            for (int r = 0; r < kChunkRows; ++r) ag[r] = au[r] = 0.0f;
-#pragma unroll
-            for (int m = 0; m < UPL; ++m) {
-                const int u = lane + 32 * m;
-                if (u < units) {
-                    unit_dot<NR>(cg[f][m], sg[f][m], xs, H, u, ag);
-                    unit_dot<NR>(cu[f][m], su[f][m], xs, H, u, au);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                ag[r] = warp_sum(ag[r]);
-                au[r] = warp_sum(au[r]);
-            }
-            if (lane < NR) {
-                float g = 0.f, uu = 0.f;
-#pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    if (r == lane) { g = ag[r]; uu = au[r]; }
-                g *= tsg;
-                uu *= tsu;
-                const float h = g / (1.0f + expf(-g)) * uu;
-                const size_t hrow = (size_t)(ch.y + lane) * a.hstride + i + f;
-                if (MODE == MOE_W4A16) {
-                    static_cast<__nv_bfloat16 *>(a.hbuf)[hrow] = __float2bfloat16_rn(h);
-                } else {
-                    static_cast<float *>(a.hbuf)[hrow] = h;
-                    lmax = fmaxf(lmax, fabsf(h));
-                }
-            }
+        for (int r = 0; r < NR; ++r)
+            if (r == lane) { g = ag[r]; uu = au[r]; }
+        g *= tsg;
+        uu *= tsu;
+        const float h = g / (1.0f + expf(-g)) * uu;
+        const size_t hrow = (size_t)(ch.y + lane) * a.hstride + i;
+        if (MODE == MOE_W4A16) {
+            static_cast<__nv_bfloat16 *>(a.hbuf)[hrow] = __float2bfloat16_rn(h);
+        } else {
+            static_cast<float *>(a.hbuf)[hrow] = h;
+            lmax = fmaxf(lmax, fabsf(h));
         }
     }
 }
 
-// Gate + up + SwiGLU.  Item = (chunk, group of kFeatGroup features); each warp
-// takes kFeatGroup / kWarps consecutive features.
-template <int MODE, int UPL>
-__global__ void __launch_bounds__(kWarps * 32) k_gateup_simt(FfnArgs a) {
-    extern __shared__ float xs[];
-    constexpr int FPW = UPL <= 4 ? 2 : 1;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int Imax = max(a.I, a.Is);
-    const int groups = (Imax + kFeatGroup - 1) / kFeatGroup;
-    const int n_items = a.scratch->n_chunks * groups;
+// Gate + up + SwiGLU.  Dynamic shared memory: x tile [kChunkRows][H] fp32,
+// then nw warps x `slots` slots of (2 code rows + 2 scale rows), then the
+// slot barriers.
+template <int MODE>
+__global__ void __launch_bounds__(256) k_gateup_stream(FfnArgs a, int slots) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int H = a.H;
+    float *xs = reinterpret_cast<float *>(smem);
+    const int slot_bytes = H + H / 8;
+    uint8_t *rings = smem + (size_t)kChunkRows * H * 4;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rings + (size_t)nw * slots * slot_bytes);
+    Ring rg{rings + (size_t)warp * slots * slot_bytes, bars + warp * slots, slot_bytes, slots};
+    if (lane == 0)
+        for (int s = 0; s < slots; ++s) mbar_init(rg.bars + s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    const int n_items = gateup_items(a);
+    const int per_warp = 128 / nw;
     const float xscale = (MODE == MOE_W4A4) ? __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f) : 1.0f;
+    int issued = 0;
+    if (lane == 0)
+        while (issued < slots && gateup_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    bool ok = true;
+    int q = 0, done = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-        const int4 ch = a.chunks[item / groups];
-        const int fg = item % groups;
+        int fg;
+        const int4 ch = gateup_item(a, item, fg);
         const bool sh = (ch.x == a.E);
-        const int I = sh ? a.Is : a.I;
-        if (fg * kFeatGroup >= I) continue;
+        const ExpertPtrs &W = sh ? a.s : a.r;
+        const int e = sh ? 0 : ch.x;
         __syncthreads();
         stage_x<MODE>(a, ch, xs);
         __syncthreads();
-        const ExpertPtrs &W = sh ? a.s : a.r;
-        const int e = sh ? 0 : ch.x;
         const float tsg = W.gts[e] * xscale, tsu = W.uts[e] * xscale;
         float lmax = 0.0f;
-        const int i0 = fg * kFeatGroup + warp * (kFeatGroup / kWarps);
-        const int i_end = min(i0 + kFeatGroup / kWarps, I);
-        switch (ch.z) {
-            case 1: gateup_rows<MODE, UPL, FPW, 1>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
-            case 2: gateup_rows<MODE, UPL, FPW, 2>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
-            case 3: gateup_rows<MODE, UPL, FPW, 3>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
-            default: gateup_rows<MODE, UPL, FPW, 4>(a, W, e, I, i0, i_end, ch, xs, tsg, tsu, lmax); break;
+        for (int f = 0; f < per_warp; ++f, ++q) {
+            if (ok && !mbar_wait(rg.bar(q), rg.parity(q), a.err)) ok = false;
+            if (ok) {
+                done = q + 1;
+                const uint8_t *slot = rg.slot(q);
+                const int i = fg * 128 + warp * per_warp + f;
+                switch (ch.z) {
+                    case 1: gateup_compute<MODE, 1>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    case 2: gateup_compute<MODE, 2>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    case 3: gateup_compute<MODE, 3>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    default: gateup_compute<MODE, 4>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && ok && issued == q + slots && gateup_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+            issued = __shfl_sync(0xffffffffu, issued, 0);
         }
         if (MODE == MOE_W4A4) {
             lmax = warp_max(lmax);
             if (lane == 0 && lmax > 0.0f) atomic_max_nonneg(sh ? a.hs_amax : a.h_amax, lmax);
         }
     }
+    // after a timeout, wait (bounded) for copies still landing in this warp's slots
+    for (int d = done; d < issued; ++d) mbar_wait(rg.bar(d), rg.parity(d), a.err);
 }
 
 template <int MODE>
@@ -271,67 +326,87 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
     }
 }
 
-// Down rows j0 .. j0+RPW-1 for NR tokens: loads first, then arithmetic, then one
-// atomic add per (row, token) of y * tensor scales * routing weight.
-template <int UPL, int RPW, int NR>
-__device__ __forceinline__ void down_rows(const FfnArgs &a, const ExpertPtrs &W, int e, int I, int j0,
-                                          const float *hs, float scale, float wrow, int tok) {
+// Down: item = (chunk, group of 128 output rows); warp w owns rows
+// og*128 + w*rpw .. +rpw, streamed kDownRows rows per slot.
+constexpr int kDownRows = 8;
+
+__device__ __forceinline__ bool down_issue(const FfnArgs &a, const Ring &rg, int q, int n_items, int nw, int warp) {
+    const int steps = 128 / nw / kDownRows;
+    const int item = blockIdx.x + (q / steps) * gridDim.x;
+    if (item >= n_items) return false;
+    const int groups = a.H / 128;
+    const int4 ch = a.chunks[item / groups];
+    const int og = item % groups;
+    const bool sh = (ch.x == a.E);
+    const ExpertPtrs &W = sh ? a.s : a.r;
+    const int I = sh ? a.Is : a.I, e = sh ? 0 : ch.x;
+    const size_t row = (size_t)e * a.H + og * 128 + warp * (128 / nw) + (q % steps) * kDownRows;
+    uint8_t *dst = rg.slot(q);
+    uint64_t *bar = rg.bar(q);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_expect_tx(bar, kDownRows * (I / 2 + I / 16));
+    bulk_copy(dst, W.dc + row * (I / 2), kDownRows * (I / 2), bar);
+    bulk_copy(dst + kDownRows * (I / 2), W.ds + row * (I / 16), kDownRows * (I / 16), bar);
+    return true;
+}
+
+template <int NR>
+__device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *slot, int I, int j0, const float *hs,
+                                             float scale, float wrow, int tok) {
     const int lane = threadIdx.x & 31;
-    const int H = a.H, units = I / 32;
-    uint4 c[RPW][UPL];
-    uint32_t s[RPW][UPL];
+    const int units = I / 32;
+    float acc[kDownRows][kChunkRows];
 #pragma unroll
-    for (int q = 0; q < RPW; ++q) {
-        const size_t row = (size_t)e * H + j0 + q;
-        const uint8_t *dc = W.dc + row * (I / 2), *ds = W.ds + row * (I / 16);
-#pragma unroll
-        for (int m = 0; m < UPL; ++m) {
-            const int u = lane + 32 * m;
-            if (u < units) {
-                c[q][m] = ldg_stream(dc + u * 16);
-                s[q][m] = __ldg(reinterpret_cast<const unsigned short *>(ds + u * 2));
-            }
-        }
-    }
-    float acc[RPW][kChunkRows];
-#pragma unroll
-    for (int q = 0; q < RPW; ++q)
+    for (int q = 0; q < kDownRows; ++q)
 #pragma unroll
         for (int r = 0; r < kChunkRows; ++r) acc[q][r] = 0.0f;
+    for (int u = lane; u < units; u += 32) {
 #pragma unroll
-    for (int q = 0; q < RPW; ++q)
-#pragma unroll
-        for (int m = 0; m < UPL; ++m) {
-            const int u = lane + 32 * m;
-            if (u < units) unit_dot<NR>(c[q][m], s[q][m], hs, I, u, acc[q]);
+        for (int q = 0; q < kDownRows; ++q) {
+            const uint4 c = *reinterpret_cast<const uint4 *>(slot + q * (I / 2) + u * 16);
+            const uint32_t s = *reinterpret_cast<const unsigned short *>(slot + kDownRows * (I / 2) + q * (I / 16) + u * 2);
+            unit_dot<NR>(c, s, hs, I, u, acc[q]);
         }
+    }
 #pragma unroll
-    for (int q = 0; q < RPW; ++q)
+    for (int q = 0; q < kDownRows; ++q)
 #pragma unroll
         for (int r = 0; r < NR; ++r) acc[q][r] = warp_sum(acc[q][r]);
-    // lane (q * NR + r) adds one value
     const int q = lane / NR, r = lane % NR;
     float y = 0.f;
 #pragma unroll
-    for (int qq = 0; qq < RPW; ++qq)
+    for (int qq = 0; qq < kDownRows; ++qq)
 #pragma unroll
         for (int rr = 0; rr < NR; ++rr)
             if (qq == q && rr == r) y = acc[qq][rr];
     const float wr = __shfl_sync(0xffffffffu, wrow, r);
     const int tk = __shfl_sync(0xffffffffu, tok, r);
-    if (q < RPW) atomicAdd(a.acc + (size_t)tk * H + j0 + q, y * scale * wr);
+    if (q < kDownRows) atomicAdd(a.acc + (size_t)tk * a.H + j0 + q, y * scale * wr);
 }
 
-// Down + routing weight + scatter-add.  Item = (chunk, group of kFeatGroup
-// output rows); a warp takes kFeatGroup / kWarps rows, RPW at a time.
-template <int MODE, int UPL>
-__global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
-    extern __shared__ float hs[];
-    constexpr int RPW = UPL <= 2 ? 8 : 4;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int H = a.H;
-    const int groups = H / kFeatGroup;
+template <int MODE>
+__global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    const int Imax = max(a.I, a.Is);
+    float *hs = reinterpret_cast<float *>(smem);
+    const int slot_bytes = kDownRows * (Imax / 2 + Imax / 16);
+    uint8_t *rings = smem + (size_t)kChunkRows * Imax * 4;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(rings + (size_t)nw * slots * slot_bytes);
+    Ring rg{rings + (size_t)warp * slots * slot_bytes, bars + warp * slots, slot_bytes, slots};
+    if (lane == 0)
+        for (int s = 0; s < slots; ++s) mbar_init(rg.bars + s, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    const int groups = a.H / 128;
     const int n_items = a.scratch->n_chunks * groups;
+    const int steps = 128 / nw / kDownRows;
+    int issued = 0;
+    if (lane == 0)
+        while (issued < slots && down_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    bool ok = true;
+    int q = 0, done = 0;
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int4 ch = a.chunks[item / groups];
         const int og = item % groups;
@@ -351,53 +426,64 @@ __global__ void __launch_bounds__(kWarps * 32) k_down_simt(FfnArgs a) {
             tok = token_of(pair, a.P, a.k);
             wrow = sh ? 1.0f : a.wts[pair];
         }
-        for (int q0 = 0; q0 < kFeatGroup / kWarps; q0 += RPW) {
-            const int j0 = og * kFeatGroup + warp * (kFeatGroup / kWarps) + q0;
-            switch (ch.z) {
-                case 1: down_rows<UPL, RPW, 1>(a, W, e, I, j0, hs, scale, wrow, tok); break;
-                case 2: down_rows<UPL, RPW, 2>(a, W, e, I, j0, hs, scale, wrow, tok); break;
-                case 3: down_rows<UPL, RPW, 3>(a, W, e, I, j0, hs, scale, wrow, tok); break;
-                default: down_rows<UPL, RPW, 4>(a, W, e, I, j0, hs, scale, wrow, tok); break;
+        for (int st = 0; st < steps; ++st, ++q) {
+            if (ok && !mbar_wait(rg.bar(q), rg.parity(q), a.err)) ok = false;
+            if (ok) {
+                done = q + 1;
+                const uint8_t *slot = rg.slot(q);
+                const int j0 = og * 128 + warp * (128 / nw) + st * kDownRows;
+                switch (ch.z) {
+                    case 1: down_compute<1>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    case 2: down_compute<2>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    case 3: down_compute<3>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    default: down_compute<4>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                }
+            }
+            __syncwarp();
+            if (lane == 0 && ok && issued == q + slots && down_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+            issued = __shfl_sync(0xffffffffu, issued, 0);
+        }
+    }
+    for (int d = done; d < issued; ++d) mbar_wait(rg.bar(d), rg.parity(d), a.err);
+}
+
+constexpr size_t kSmemBudget = 227 * 1024;
+
+// Largest (warps, slots) whose shared memory fits, preferring 8 warps.
+bool pick_config(size_t fixed, size_t slot_bytes, int &nw, int &slots) {
+    for (int w : {8, 4, 2}) {
+        for (int s : {3, 2, 1}) {
+            const size_t need = fixed + (size_t)w * s * slot_bytes + (size_t)w * s * 8 + 128;
+            if (need <= kSmemBudget) {
+                nw = w;
+                slots = s;
+                return true;
             }
         }
     }
-}
-
-template <int MODE, int UPL>
-cudaError_t launch_gateup(const FfnArgs &a, int grid, cudaStream_t st) {
-    const size_t smem = sizeof(float) * kChunkRows * a.H;
-    cudaError_t e = cudaFuncSetAttribute(k_gateup_simt<MODE, UPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    k_gateup_simt<MODE, UPL><<<grid, kWarps * 32, smem, st>>>(a);
-    return cudaGetLastError();
-}
-
-template <int MODE, int UPL>
-cudaError_t launch_down(const FfnArgs &a, int grid, cudaStream_t st) {
-    const size_t smem = sizeof(float) * kChunkRows * max(a.I, a.Is);
-    cudaError_t e = cudaFuncSetAttribute(k_down_simt<MODE, UPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    k_down_simt<MODE, UPL><<<grid, kWarps * 32, smem, st>>>(a);
-    return cudaGetLastError();
+    return false;
 }
 
 template <int MODE>
 cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st) {
-    const int grid = p.num_sms * 4;
+    int nw = 0, slots = 0;
     if (part == 0) {
-        const int upl_h = (a.H / 32 + 31) / 32;
-        if (upl_h <= 1) return launch_gateup<MODE, 1>(a, grid, st);
-        if (upl_h <= 2) return launch_gateup<MODE, 2>(a, grid, st);
-        if (upl_h <= 4) return launch_gateup<MODE, 4>(a, grid, st);
-        return launch_gateup<MODE, 8>(a, grid, st);
+        const size_t fixed = (size_t)kChunkRows * a.H * 4, slot = (size_t)a.H + a.H / 8;
+        if (!pick_config(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
+        const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
+        cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        k_gateup_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
+        return cudaGetLastError();
     }
-    const int upl_i = (max(a.I, a.Is) / 32 + 31) / 32;
-    if (upl_i <= 1) return launch_down<MODE, 1>(a, grid, st);
-    if (upl_i <= 2) return launch_down<MODE, 2>(a, grid, st);
-    if (upl_i <= 4) return launch_down<MODE, 4>(a, grid, st);
-    return launch_down<MODE, 8>(a, grid, st);
+    const int Imax = max(a.I, a.Is);
+    const size_t fixed = (size_t)kChunkRows * Imax * 4, slot = (size_t)kDownRows * (Imax / 2 + Imax / 16);
+    if (!pick_config(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
+    const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
+    cudaError_t e = cudaFuncSetAttribute(k_down_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_down_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -426,6 +512,7 @@ cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtr
     a.h_amax = &p.scratch->h_amax;
     a.hs_amax = &p.scratch->hs_amax;
     a.acc = p.acc;
+    a.err = p.err;
     a.r = routed;
     if (shared) a.s = *shared;
     else a.s = routed;

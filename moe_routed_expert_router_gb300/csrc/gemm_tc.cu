@@ -38,7 +38,6 @@ constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
 constexpr int kStageBytes = 3 * kTile + 5 * kSf;
 constexpr int kThreads = 192;
-constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single wait
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
 
@@ -67,63 +66,11 @@ struct TcArgs {
     int *err;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ uint64_t now_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Wait for the phase of `bar` with the given parity; false (and the timeout
-// bit set) if it has not completed within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
-    if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = now_ns();
-    while (!mbar_test(bar, parity)) {
-        if (now_ns() - t0 > kWaitNs) {
-            atomicOr(err, kErrTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
     asm volatile(
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
         ::"r"(smem_u32(dst)), "l"(map), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
-}
-
-__device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -203,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
     uint64_t *empty = full + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 1;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(acc_empty + 1);
+    uint64_t *drain = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = a.scratch->n_tiles * a.nf;
@@ -215,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
+        mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -232,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             int s = 0;
             uint32_t ph = 0;
             bool ok = true;
+            uint32_t used = 0, last_ph = 0;  // stages loaded at least once, parity of their last load
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item(a, item, EPI, it)) continue;
@@ -257,9 +207,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     tma_2d(st + 3 * kTile, &a.s0[m], full + s, ks * 16, r0);
                     tma_2d(st + 3 * kTile + kSf, S1, full + s, ks * 16, r1);
                     bulk_copy(st + 3 * kTile + 4 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
+                    used |= 1u << s;
+                    last_ph = (last_ph & ~(1u << s)) | (ph << s);
                     if (++s == kStages) { s = 0; ph ^= 1; }
                 }
             }
+            // every load has landed before the block exits (already true unless a wait ran out)
+            for (int t = 0; t < kStages; ++t)
+                if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
         }
     } else if (warp == 1) {
         // ------------------------------------------------ scale re-layout + MMA issue
@@ -320,6 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             if (lane == 0) mma_commit(acc_full);
             __syncwarp();
         }
+        // all issued MMAs / copies complete before the accumulators are freed
+        if (lane == 0) mma_commit(drain);
+        __syncwarp();
+        mbar_wait(drain, 0, a.err);
     } else {
         // ------------------------------------------------ epilogue (warps 2..5)
         const int quad = warp & 3;

@@ -13,83 +13,225 @@ namespace {
 // Logits in the fixed order: lane l of a warp owns the 8-value chunks c of H
 // with c mod 32 == l and sums fmaf over them in increasing h; the lane sums are
 // combined with an xor butterfly (16, 8, 4, 2, 1); the bias is added last.
-// A warp computes a TT x TE tile (tokens x experts); the block holds 4 warps
-// side by side along the experts.  The blocks with blockIdx.x == 0 also check
-// that x is finite and, for W4A4, fold x into the batch amax.
-template <int TT, int TE>
-__global__ void __launch_bounds__(128) k_router_logits(const uint16_t *__restrict__ x, int T, int H,
-                                                       const float *__restrict__ rw, const float *__restrict__ bias,
-                                                       int E, float *__restrict__ logits, int *err,
-                                                       unsigned int *x_amax) {
+// Every kernel below keeps exactly this order, whatever its tiling.
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &q, float (&v)[8]) {
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __uint_as_float(u[j] << 16);
+        v[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+    }
+}
+
+__device__ __forceinline__ bool bf16x8_bad(const uint4 &q) {
+    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) bad |= ((u[j] & 0x7F80u) == 0x7F80u) | ((u[j] & 0x7F800000u) == 0x7F800000u);
+    return bad;
+}
+
+__device__ __forceinline__ float bf16x8_amax(const uint4 &q) {
+    float v[8];
+    bf16x8_to_f32(q, v);
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+    return m;
+}
+
+__device__ __forceinline__ void butterfly_store(float v, int lane, float *dst, const float *bias, int e) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) *dst = bias ? v + bias[e] : v;
+}
+
+// Small batches: one warp per (expert, group of TT tokens); U chunks' loads
+// are issued before their multiply-adds.  Warps with token group 0 of expert 0
+// also check x and fold it into the batch amax.
+template <int TT, int U>
+__global__ void __launch_bounds__(256) k_router_small(const uint16_t *__restrict__ x, int T, int H,
+                                                      const float *__restrict__ rw, const float *__restrict__ bias,
+                                                      int E, float *__restrict__ logits, int *err,
+                                                      unsigned int *x_amax) {
     const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int e0 = (blockIdx.x * 4 + warp) * TE;
-    const int t0 = blockIdx.y * TT;
-    const bool check = (blockIdx.x == 0);
-    float acc[TT][TE];
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int ntg = (T + TT - 1) / TT;
+    const int e = gw / ntg, t0 = (gw % ntg) * TT;
+    if (e >= E) return;
+    const bool check = (e == 0);
+    float acc[TT];
 #pragma unroll
-    for (int t = 0; t < TT; ++t)
-#pragma unroll
-        for (int e = 0; e < TE; ++e) acc[t][e] = 0.0f;
+    for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
     bool bad = false;
     float amax = 0.0f;
     const int nchunk = H >> 3;
-    for (int c = lane; c < nchunk; c += 32) {
-        float w[TE][8];
+    const float *wrow = rw + (size_t)e * H;
+    for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
+        float4 w[U][2];
+        uint4 xq[U][TT];
 #pragma unroll
-        for (int e = 0; e < TE; ++e) {
-            if (e0 + e < E) {
-                const float4 *p = reinterpret_cast<const float4 *>(rw + (size_t)(e0 + e) * H + c * 8);
-                float4 a = __ldg(p), b = __ldg(p + 1);
-                w[e][0] = a.x; w[e][1] = a.y; w[e][2] = a.z; w[e][3] = a.w;
-                w[e][4] = b.x; w[e][5] = b.y; w[e][6] = b.z; w[e][7] = b.w;
-            } else {
+        for (int u = 0; u < U; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < nchunk) {
+                const float4 *p = reinterpret_cast<const float4 *>(wrow + c * 8);
+                w[u][0] = __ldg(p);
+                w[u][1] = __ldg(p + 1);
 #pragma unroll
-                for (int j = 0; j < 8; ++j) w[e][j] = 0.0f;
+                for (int t = 0; t < TT; ++t)
+                    if (t0 + t < T) xq[u][t] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * H + c * 8));
             }
         }
 #pragma unroll
-        for (int t = 0; t < TT; ++t) {
-            if (t0 + t >= T) continue;
-            uint4 q = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * H + c * 8));
-            uint32_t u[4] = {q.x, q.y, q.z, q.w};
-            float xv[8];
+        for (int u = 0; u < U; ++u) {
+            if (c0 + 32 * u >= nchunk) break;
+            const float wv[8] = {w[u][0].x, w[u][0].y, w[u][0].z, w[u][0].w, w[u][1].x, w[u][1].y, w[u][1].z, w[u][1].w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                xv[2 * j] = __uint_as_float(u[j] << 16);
-                xv[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+            for (int t = 0; t < TT; ++t) {
+                if (t0 + t >= T) continue;
+                float xv[8];
+                bf16x8_to_f32(xq[u][t], xv);
                 if (check) {
-                    bad |= ((u[j] & 0x7F80u) == 0x7F80u) | ((u[j] & 0x7F800000u) == 0x7F800000u);
-                    amax = fmaxf(amax, fmaxf(fabsf(xv[2 * j]), fabsf(xv[2 * j + 1])));
+                    bad |= bf16x8_bad(xq[u][t]);
+                    amax = fmaxf(amax, bf16x8_amax(xq[u][t]));
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[t] = fmaf(xv[j], wv[j], acc[t]);
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-#pragma unroll
-                for (int e = 0; e < TE; ++e) acc[t][e] = fmaf(xv[j], w[e][j], acc[t][e]);
         }
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t)
+        if (t0 + t < T) butterfly_store(acc[t], lane, logits + (size_t)(t0 + t) * E + e, bias, e);
+    if (check) {
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
+        if (x_amax) {
+            amax = warp_max(amax);
+            if (lane == 0) atomic_max_nonneg(x_amax, amax);
+        }
+    }
+}
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
+    const uint32_t d = smem_u32(dst);
+    const int n = valid ? 16 : 0;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
+}
+
+// Large batches: a block computes 16 tokens x 32 experts with 8 warps (2 x 4
+// sub-tiles of 8 x 8).  Slabs of 256 H positions of x (bf16) and of the router
+// weight (fp32) are double-buffered in shared memory with cp.async; in every
+// slab lane l handles chunk l, so each lane still walks its chunks l, l+32, ...
+// in increasing order.  The weight slab is stored as [expert][half][chunk][4]
+// so the lanes' 16-byte reads are conflict-free.
+constexpr int kRT = 16, kRE = 32;
+constexpr int kRouterTiledSmem = 2 * kRT * 32 * 16 + 2 * kRE * 2 * 32 * 16;
+
+__global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
+                                                      const float *__restrict__ rw, const float *__restrict__ bias,
+                                                      int E, float *__restrict__ logits, int *err,
+                                                      unsigned int *x_amax) {
+    extern __shared__ __align__(16) uint4 rsmem[];
+    uint4 (*xs)[kRT][32] = reinterpret_cast<uint4 (*)[kRT][32]>(rsmem);                 // [2][16][32]: 2 x 8 KB
+    float4 (*ws)[kRE][2][32] = reinterpret_cast<float4 (*)[kRE][2][32]>(rsmem + 2 * kRT * 32);  // [2][32][2][32]: 2 x 32 KB
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRE;
+    const int tw = (warp >> 2) * 8, ew = (warp & 3) * 8;
+    const int slabs = H / 256;
+    const bool check = (blockIdx.x == 0) && ((warp & 3) == 0);
+    auto load = [&](int s, int b) {
 #pragma unroll
-        for (int e = 0; e < TE; ++e) {
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+            const bool v = t0 + row < T;
+            cp_async16(&xs[b][row][c], x + (size_t)(v ? t0 + row : 0) * H + s * 256 + c * 8, v);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = tid + 256 * i, row = idx >> 6, c = (idx >> 1) & 31, half = idx & 1;
+            const bool v = e0 + row < E;
+            cp_async16(&ws[b][row][half][c], rw + (size_t)(v ? e0 + row : 0) * H + s * 256 + c * 8 + half * 4, v);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    float acc[8][8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+    bool bad = false;
+    float amax = 0.0f;
+    load(0, 0);
+    for (int s = 0; s < slabs; ++s) {
+        const int b = s & 1;
+        if (s + 1 < slabs) {
+            load(s + 1, b ^ 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        uint4 xq[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) xq[t] = xs[b][tw + t][lane];
+        if (check) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+                if (t0 + tw + t < T) {
+                    bad |= bf16x8_bad(xq[t]);
+                    amax = fmaxf(amax, bf16x8_amax(xq[t]));
+                }
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            float xv[8][4];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const uint32_t lo = half ? xq[t].z : xq[t].x, hi = half ? xq[t].w : xq[t].y;
+                xv[t][0] = __uint_as_float(lo << 16);
+                xv[t][1] = __uint_as_float(lo & 0xFFFF0000u);
+                xv[t][2] = __uint_as_float(hi << 16);
+                xv[t][3] = __uint_as_float(hi & 0xFFFF0000u);
+            }
+            float4 wv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wv[e] = ws[b][ew + e][half][lane];
+#pragma unroll
+            for (int t = 0; t < 8; ++t)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    acc[t][e] = fmaf(xv[t][0], wv[e].x, acc[t][e]);
+                    acc[t][e] = fmaf(xv[t][1], wv[e].y, acc[t][e]);
+                    acc[t][e] = fmaf(xv[t][2], wv[e].z, acc[t][e]);
+                    acc[t][e] = fmaf(xv[t][3], wv[e].w, acc[t][e]);
+                }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
             float v = acc[t][e];
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
             acc[t][e] = v;
         }
-    if (lane == 0) {
+    // lane j writes the pairs (t, e) with t * 8 + e == j or j + 32
 #pragma unroll
-        for (int t = 0; t < TT; ++t)
+    for (int k2 = 0; k2 < 2; ++k2) {
+        const int j = lane + 32 * k2, t = j >> 3, e = j & 7;
+        float v = 0.f;
 #pragma unroll
-            for (int e = 0; e < TE; ++e)
-                if (t0 + t < T && e0 + e < E) {
-                    float v = acc[t][e];
-                    if (bias) v = v + bias[e0 + e];
-                    logits[(size_t)(t0 + t) * E + e0 + e] = v;
-                }
+        for (int tt = 0; tt < 8; ++tt)
+#pragma unroll
+            for (int ee = 0; ee < 8; ++ee)
+                if (tt == t && ee == e) v = acc[tt][ee];
+        const int tg = t0 + tw + t, eg = e0 + ew + e;
+        if (tg < T && eg < E) logits[(size_t)tg * E + eg] = bias ? v + bias[eg] : v;
     }
-    if (check && warp == 0) {
+    if (check) {
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
         if (x_amax) {
             amax = warp_max(amax);
@@ -326,6 +468,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
     if (tid == 0) {
         scratch->n_tiles = s_tb[E + 1];
         scratch->n_chunks = s_cb[E + 1];
+        scratch->n_chunks_routed = s_cb[E];
         int na = 0;
         for (int e = 0; e < E; ++e) na += (s_off[e + 1] > s_off[e]);
         scratch->n_active = na;
@@ -339,15 +482,13 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     const int H = p.cfg.hidden, E = p.cfg.num_experts;
     unsigned int *amax = (p.cfg.mode == MOE_W4A4) ? &p.scratch->x_amax : nullptr;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
-    if (T <= 4) {
-        dim3 g((E + 3) / 4, (T + 3) / 4);
-        k_router_logits<4, 1><<<g, 128, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
-    } else if (T <= 16) {
-        dim3 g((E + 3) / 4, (T + 15) / 16);
-        k_router_logits<16, 1><<<g, 128, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
+    if (T <= 32) {
+        const int ntg = (T + 1) / 2;
+        const int warps = E * ntg;
+        k_router_small<2, 4><<<(warps + 7) / 8, 256, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
     } else {
-        dim3 g((E + 31) / 32, (T + 7) / 8);
-        k_router_logits<8, 8><<<g, 128, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
+        dim3 g((E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
+        k_router_tiled<<<g, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -368,6 +509,8 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
 size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (size_t)E + 8); }
 
 cudaError_t configure_group_kernel(int E) {
+    cudaError_t e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(E));
 }
 
