@@ -213,6 +213,14 @@ moe_status moe_plan_set_profiling(moe_plan plan, int32_t enable);
  * the stage executions; clears the record.  Host arrays; any may be NULL. */
 moe_status moe_plan_read_profile(moe_plan plan, float *ms, int64_t *launches, int64_t *calls);
 
+/* Failure-detection check: launch one block whose waits use the same bounded
+ * mbarrier wait as the expert kernels, on a barrier nothing will arrive on,
+ * with the bound set to `wait_ns` nanoseconds (at most one second).  The wait
+ * runs out, the kernel records MOE_ERR_TIMEOUT in the plan's error word and
+ * returns normally; moe_plan_sync_status then reports it and the context stays
+ * usable.  Faults nothing and hangs nothing. */
+moe_status moe_plan_check_timeout(moe_plan plan, int64_t wait_ns, void *stream);
+
 /* Text of a status code (static storage). */
 const char *moe_status_string(moe_status s);
 

@@ -397,6 +397,11 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream) {
     return MOE_OK;
 }
 
+moe_status moe_plan_check_timeout(moe_plan plan, int64_t wait_ns, void *stream) {
+    if (!plan || wait_ns < 0 || wait_ns > 1000000000LL) return MOE_ERR_INVALID_ARG;
+    return cuda_status(moe::launch_wait_check(plan->p.err, (uint64_t)wait_ns, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes) {
     if (!plan || !name || !ptr) return MOE_ERR_INVALID_ARG;
     const Plan &p = plan->p;

@@ -37,7 +37,8 @@ constexpr int kRowBytes = kBK / 2;        // 128 code bytes per row per stage
 constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
 constexpr int kStageBytes = 3 * kTile + 5 * kSf;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                      // two per 32-lane TMEM quadrant
+constexpr int kThreads = 32 * (3 + kEpiWarps);    // producer, MMA, scale re-layout, epilogue
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
 
@@ -46,7 +47,7 @@ struct TcArgs {
     CUtensorMap a1[2];      // up codes (G1) / unused (G2: second half of down rows from a0)
     CUtensorMap s0[2];      // plain scale tiles matching a0
     CUtensorMap s1[2];      // matching a1
-    CUtensorMap b;          // token rows: Xp codes (G1) / SwiGLU codes (G2), [rows][Kb]
+    CUtensorMap b[3];       // token rows: Xp codes (G1) / SwiGLU codes (G2), boxes of 32, 64, 128 rows
     const uint8_t *b_atoms; // token-row scales in the tensor-core layout
     int b_atoms_per_block;  // 512-byte atoms per 128-row block (= row length / 64)
     const int4 *tiles;      // {expert (E = shared), first padded row, valid rows, 0}
@@ -87,16 +88,22 @@ __device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
 }
 
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1, UE4M3 scales, K-major,
-// M = 128, N = 128.
-constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+// M = 128, N = n (a multiple of 16).
+__device__ __forceinline__ uint32_t idesc_fp4(uint32_t n) {
+    return (1u << 7) | (1u << 10) | ((n >> 3) << 17) | (0u << 23) | ((128u >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb, uint32_t acc) {
+__device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-        ::"r"(d), "l"(a), "l"(b), "r"(kIdesc), "r"(acc), "r"(sfa), "r"(sfb)
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
         : "memory");
 }
+
+// Token rows a tile loads and multiplies: 32, 64 or 128 (index into TcArgs::b).
+__device__ __forceinline__ int rows_class(int valid) { return valid <= 32 ? 0 : (valid <= 64 ? 1 : 2); }
 
 __device__ __forceinline__ void sf_copy(uint32_t taddr, uint64_t desc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
@@ -147,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
-    uint64_t *empty = full + kStages;
+    uint64_t *sf_ready = full + kStages;
+    uint64_t *empty = sf_ready + kStages;
     uint64_t *acc_full = empty + kStages;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
@@ -159,10 +167,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
+            mbar_init(sf_ready + s, 1);
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        mbar_init(acc_empty, kEpiWarps);
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -195,15 +204,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 }
                 const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
                 const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
+                const int rc = rows_class(it.valid);
+                const uint32_t b_bytes = (32u << rc) * kRowBytes;
                 const uint8_t *batoms = a.b_atoms + (size_t)(it.row0 / 128) * a.b_atoms_per_block * 512;
                 const int ks_n = it.K / kBK;
                 for (int ks = 0; ks < ks_n; ++ks) {
                     if (!mbar_wait(empty + s, ph ^ 1, a.err)) { ok = false; break; }
                     uint8_t *st = smem + s * kStageBytes;
-                    mbar_expect_tx(full + s, 3 * kTile + 3 * kSf);
+                    mbar_expect_tx(full + s, 2 * kTile + b_bytes + 3 * kSf);
                     tma_2d(st, &a.a0[m], full + s, ks * kRowBytes, r0);
                     tma_2d(st + kTile, A1, full + s, ks * kRowBytes, r1);
-                    tma_2d(st + 2 * kTile, &a.b, full + s, ks * kRowBytes, it.row0);
+                    tma_2d(st + 2 * kTile, &a.b[rc], full + s, ks * kRowBytes, it.row0);
                     tma_2d(st + 3 * kTile, &a.s0[m], full + s, ks * 16, r0);
                     tma_2d(st + 3 * kTile + kSf, S1, full + s, ks * 16, r1);
                     bulk_copy(st + 3 * kTile + 4 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
@@ -216,24 +227,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             for (int t = 0; t < kStages; ++t)
                 if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ scale re-layout + MMA issue
+    } else if (warp == 2) {
+        // ------------------------------------------------ weight scale re-layout
+        // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each: the 4
+        // scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
         int s = 0;
-        uint32_t ph = 0, aph = 0;
-        bool ok = true;
-        const uint32_t d0 = tmem, d1 = tmem + 128;
-        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        uint32_t ph = 0;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             Item it;
             if (!decode_item(a, item, EPI, it)) continue;
-            if (!mbar_wait(acc_empty, aph ^ 1, a.err)) break;
-            aph ^= 1;
-            tc_fence_after();
             const int ks_n = it.K / kBK;
+            bool ok = true;
             for (int ks = 0; ks < ks_n; ++ks) {
                 if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
                 uint8_t *st = smem + s * kStageBytes;
-                // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each: the
-                // 4 scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
 #pragma unroll
                 for (int op = 0; op < 2; ++op) {
                     const uint4 *src = reinterpret_cast<const uint4 *>(st + 3 * kTile + op * kSf);
@@ -248,9 +255,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) {
+                if (lane == 0) mbar_arrive(sf_ready + s);
+                if (++s == kStages) { s = 0; ph ^= 1; }
+            }
+            if (!ok) break;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue (one lane)
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0, aph = 0;
+            bool ok = true;
+            const uint32_t d0 = tmem, d1 = tmem + 128;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item(a, item, EPI, it)) continue;
+                if (!mbar_wait(acc_empty, aph ^ 1, a.err)) break;
+                aph ^= 1;
+                tc_fence_after();
+                const uint32_t idesc = idesc_fp4(32u << rows_class(it.valid));
+                const int ks_n = it.K / kBK;
+                for (int ks = 0; ks < ks_n; ++ks) {
+                    if (!mbar_wait(sf_ready + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t base = smem_u32(st);
+                    const uint32_t base = smem_u32(smem + s * kStageBytes);
                     const uint32_t at0 = base + 3 * kTile + 2 * kSf, at1 = at0 + kSf, atb = at0 + 2 * kSf;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -262,26 +290,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks | kk) ? 1u : 0u;
                         const uint64_t bd = desc_sw128(base + 2 * kTile + 32 * kk);
-                        mma_fp4(d0, desc_sw128(base + 32 * kk), bd, tmem + 256 + 4 * kk, tmem + 288 + 4 * kk, accum);
-                        mma_fp4(d1, desc_sw128(base + kTile + 32 * kk), bd, tmem + 272 + 4 * kk, tmem + 288 + 4 * kk,
+                        mma_fp4(d0, desc_sw128(base + 32 * kk), bd, idesc, tmem + 256 + 4 * kk, tmem + 288 + 4 * kk,
                                 accum);
+                        mma_fp4(d1, desc_sw128(base + kTile + 32 * kk), bd, idesc, tmem + 272 + 4 * kk,
+                                tmem + 288 + 4 * kk, accum);
                     }
                     mma_commit(empty + s);
+                    if (++s == kStages) { s = 0; ph ^= 1; }
                 }
-                __syncwarp();
-                if (++s == kStages) { s = 0; ph ^= 1; }
+                if (!ok) break;
+                mma_commit(acc_full);
             }
-            if (!ok) break;
-            if (lane == 0) mma_commit(acc_full);
-            __syncwarp();
+            // all issued MMAs / copies complete before the accumulators are freed
+            mma_commit(drain);
+            mbar_wait(drain, 0, a.err);
         }
-        // all issued MMAs / copies complete before the accumulators are freed
-        if (lane == 0) mma_commit(drain);
-        __syncwarp();
-        mbar_wait(drain, 0, a.err);
     } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int quad = warp & 3;
+        // ------------------------------------------------ epilogue (8 warps)
+        const int quad = warp & 3;                 // TMEM lanes this warp may read
+        const int col0 = ((warp - 3) >> 2) * 64;   // its half of the token columns
         uint32_t aph = 0;
         float lmax = 0.0f, lmax_s = 0.0f;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -293,20 +320,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
             const int m = it.sh ? 1 : 0;
             const int e = it.sh ? 0 : it.e;
+            const int n_end = min(col0 + 64, it.valid);
             if (EPI == kSwiGLU) {
                 const float xts = __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
                 const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
                 const int feat = it.f * 128 + quad * 32 + lane;
                 float mx = 0.0f;
-                for (int n0 = 0; n0 < 128 && n0 < it.valid; n0 += 16) {
+                for (int n0 = col0; n0 < n_end; n0 += 16) {
                     float g[16], u[16];
                     tmem_ld16(lane_base + n0, g);
                     tmem_ld16(lane_base + 128 + n0, u);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        if (n0 + j < it.valid) {
+                        if (n0 + j < n_end) {
                             const float gv = g[j] * sg, uv = u[j] * su;
-                            const float h = gv / (1.0f + expf(-gv)) * uv;
+                            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
                             a.hbuf[(size_t)(it.row0 + n0 + j) * a.hstride + feat] = h;
                             mx = fmaxf(mx, fabsf(h));
                         }
@@ -316,12 +344,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 else lmax = fmaxf(lmax, mx);
             } else {
                 const float ds = a.ts_a0[m][e] * a.b_ts[m];
-                // column n's token and routing weight, spread over the lanes
-                int tok[4];
-                float wgt[4];
+                // columns col0 + lane and col0 + 32 + lane: token and routing weight
+                int tok[2];
+                float wgt[2];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int n = lane + 32 * q;
+                for (int q = 0; q < 2; ++q) {
+                    const int n = col0 + lane + 32 * q;
                     tok[q] = 0;
                     wgt[q] = 0.0f;
                     if (n < it.valid) {
@@ -331,19 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     }
                 }
                 const int j0 = it.f * 256 + quad * 32 + lane;
-                for (int n0 = 0; n0 < 128 && n0 < it.valid; n0 += 16) {
+                for (int n0 = col0; n0 < n_end; n0 += 16) {
                     float y0[16], y1[16];
                     tmem_ld16(lane_base + n0, y0);
                     tmem_ld16(lane_base + 128 + n0, y1);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int n = n0 + j;
-                        const int t = __shfl_sync(0xffffffffu, tok[n >> 5], n & 31);
-                        const float wv = __shfl_sync(0xffffffffu, wgt[n >> 5], n & 31);
-                        if (n < it.valid) {
+                        const int n = n0 + j, c = n - col0;
+                        const int t = __shfl_sync(0xffffffffu, tok[c >> 5], c & 31);
+                        const float wv = __shfl_sync(0xffffffffu, wgt[c >> 5], c & 31) * ds;
+                        if (n < n_end) {
                             float *dst = a.acc + (size_t)t * a.H + j0;
-                            atomicAdd(dst, y0[j] * ds * wv);
-                            atomicAdd(dst + 128, y1[j] * ds * wv);
+                            atomicAdd(dst, y0[j] * wv);
+                            atomicAdd(dst + 128, y1[j] * wv);
                         }
                     }
                 }
@@ -430,7 +458,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t row
     return r == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = kStages * kStageBytes + 256 + 1024;
+constexpr size_t kSmemBytes = kStages * kStageBytes + 512 + 1024;
 
 }  // namespace
 
@@ -491,7 +519,7 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *, int T, const ExpertPtrs &
         ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
         ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
-        ok &= make_map(&a.b, p.xp, H / 2, p.rows_pad_max, H / 2, 128, 128, true);
+        for (int c = 0; c < 3; ++c) ok &= make_map(&a.b[c], p.xp, H / 2, p.rows_pad_max, H / 2, 128, 32u << c, true);
         a.b_atoms = p.xp_atoms;
         a.b_atoms_per_block = H / 64;
         a.nf = Imax / 128;
@@ -511,7 +539,7 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *, int T, const ExpertPtrs &
     a.a1[1] = a.a0[1];
     a.s1[0] = a.s0[0];
     a.s1[1] = a.s0[1];
-    ok &= make_map(&a.b, p.hq, Imax / 2, p.rows_pad_max, Imax / 2, 128, 128, true);
+    for (int c = 0; c < 3; ++c) ok &= make_map(&a.b[c], p.hq, Imax / 2, p.rows_pad_max, Imax / 2, 128, 32u << c, true);
     a.b_atoms = p.hq_atoms;
     a.b_atoms_per_block = Imax / 64;
     a.nf = H / 256;

@@ -211,12 +211,12 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity; false (and the timeout
-// bit set) if it has not completed within kWaitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+// bit set) if it has not completed within `limit_ns` (kWaitNs by default).
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err, uint64_t limit_ns = kWaitNs) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = now_ns();
     while (!mbar_test(bar, parity)) {
-        if (now_ns() - t0 > kWaitNs) {
+        if (now_ns() - t0 > limit_ns) {
             atomicOr(err, kErrTimeout);
             return false;
         }
@@ -250,5 +250,6 @@ cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtr
                             const ExpertPtrs *shared, int part, cudaStream_t st);
 cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st);
 cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st);
+cudaError_t launch_wait_check(int *err, uint64_t limit_ns, cudaStream_t st);
 
 }  // namespace moe

@@ -162,6 +162,17 @@ __global__ void __launch_bounds__(kThreads) k_finalize(float4 *__restrict__ acc,
     }
 }
 
+// One block waits on an mbarrier that nothing arrives on, through the same
+// bounded wait the pipelined kernels use: the bound runs out and the timeout
+// bit is set.
+__global__ void k_wait_check(int *err, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    __syncthreads();
+    mbar_wait(&bar, 0, err, limit_ns);
+}
+
 int grid_for(int64_t work, int num_sms) {
     int64_t g = (work + kThreads - 1) / kThreads;
     int64_t cap = (int64_t)num_sms * 8;
@@ -214,6 +225,11 @@ cudaError_t launch_quant_nvfp4(const float *w, int batch, int rows, int cols, ui
     k_quant_f32<<<grid_for(per / 16 * batch, sms), kThreads, 0, st>>>(
         w, per / 16, batch, reinterpret_cast<const unsigned int *>(ts), reinterpret_cast<uint2 *>(codes), scales);
     k_ts_finalize<<<(batch + 255) / 256, 256, 0, st>>>(ts, batch);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wait_check(int *err, uint64_t limit_ns, cudaStream_t st) {
+    k_wait_check<<<1, 32, 0, st>>>(err, limit_ns);
     return cudaGetLastError();
 }
 

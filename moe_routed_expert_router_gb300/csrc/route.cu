@@ -10,107 +10,18 @@
 namespace moe {
 namespace {
 
-// Logits in the fixed order: lane l of a warp owns the 8-value chunks c of H
-// with c mod 32 == l and sums fmaf over them in increasing h; the lane sums are
-// combined with an xor butterfly (16, 8, 4, 2, 1); the bias is added last.
-// Every kernel below keeps exactly this order, whatever its tiling.
+// Logits in the fixed order: position h of H belongs to lane h mod 32 of a
+// warp, which sums fmaf over its positions in increasing h starting from +0;
+// the 32 lane sums are combined with an xor butterfly (16, 8, 4, 2, 1); the
+// bias is added last.  Every kernel below keeps exactly this order, whatever
+// its tiling: x and the router weight are staged in shared memory so that lane
+// l reads position 32j + l of every 32-position group.
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &q, float (&v)[8]) {
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        v[2 * j] = __uint_as_float(u[j] << 16);
-        v[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
-    }
-}
+__device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
 
-__device__ __forceinline__ bool bf16x8_bad(const uint4 &q) {
-    const uint32_t u[4] = {q.x, q.y, q.z, q.w};
-    bool bad = false;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) bad |= ((u[j] & 0x7F80u) == 0x7F80u) | ((u[j] & 0x7F800000u) == 0x7F800000u);
-    return bad;
-}
-
-__device__ __forceinline__ float bf16x8_amax(const uint4 &q) {
-    float v[8];
-    bf16x8_to_f32(q, v);
-    float m = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
-    return m;
-}
-
-__device__ __forceinline__ void butterfly_store(float v, int lane, float *dst, const float *bias, int e) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
-    if (lane == 0) *dst = bias ? v + bias[e] : v;
-}
-
-// Small batches: one warp per (expert, group of TT tokens); U chunks' loads
-// are issued before their multiply-adds.  Warps with token group 0 of expert 0
-// also check x and fold it into the batch amax.
-template <int TT, int U>
-__global__ void __launch_bounds__(256) k_router_small(const uint16_t *__restrict__ x, int T, int H,
-                                                      const float *__restrict__ rw, const float *__restrict__ bias,
-                                                      int E, float *__restrict__ logits, int *err,
-                                                      unsigned int *x_amax) {
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const int ntg = (T + TT - 1) / TT;
-    const int e = gw / ntg, t0 = (gw % ntg) * TT;
-    if (e >= E) return;
-    const bool check = (e == 0);
-    float acc[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
-    bool bad = false;
-    float amax = 0.0f;
-    const int nchunk = H >> 3;
-    const float *wrow = rw + (size_t)e * H;
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * U) {
-        float4 w[U][2];
-        uint4 xq[U][TT];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int c = c0 + 32 * u;
-            if (c < nchunk) {
-                const float4 *p = reinterpret_cast<const float4 *>(wrow + c * 8);
-                w[u][0] = __ldg(p);
-                w[u][1] = __ldg(p + 1);
-#pragma unroll
-                for (int t = 0; t < TT; ++t)
-                    if (t0 + t < T) xq[u][t] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + t) * H + c * 8));
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (c0 + 32 * u >= nchunk) break;
-            const float wv[8] = {w[u][0].x, w[u][0].y, w[u][0].z, w[u][0].w, w[u][1].x, w[u][1].y, w[u][1].z, w[u][1].w};
-#pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                if (t0 + t >= T) continue;
-                float xv[8];
-                bf16x8_to_f32(xq[u][t], xv);
-                if (check) {
-                    bad |= bf16x8_bad(xq[u][t]);
-                    amax = fmaxf(amax, bf16x8_amax(xq[u][t]));
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[t] = fmaf(xv[j], wv[j], acc[t]);
-            }
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-        if (t0 + t < T) butterfly_store(acc[t], lane, logits + (size_t)(t0 + t) * E + e, bias, e);
-    if (check) {
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
-        if (x_amax) {
-            amax = warp_max(amax);
-            if (lane == 0) atomic_max_nonneg(x_amax, amax);
-        }
-    }
+__device__ __forceinline__ bool bf16x2_bad(uint32_t u) {
+    return ((u & 0x7F80u) == 0x7F80u) | ((u & 0x7F800000u) == 0x7F800000u);
 }
 
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
@@ -119,47 +30,42 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool vali
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
 }
 
-// Large batches: a block computes 16 tokens x 32 experts with 8 warps (2 x 4
-// sub-tiles of 8 x 8).  Slabs of 256 H positions of x (bf16) and of the router
-// weight (fp32) are double-buffered in shared memory with cp.async; in every
-// slab lane l handles chunk l, so each lane still walks its chunks l, l+32, ...
-// in increasing order.  The weight slab is stored as [expert][half][chunk][4]
-// so the lanes' 16-byte reads are conflict-free.
-constexpr int kRT = 16, kRE = 32;
-constexpr int kRouterTiledSmem = 2 * kRT * 32 * 16 + 2 * kRE * 2 * 32 * 16;
+// Small batches (T <= 16): 8 warps a block, warp w takes expert
+// e0 + w / ntg and tokens (w % ntg) * 8 .. +8, ntg = ceil(T / 8).  Slabs of
+// 256 positions of the block's router rows and of x are double-buffered in
+// shared memory (cp.async); every lane then reads its positions from there.
+constexpr int kSmallSlab = 256;
 
-__global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
+__global__ void __launch_bounds__(256) k_router_small(const uint16_t *__restrict__ x, int T, int H,
                                                       const float *__restrict__ rw, const float *__restrict__ bias,
                                                       int E, float *__restrict__ logits, int *err,
                                                       unsigned int *x_amax) {
-    extern __shared__ __align__(16) uint4 rsmem[];
-    uint4 (*xs)[kRT][32] = reinterpret_cast<uint4 (*)[kRT][32]>(rsmem);                 // [2][16][32]: 2 x 8 KB
-    float4 (*ws)[kRE][2][32] = reinterpret_cast<float4 (*)[kRE][2][32]>(rsmem + 2 * kRT * 32);  // [2][32][2][32]: 2 x 32 KB
+    __shared__ __align__(16) float wsm[2][8][kSmallSlab];        // 16 KB
+    __shared__ __align__(16) uint16_t xsm[2][16][kSmallSlab];    // 16 KB
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRE;
-    const int tw = (warp >> 2) * 8, ew = (warp & 3) * 8;
-    const int slabs = H / 256;
-    const bool check = (blockIdx.x == 0) && ((warp & 3) == 0);
+    const int ntg = (T + 7) / 8, epb = 8 / ntg;
+    const int e0 = blockIdx.x * epb;
+    const int ew = warp / ntg, t0 = (warp % ntg) * 8;
+    const int e = e0 + ew;
+    const int slabs = H / kSmallSlab;
+    const bool check = (blockIdx.x == 0);
     auto load = [&](int s, int b) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
-            const bool v = t0 + row < T;
-            cp_async16(&xs[b][row][c], x + (size_t)(v ? t0 + row : 0) * H + s * 256 + c * 8, v);
+        // router rows: epb rows x 256 floats = epb * 64 chunks of 16 B
+        for (int idx = tid; idx < epb * (kSmallSlab / 4); idx += 256) {
+            const int r = idx / (kSmallSlab / 4), c = idx % (kSmallSlab / 4);
+            const bool v = e0 + r < E;
+            cp_async16(&wsm[b][r][c * 4], rw + (size_t)(v ? e0 + r : 0) * H + s * kSmallSlab + c * 4, v);
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int idx = tid + 256 * i, row = idx >> 6, c = (idx >> 1) & 31, half = idx & 1;
-            const bool v = e0 + row < E;
-            cp_async16(&ws[b][row][half][c], rw + (size_t)(v ? e0 + row : 0) * H + s * 256 + c * 8 + half * 4, v);
+        // x rows: T rows x 256 bf16 = T * 32 chunks
+        for (int idx = tid; idx < T * (kSmallSlab / 8); idx += 256) {
+            const int r = idx / (kSmallSlab / 8), c = idx % (kSmallSlab / 8);
+            cp_async16(&xsm[b][r][c * 8], x + (size_t)r * H + s * kSmallSlab + c * 8, true);
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    float acc[8][8];
+    float acc[8];
 #pragma unroll
-    for (int t = 0; t < 8; ++t)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+    for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
     bool bad = false;
     float amax = 0.0f;
     load(0, 0);
@@ -172,41 +78,144 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
             asm volatile("cp.async.wait_group 0;" ::: "memory");
         }
         __syncthreads();
-        uint4 xq[8];
-#pragma unroll
-        for (int t = 0; t < 8; ++t) xq[t] = xs[b][tw + t][lane];
-        if (check) {
-#pragma unroll
-            for (int t = 0; t < 8; ++t)
-                if (t0 + tw + t < T) {
-                    bad |= bf16x8_bad(xq[t]);
-                    amax = fmaxf(amax, bf16x8_amax(xq[t]));
-                }
-        }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            float xv[8][4];
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-                const uint32_t lo = half ? xq[t].z : xq[t].x, hi = half ? xq[t].w : xq[t].y;
-                xv[t][0] = __uint_as_float(lo << 16);
-                xv[t][1] = __uint_as_float(lo & 0xFFFF0000u);
-                xv[t][2] = __uint_as_float(hi << 16);
-                xv[t][3] = __uint_as_float(hi & 0xFFFF0000u);
+        if (check && warp == 0) {  // x check and amax: warp 0 of block 0 reads every token once
+            for (int idx = lane; idx < T * (kSmallSlab / 2); idx += 32) {
+                const uint32_t u = reinterpret_cast<const uint32_t *>(&xsm[b][0][0])[idx];
+                bad |= bf16x2_bad(u);
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u)), fabsf(bf16_hi(u))));
             }
-            float4 wv[8];
+        }
+        if (e < E) {
+#pragma unroll 4
+            for (int j = 0; j < kSmallSlab / 32; ++j) {
+                const int h = 32 * j + lane;
+                const float wv = wsm[b][ew][h];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = ws[b][ew + e][half][lane];
+                for (int t = 0; t < 8; ++t)
+                    if (t0 + t < T) acc[t] = fmaf(__uint_as_float((uint32_t)xsm[b][t0 + t][h] << 16), wv, acc[t]);
+            }
+        }
+        __syncthreads();
+    }
+    if (e < E) {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            if (t0 + t >= T) break;
+            float v = acc[t];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) logits[(size_t)(t0 + t) * E + e] = bias ? v + bias[e] : v;
+        }
+    }
+    if (check && warp == 0) {
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
+        if (x_amax) {
+            amax = warp_max(amax);
+            if (lane == 0) atomic_max_nonneg(x_amax, amax);
+        }
+    }
+}
+
+// Large batches: a block computes 16 tokens x 32 experts with 8 warps (2 x 4
+// sub-tiles of 8 x 8).  Slabs of 256 positions are staged TRANSPOSED in shared
+// memory -- x as [h][16 tokens] bf16 (48-byte rows), the router weight as
+// [h][32 experts] fp32 (144-byte rows), the paddings keeping the lanes' 16-byte
+// reads conflict-free -- through registers (double-buffered), so that lane l
+// reads the 8 tokens' x and the 8 experts' weights of position 32j + l with one
+// and two 16-byte loads.
+constexpr int kRT = 16, kRE = 32, kRSlab = 256;
+constexpr int kXPitch = 24;    // bf16 per x row (16 used)
+constexpr int kWPitch = 36;    // floats per weight row (32 used)
+constexpr int kRouterTiledSmem = 2 * kRSlab * kXPitch * 2 + 2 * kRSlab * kWPitch * 4;
+
+__global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
+                                                      const float *__restrict__ rw, const float *__restrict__ bias,
+                                                      int E, float *__restrict__ logits, int *err,
+                                                      unsigned int *x_amax) {
+    extern __shared__ __align__(16) uint8_t rsmem[];
+    uint16_t *xT = reinterpret_cast<uint16_t *>(rsmem);                          // [2][256][24]
+    float *wT = reinterpret_cast<float *>(rsmem + 2 * kRSlab * kXPitch * 2);     // [2][256][36]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRE;
+    const int tw = (warp >> 2) * 8, ew = (warp & 3) * 8;
+    const int slabs = H / kRSlab;
+    const bool check = (blockIdx.x == 0);
+    uint4 xr[2];
+    float4 wr[8];
+    bool bad = false;
+    float amax = 0.0f;
+    auto fetch = [&](int s) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {  // 16 tokens x 32 chunks of 8 bf16
+            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+            xr[i] = make_uint4(0, 0, 0, 0);
+            if (t0 + row < T) xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + row) * H + s * kRSlab + c * 8));
+            if (check) {
+                const uint32_t u[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    bad |= bf16x2_bad(u[j]);
+                    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {  // 32 experts x 64 chunks of 4 floats
+            const int idx = tid + 256 * i, row = idx >> 6, c = idx & 63;
+            wr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (e0 + row < E) wr[i] = __ldg(reinterpret_cast<const float4 *>(rw + (size_t)(e0 + row) * H + s * kRSlab + c * 4));
+        }
+    };
+    auto store = [&](int b) {
+        uint16_t *xb = xT + b * kRSlab * kXPitch;
+        float *wb = wT + b * kRSlab * kWPitch;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+            const uint32_t u[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                xb[(c * 8 + 2 * j) * kXPitch + row] = (uint16_t)(u[j] & 0xFFFFu);
+                xb[(c * 8 + 2 * j + 1) * kXPitch + row] = (uint16_t)(u[j] >> 16);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = tid + 256 * i, row = idx >> 6, c = idx & 63;
+            wb[(c * 4 + 0) * kWPitch + row] = wr[i].x;
+            wb[(c * 4 + 1) * kWPitch + row] = wr[i].y;
+            wb[(c * 4 + 2) * kWPitch + row] = wr[i].z;
+            wb[(c * 4 + 3) * kWPitch + row] = wr[i].w;
+        }
+    };
+    float acc[8][8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+    fetch(0);
+    store(0);
+    __syncthreads();
+    for (int s = 0; s < slabs; ++s) {
+        const int b = s & 1;
+        if (s + 1 < slabs) fetch(s + 1);
+        const uint16_t *xb = xT + b * kRSlab * kXPitch;
+        const float *wb = wT + b * kRSlab * kWPitch;
+#pragma unroll 2
+        for (int j = 0; j < kRSlab / 32; ++j) {
+            const int h = 32 * j + lane;
+            const uint4 xq = *reinterpret_cast<const uint4 *>(xb + h * kXPitch + tw);
+            const float4 w0 = *reinterpret_cast<const float4 *>(wb + h * kWPitch + ew);
+            const float4 w1 = *reinterpret_cast<const float4 *>(wb + h * kWPitch + ew + 4);
+            const float xv[8] = {bf16_lo(xq.x), bf16_hi(xq.x), bf16_lo(xq.y), bf16_hi(xq.y),
+                                 bf16_lo(xq.z), bf16_hi(xq.z), bf16_lo(xq.w), bf16_hi(xq.w)};
+            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
             for (int t = 0; t < 8; ++t)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    acc[t][e] = fmaf(xv[t][0], wv[e].x, acc[t][e]);
-                    acc[t][e] = fmaf(xv[t][1], wv[e].y, acc[t][e]);
-                    acc[t][e] = fmaf(xv[t][2], wv[e].z, acc[t][e]);
-                    acc[t][e] = fmaf(xv[t][3], wv[e].w, acc[t][e]);
-                }
+                for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(xv[t], wv[e], acc[t][e]);
         }
+        if (s + 1 < slabs) store(b ^ 1);
         __syncthreads();
     }
 #pragma unroll
@@ -218,7 +227,6 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
             for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
             acc[t][e] = v;
         }
-    // lane j writes the pairs (t, e) with t * 8 + e == j or j + 32
 #pragma unroll
     for (int k2 = 0; k2 < 2; ++k2) {
         const int j = lane + 32 * k2, t = j >> 3, e = j & 7;
@@ -232,6 +240,7 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
         if (tg < T && eg < E) logits[(size_t)tg * E + eg] = bias ? v + bias[eg] : v;
     }
     if (check) {
+        // fold every thread's check into the error word and the amax
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
         if (x_amax) {
             amax = warp_max(amax);
@@ -482,10 +491,9 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     const int H = p.cfg.hidden, E = p.cfg.num_experts;
     unsigned int *amax = (p.cfg.mode == MOE_W4A4) ? &p.scratch->x_amax : nullptr;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
-    if (T <= 32) {
-        const int ntg = (T + 1) / 2;
-        const int warps = E * ntg;
-        k_router_small<2, 4><<<(warps + 7) / 8, 256, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
+    if (T <= 16 && H % kSmallSlab == 0) {
+        const int ntg = (T + 7) / 8, epb = 8 / ntg;
+        k_router_small<<<(E + epb - 1) / epb, 256, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
     } else {
         dim3 g((E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
         k_router_tiled<<<g, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);

@@ -241,7 +241,7 @@ void oracle_router_logits(const uint16_t *x, int32_t T, int32_t H, const float *
             float part[32], next[32];
             for (int l = 0; l < 32; ++l) part[l] = 0.0f;
             for (int32_t h = 0; h < H; ++h) {
-                int l = (h >> 3) & 31;
+                int l = h & 31;
                 part[l] = fmaf(xf[h], w[h], part[l]);
             }
             for (int off = 16; off >= 1; off >>= 1) {

@@ -79,3 +79,15 @@ def test_nonfinite_activation_is_refused():
         x[3, 17] = 0.0
         plan.route(x, synth.router_weight(w, 0, "cuda"))
         assert plan.sync_status() == moe.OK
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    w = synth.WORKLOADS["tiny_w4a16"]
+    with plan_for(w) as plan:
+        plan.check_timeout(20_000_000)             # 20 ms bound on a barrier nobody arrives on
+        assert plan.sync_status() == moe.ERR_TIMEOUT
+        assert plan.sync_status() == moe.OK         # the error word was cleared
+        x = synth.activations(w, 0, device="cuda")  # the context still runs work
+        r = plan.route(x, synth.router_weight(w, 0, "cuda"))
+        assert plan.sync_status() == moe.OK
+        assert int(r["expert_offsets"][-1]) == w.tokens * w.top_k

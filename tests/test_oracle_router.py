@@ -13,25 +13,25 @@ def _bf16(a):
 
 
 def test_logit_order_hand_worked():
-    # H = 256: position h belongs to lane (h // 8) % 32.  One large term in lane 0
-    # and two ones; the butterfly (offsets 16, 8, 4, 2, 1) decides the rounding.
+    # Position h belongs to lane h mod 32; each lane sums in increasing h; the
+    # butterfly adds lane l ^ 16, ^ 8, ^ 4, ^ 2, ^ 1.  One 2^24 term at h = 0
+    # (lane 0) and two ones: where they sit decides the fp32 rounding.
     H = 256
-    x = np.zeros((2, H))
     w = np.zeros((1, H), np.float32)
     w[0, 0] = 2.0 ** 24
-    w[0, 8] = w[0, 16] = w[0, 24] = 1.0
-    x[0, [0, 8, 16]] = 1.0   # ones in lanes 1 and 2: lane0+=lane2 then +=lane1, each 2^24+1 -> 2^24
-    x[1, [0, 8, 24]] = 1.0   # ones in lanes 1 and 3: lane1+=lane3 gives 2, then 2^24+2 exactly
+    w[0, [1, 2, 3, 32]] = 1.0
+    x = np.zeros((4, H))
+    x[0, [0, 1, 3]] = 1.0    # lanes 1 and 3: (l1 + l3) = 2 at offset 2, then 2^24 + 2 exactly
+    x[1, [0, 1, 2]] = 1.0    # lanes 1 and 2: 2^24 + l2 -> 2^24 at offset 2, + l1 -> 2^24 at offset 1
+    x[2, [0, 32, 1]] = 1.0   # h = 32 is lane 0 again: (2^24 + 1) -> 2^24 inside the lane, then + l1
+    x[3, [0, 3]] = 1.0       # a single one: 2^24 + 1 -> 2^24 (ties to even)
     lg = oracle.router_logits(_bf16(x), w, None)
-    assert lg[0, 0] == 2.0 ** 24
-    assert lg[1, 0] == 2.0 ** 24 + 2
-    # within a lane the sum runs in increasing h with one rounding per step
-    x2 = np.zeros((1, H)); w2 = np.zeros((1, H), np.float32)
-    x2[0, [0, 1, 2]] = 1.0
-    w2[0, 0] = 2.0 ** 24; w2[0, 1] = 1.0; w2[0, 2] = 1.0   # (2^24 + 1) + 1 -> 2^24
-    assert oracle.router_logits(_bf16(x2), w2, None)[0, 0] == 2.0 ** 24
+    assert lg[0, 0] == 2.0 ** 24 + 2
+    assert lg[1, 0] == 2.0 ** 24
+    assert lg[2, 0] == 2.0 ** 24
+    assert lg[3, 0] == 2.0 ** 24
     b = np.array([0.5], np.float32)
-    assert oracle.router_logits(_bf16(x2), w2, b)[0, 0] == 2.0 ** 24  # bias added last in fp32
+    assert oracle.router_logits(_bf16(x[:1]), w, b)[0, 0] == 2.0 ** 24 + 2  # bias added last in fp32
 
 
 def test_logits_within_fp32_error_bound_of_exact_dot():
