@@ -221,6 +221,30 @@ moe_status moe_plan_read_profile(moe_plan plan, float *ms, int64_t *launches, in
  * usable.  Faults nothing and hangs nothing. */
 moe_status moe_plan_check_timeout(moe_plan plan, int64_t wait_ns, void *stream);
 
+/* Routing and grouping, as moe_route, for callers that cannot allocate device
+ * memory: code running inside another allocator's arena or under a
+ * memory-capped runtime, or a host that forbids device allocations after
+ * start-up.  The pages have no counterpart of this entry point; it exists for
+ * those callers only.
+ *
+ * It needs no plan and calls no cudaMalloc, cudaFree or other allocating
+ * routine.  Its scratch (logits, counts, offsets, placement) is one
+ * file-scope device array of about 5.6 MB, held on every GPU that loads the
+ * library until the process exits.  Limits: T * num_experts <= 2^20,
+ * T * top_k <= 2^16, num_experts <= 1024, hidden a multiple of 256 up to
+ * 8192; beyond them it returns MOE_ERR_UNSUPPORTED_SHAPE and launches nothing.
+ * The first call on a device looks up the array's device address and sets the
+ * grouping kernel's shared-memory size; make that first call before any stream
+ * capture.  Every call shares the one array: calls that overlap on the GPU
+ * (other streams, other threads) race and must be serialised by the caller.
+ * The counts are cleared at the start of each call.  Outputs and argument
+ * layout are moe_route's; router: moe_router_kind; renormalize: 0 or 1.
+ * Device-side findings (a non-finite activation) are not reported here. */
+moe_status moe_route_static(const void *x_bf16, int32_t T, int32_t hidden, const float *router_w,
+                            const float *router_bias, int32_t num_experts, int32_t top_k, int32_t router,
+                            int32_t renormalize, int32_t *topk_ids, float *topk_w, int32_t *expert_offsets,
+                            int32_t *sorted_rows, void *stream);
+
 /* Text of a status code (static storage). */
 const char *moe_status_string(moe_status s);
 

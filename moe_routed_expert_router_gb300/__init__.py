@@ -28,7 +28,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_NONFINITE, ERR_T
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_route", "moe_forward", "moe_forward_host",
            "moe_quantize_act", "moe_quantize_nvfp4", "moe_plan_sync_status", "moe_plan_debug_buffer",
            "moe_plan_set_profiling", "moe_plan_read_profile", "moe_plan_set_path", "moe_plan_check_timeout",
-           "moe_status_string", "moe_version"]
+           "moe_route_static", "moe_status_string", "moe_version"]
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
 STAGES = ["route", "group", "quant_x", "permute", "gate_up", "quant_h", "down", "finalize"]
 
@@ -76,6 +76,7 @@ def lib():
         L.moe_plan_set_profiling.argtypes = [P, I32]
         L.moe_plan_set_path.argtypes = [P, I32]
         L.moe_plan_check_timeout.argtypes = [P, ctypes.c_int64, P]
+        L.moe_route_static.argtypes = [P, I32, I32, P, P, I32, I32, I32, I32, P, P, P, P, P]
         L.moe_plan_read_profile.argtypes = [P, P, P, P]
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
