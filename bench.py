@@ -396,12 +396,17 @@ def main():
     ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma-separated workload fields for a scaled-down profiling run, e.g. tokens=1024,experts=64")
     ap.add_argument("--instances", type=int, default=0,
                     help="use only the first N seeded instances / batches (0 = all; for small profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     w = synth.WORKLOADS[args.workload]
+    if args.override:
+        kv = dict(item.split("=") for item in args.override.split(","))
+        w = synth.scaled(w, **{k: int(v) for k, v in kv.items()})
     if args.impl == "reference":
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         if rank == 0:

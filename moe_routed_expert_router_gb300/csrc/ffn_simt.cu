@@ -17,14 +17,12 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kFeatGroup = 128;  // features (gate/up) or output rows (down) per work item
 
-// Row-major [kChunkRows][K] fp32 tile in shared memory with 16-byte chunks
-// xor-swizzled inside each group of 8, so a warp reading one 32-value unit per
-// lane (unit u = lane + 32m) hits distinct banks.
-__device__ __forceinline__ int swz(int k) {
-    int q = k >> 2;
-    q = (q & ~7) | ((q ^ (q >> 3)) & 7);
-    return (q << 2) | (k & 3);
-}
+// Activation tile in shared memory: kChunkRows rows of K fp32 values, each row
+// stored chunk-major -- the 4-value chunk j (0..7) of 32-value unit u sits at
+// float offset (j * (K / 32) + u) * 4 -- so a warp reading one unit per lane
+// (u = lane + 32m) touches consecutive 16-byte words, with no per-load index
+// arithmetic beyond a constant stride.
+__device__ __forceinline__ int tile_pos(int k, int K) { return (((k & 31) >> 2) * (K >> 5) + (k >> 5)) * 4 + (k & 3); }
 
 struct FfnArgs {
     const int4 *chunks;
@@ -66,6 +64,8 @@ __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const floa
                                          float (&acc)[kChunkRows]) {
     const float2 scf = f16x2_to_f32x2(e4m3x2_to_f16x2(sp));
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+    const int cs = K >> 3;   // floats between chunk j and chunk j+1 of a unit (K/32 units x 4)
+    const float *xu = xs + u * 4;
 #pragma unroll
     for (int blk = 0; blk < 2; ++blk) {
         float2 w[8];
@@ -77,14 +77,13 @@ __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const floa
             for (int j = 0; j < 4; ++j) w[q * 4 + j] = f16x2_to_f32x2(h[j]);
         }
         const float sc = blk ? scf.y : scf.x;
-        const int kbase = u * 32 + blk * 16;
 #pragma unroll
         for (int r = 0; r < NR; ++r) {
-            const float *row = xs + r * K;
+            const float *row = xu + r * K + blk * 4 * cs;
             float2 p = make_float2(0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 xv = *reinterpret_cast<const float4 *>(row + swz(kbase + 4 * j));
+                const float4 xv = *reinterpret_cast<const float4 *>(row + j * cs);
                 p = ffma2(w[2 * j], make_float2(xv.x, xv.y), p);
                 p = ffma2(w[2 * j + 1], make_float2(xv.z, xv.w), p);
             }
@@ -127,7 +126,8 @@ __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
         float *row = xs + r * H;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<float4 *>(row + swz(b * 16 + 4 * j)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            *reinterpret_cast<float4 *>(row + tile_pos(b * 16 + 4 * j, H)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
 }
 
@@ -229,7 +229,7 @@ __device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *
 // then nw warps x `slots` slots of (2 code rows + 2 scale rows), then the
 // slot barriers.
 template <int MODE>
-__global__ void __launch_bounds__(256) k_gateup_stream(FfnArgs a, int slots) {
+__global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int H = a.H;
@@ -322,7 +322,8 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
         float *rowp = hs + r * I;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-            *reinterpret_cast<float4 *>(rowp + swz(b * 16 + 4 * j)) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            *reinterpret_cast<float4 *>(rowp + tile_pos(b * 16 + 4 * j, I)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     }
 }
 
@@ -449,10 +450,12 @@ __global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
 
 constexpr size_t kSmemBudget = 227 * 1024;
 
-// Largest (warps, slots) whose shared memory fits, preferring 8 warps.
-bool pick_config(size_t fixed, size_t slot_bytes, int &nw, int &slots) {
-    for (int w : {8, 4, 2}) {
-        for (int s : {3, 2, 1}) {
+// Largest (warps, slots) whose shared memory fits, preferring more warps
+// (up to max_warps) and then deeper rings.
+bool pick_config(size_t fixed, size_t slot_bytes, int max_warps, int &nw, int &slots) {
+    for (int w : {16, 8, 4, 2}) {
+        if (w > max_warps) continue;
+        for (int s : {3, 2}) {
             const size_t need = fixed + (size_t)w * s * slot_bytes + (size_t)w * s * 8 + 128;
             if (need <= kSmemBudget) {
                 nw = w;
@@ -464,12 +467,26 @@ bool pick_config(size_t fixed, size_t slot_bytes, int &nw, int &slots) {
     return false;
 }
 
+// Fallback for wide rows: 8, 4 or 2 warps with a single slot each.
+bool pick_config1(size_t fixed, size_t slot_bytes, int &nw, int &slots) {
+    for (int w : {8, 4, 2}) {
+        const size_t need = fixed + (size_t)w * slot_bytes + (size_t)w * 8 + 128;
+        if (need <= kSmemBudget) {
+            nw = w;
+            slots = 1;
+            return true;
+        }
+    }
+    return false;
+}
+
 template <int MODE>
 cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st) {
     int nw = 0, slots = 0;
     if (part == 0) {
         const size_t fixed = (size_t)kChunkRows * a.H * 4, slot = (size_t)a.H + a.H / 8;
-        if (!pick_config(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
+        if (!pick_config(fixed, slot, 16, nw, slots) && !pick_config1(fixed, slot, nw, slots))
+            return cudaErrorInvalidValue;
         const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
         cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
@@ -478,7 +495,7 @@ cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st)
     }
     const int Imax = max(a.I, a.Is);
     const size_t fixed = (size_t)kChunkRows * Imax * 4, slot = (size_t)kDownRows * (Imax / 2 + Imax / 16);
-    if (!pick_config(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
+    if (!pick_config(fixed, slot, 8, nw, slots) && !pick_config1(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
     const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
     cudaError_t e = cudaFuncSetAttribute(k_down_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

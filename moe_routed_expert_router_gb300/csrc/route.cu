@@ -146,8 +146,8 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
     float amax = 0.0f;
     auto fetch = [&](int s) {
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {  // 16 tokens x 32 chunks of 8 bf16
-            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+        for (int i = 0; i < 2; ++i) {  // 16 tokens x 32 chunks of 8 bf16; lanes walk the tokens
+            const int idx = tid + 256 * i, row = idx & 15, c = idx >> 4;
             xr[i] = make_uint4(0, 0, 0, 0);
             if (t0 + row < T) xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + row) * H + s * kRSlab + c * 8));
             if (check) {
@@ -160,8 +160,8 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
             }
         }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {  // 32 experts x 64 chunks of 4 floats
-            const int idx = tid + 256 * i, row = idx >> 6, c = idx & 63;
+        for (int i = 0; i < 8; ++i) {  // 32 experts x 64 chunks of 4 floats; lanes walk the experts
+            const int idx = tid + 256 * i, row = idx & 31, c = idx >> 5;
             wr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (e0 + row < E) wr[i] = __ldg(reinterpret_cast<const float4 *>(rw + (size_t)(e0 + row) * H + s * kRSlab + c * 4));
         }
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
         float *wb = wT + b * kRSlab * kWPitch;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-            const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+            const int idx = tid + 256 * i, row = idx & 15, c = idx >> 4;
             const uint32_t u[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const int idx = tid + 256 * i, row = idx >> 6, c = idx & 63;
+            const int idx = tid + 256 * i, row = idx & 31, c = idx >> 5;
             wb[(c * 4 + 0) * kWPitch + row] = wr[i].x;
             wb[(c * 4 + 1) * kWPitch + row] = wr[i].y;
             wb[(c * 4 + 2) * kWPitch + row] = wr[i].z;
