@@ -259,6 +259,8 @@ def run_ours(args, w, world, rank, local):
                     router=moe.ROUTER_SIGMOID if w.router == "sigmoid" else moe.ROUTER_SOFTMAX,
                     renormalize=w.renormalize, mode=moe.W4A4 if w.mode == "w4a4" else moe.W4A16,
                     has_shared=w.shared_inter > 0, shared_inter=w.shared_inter)
+    plan.set_path({"auto": moe.PATH_AUTO, "cuda_core": moe.PATH_CUDA_CORE,
+                   "tensor_core": moe.PATH_TENSOR_CORE}[args.path])
     ids_list = [plan.route(i.x, i.rw, i.bias)["topk_ids"].cpu().numpy() for i in insts]
     gu_bytes, dn_bytes, flops, distinct = algorithmic(w, ids_list)
     outs = [torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda") for _ in insts]
@@ -341,7 +343,8 @@ def run_ours(args, w, world, rank, local):
                    "experts": w.experts, "inter": w.inter, "top_k": w.top_k, "shared_inter": w.shared_inter,
                    "mode": w.mode, "router": w.router, "instances": len(insts),
                    "l2": "inputs larger than L2: step i runs instance i mod %d with its own weights" % len(insts),
-                   "parallelism": f"replicas x{world}", "distinct_experts_per_step": distinct},
+                   "parallelism": f"replicas x{world}", "distinct_experts_per_step": distinct,
+                   "path": args.path},
         "e2e": {"value": round(tokens / (ms_e2e / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": w.tokens * w.hidden * 2, "d2h_bytes_per_step": w.tokens * w.hidden * 2},
         "gpu_launches": launches,
@@ -396,6 +399,8 @@ def main():
     ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
+                    help="expert-FFN implementation (moe_plan_set_path)")
     ap.add_argument("--override", default="",
                     help="comma-separated workload fields for a scaled-down profiling run, e.g. tokens=1024,experts=64")
     ap.add_argument("--instances", type=int, default=0,

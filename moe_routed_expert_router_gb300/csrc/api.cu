@@ -104,9 +104,13 @@ void carve(Plan &p, Carver &c) {
     p.pad_pair = c.take<int32_t>(sizeof(int32_t) * p.rows_pad_max);
     p.chunks = c.take<int4>(sizeof(int4) * p.chunks_max);
     p.tiles = c.take<int4>(sizeof(int4) * p.tiles_max);
-    p.xp = c.take<uint8_t>(p.rows_pad_max * H / 2);
-    p.xp_atoms = c.take<uint8_t>(p.rows_pad_max * H / 16);
-    p.hq_atoms = c.take<uint8_t>(p.rows_pad_max * Imax / 16);
+    if (k.mode == MOE_W4A4) {
+        p.xp = c.take<uint8_t>(p.rows_pad_max * H / 2);
+        p.xp_atoms = c.take<uint8_t>(p.rows_pad_max * H / 16);
+        p.hq_atoms = c.take<uint8_t>(p.rows_pad_max * Imax / 16);
+    } else {
+        p.xp16 = c.take<__half>(p.rows_pad_max * H * 2);
+    }
     p.xts = c.take<float>(64);
     p.xq = c.take<uint8_t>(T * H / 2);
     p.xsc = c.take<uint8_t>(T * H / 16);

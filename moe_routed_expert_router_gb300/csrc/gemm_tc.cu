@@ -117,16 +117,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 lanes x 16 columns of fp32 into v[0..15] (each thread: its lane); the
+// caller waits with tcgen05.wait::ld before reading v.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float *v) {
+    uint32_t *r = reinterpret_cast<uint32_t *>(v);
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 struct Item {
@@ -307,6 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
         }
     } else {
         // ------------------------------------------------ epilogue (8 warps)
+        // Each warp copies its 32 lanes x 64 columns of both accumulators into
+        // registers, releases the accumulators to the MMA warp, and only then
+        // does the arithmetic and the global writes, so the next item's MMAs
+        // overlap them.
         const int quad = warp & 3;                 // TMEM lanes this warp may read
         const int col0 = ((warp - 3) >> 2) * 64;   // its half of the token columns
         uint32_t aph = 0;
@@ -321,23 +324,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             const int m = it.sh ? 1 : 0;
             const int e = it.sh ? 0 : it.e;
             const int n_end = min(col0 + 64, it.valid);
+            float v0[64], v1[64];
+            if (col0 < n_end) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    tmem_ld16_nowait(lane_base + col0 + 16 * c, v0 + 16 * c);
+                    tmem_ld16_nowait(lane_base + 128 + col0 + 16 * c, v1 + 16 * c);
+                }
+                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            if (col0 >= n_end) continue;
             if (EPI == kSwiGLU) {
                 const float xts = __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
                 const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
                 const int feat = it.f * 128 + quad * 32 + lane;
                 float mx = 0.0f;
-                for (int n0 = col0; n0 < n_end; n0 += 16) {
-                    float g[16], u[16];
-                    tmem_ld16(lane_base + n0, g);
-                    tmem_ld16(lane_base + 128 + n0, u);
+                float *hrow = a.hbuf + (size_t)(it.row0 + col0) * a.hstride + feat;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        if (n0 + j < n_end) {
-                            const float gv = g[j] * sg, uv = u[j] * su;
-                            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
-                            a.hbuf[(size_t)(it.row0 + n0 + j) * a.hstride + feat] = h;
-                            mx = fmaxf(mx, fabsf(h));
-                        }
+                for (int j = 0; j < 64; ++j) {
+                    if (col0 + j < n_end) {
+                        const float gv = v0[j] * sg, uv = v1[j] * su;
+                        const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                        hrow[(size_t)j * a.hstride] = h;
+                        mx = fmaxf(mx, fabsf(h));
                     }
                 }
                 if (it.sh) lmax_s = fmaxf(lmax_s, mx);
@@ -359,26 +371,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     }
                 }
                 const int j0 = it.f * 256 + quad * 32 + lane;
-                for (int n0 = col0; n0 < n_end; n0 += 16) {
-                    float y0[16], y1[16];
-                    tmem_ld16(lane_base + n0, y0);
-                    tmem_ld16(lane_base + 128 + n0, y1);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int n = n0 + j, c = n - col0;
-                        const int t = __shfl_sync(0xffffffffu, tok[c >> 5], c & 31);
-                        const float wv = __shfl_sync(0xffffffffu, wgt[c >> 5], c & 31) * ds;
-                        if (n < n_end) {
-                            float *dst = a.acc + (size_t)t * a.H + j0;
-                            atomicAdd(dst, y0[j] * wv);
-                            atomicAdd(dst + 128, y1[j] * wv);
-                        }
+                for (int j = 0; j < 64; ++j) {
+                    const int t = __shfl_sync(0xffffffffu, tok[j >> 5], j & 31);
+                    const float wv = __shfl_sync(0xffffffffu, wgt[j >> 5], j & 31) * ds;
+                    if (col0 + j < n_end) {
+                        float *dst = a.acc + (size_t)t * a.H + j0;
+                        atomicAdd(dst, v0[j] * wv);
+                        atomicAdd(dst + 128, v1[j] * wv);
                     }
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
         }
         if (EPI == kSwiGLU) {
             lmax = warp_max(lmax);
@@ -394,6 +397,364 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    }
+}
+
+// ------------------------------------------------------------------ W4A16
+// W4A16 on the tensor cores (tcgen05 kind::f16, fp32 accumulators).  The
+// weights arrive as NVFP4 codes (TMA, 32 code bytes = 64 K values a row a
+// stage) and are widened in shared memory by four converter warps:
+// E2M1 -> f16 with cvt.rn.f16x2.e2m1x2, times the E4M3 block scale in f16.
+// code x scale has at most 6 significant bits, so the f16 weights are exact.
+// The activations are given as f16 rows: the permute kernel writes x * 2^-s,
+// with s the smallest power of two that keeps the batch amax inside f16
+// (s = 0 for ordinary activations), and the epilogue multiplies 2^s back.
+// There is no scale factor in tensor memory, so the two accumulator pairs
+// (gate, up: 2 x 128 columns) are double-buffered and the epilogue of one
+// item overlaps the MMAs of the next.
+constexpr int kHBK = 64;                         // K values per stage
+constexpr int kHCode = 128 * 32;                 // 4 KB: 128 rows x 32 code bytes
+constexpr int kHTile = 128 * 128;                // 16 KB: 128 rows x 64 f16, 128-byte swizzle
+constexpr int kHStages = 3;
+constexpr int kHStageBytes = 2 * kHCode + 3 * kHTile;   // A0, A1 codes; A0, A1 f16; B f16
+constexpr int kHScSlot = 2 * 2048;               // two [128 rows][16 B] scale tiles (K 256)
+constexpr int kConvWarps = 4;
+constexpr int kHThreads = 32 * (2 + kConvWarps + kEpiWarps);
+constexpr size_t kHSmemBytes = kHStages * kHStageBytes + 2 * kHScSlot + 512 + 1024;
+
+struct HcArgs {
+    CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 32 B x 128 rows (gate/up or down)
+    CUtensorMap s0[2], s1[2];   // scales [rows][K/16], box 16 B x 128 rows
+    CUtensorMap b[3];           // f16 token rows [rows_pad][Kdim], box 64 x (32/64/128), 128-byte swizzle
+    const int4 *tiles;
+    const CallScratch *scratch;
+    int E, H, I, Is, nf;
+    const float *ts_a0[2], *ts_a1[2];
+    __half *hout;               // gate/up output (f16) [rows][hstride]
+    int hstride;
+    const int32_t *pad_pair;
+    const float *wts;
+    int P, k;
+    float *acc;
+    int *err;
+};
+
+// f16 scale exponent s of the activations: x * 2^-s keeps amax below 2^15.
+__device__ __forceinline__ int f16_shift(unsigned int amax_bits) {
+    const int e = (int)((amax_bits >> 23) & 0xFF) - 127;   // floor(log2(amax)) for normal amax
+    return e > 14 ? e - 14 : 0;
+}
+
+__device__ __forceinline__ uint32_t idesc_f16(uint32_t n) {
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi, Item &it) {
+    const int4 t = a.tiles[item / a.nf];
+    it.f = item % a.nf;
+    it.e = t.x;
+    it.row0 = t.y;
+    it.valid = t.z;
+    it.sh = (t.x == a.E);
+    const int I = it.sh ? a.Is : a.I;
+    if (epi == kSwiGLU) {
+        it.K = a.H;
+        return it.f * 128 < I;
+    }
+    it.K = I;
+    return true;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant__ HcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *scs = smem + kHStages * kHStageBytes;                       // scale ring, 2 slots
+    uint64_t *full = reinterpret_cast<uint64_t *>(scs + 2 * kHScSlot);
+    uint64_t *conv = full + kHStages;
+    uint64_t *empty = conv + kHStages;
+    uint64_t *acc_full = empty + kHStages;      // [2]
+    uint64_t *acc_empty = acc_full + 2;         // [2]
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = a.scratch->n_tiles * a.nf;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kHStages; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(conv + s, kConvWarps);
+            mbar_init(empty + s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(acc_full + b, 1);
+            mbar_init(acc_empty + b, kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            int kbg = 0;   // 256-value scale blocks issued so far (scale ring slot = kbg & 1)
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int m = it.sh ? 1 : 0;
+                int r0, r1;
+                if (EPI == kSwiGLU) {
+                    r0 = r1 = (it.sh ? 0 : it.e * a.I) + it.f * 128;
+                } else {
+                    r0 = (it.sh ? 0 : it.e * a.H) + it.f * 256;
+                    r1 = r0 + 128;
+                }
+                const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
+                const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
+                const int rc = rows_class(it.valid);
+                const uint32_t b_bytes = (32u << rc) * 128u;
+                const int ks_n = it.K / kHBK;
+                for (int ks = 0; ks < ks_n; ++ks) {
+                    if (!mbar_wait(empty + s, ph ^ 1, a.err)) { ok = false; break; }
+                    uint8_t *st = smem + s * kHStageBytes;
+                    const bool sc = (ks & 3) == 0;
+                    mbar_expect_tx(full + s, 2 * kHCode + b_bytes + (sc ? kHScSlot : 0));
+                    tma_2d(st, &a.a0[m], full + s, ks * 32, r0);
+                    tma_2d(st + kHCode, A1, full + s, ks * 32, r1);
+                    tma_2d(st + 2 * kHCode + 2 * kHTile, &a.b[rc], full + s, ks * kHBK, it.row0);
+                    if (sc) {
+                        uint8_t *slot = scs + (kbg++ & 1) * kHScSlot;
+                        tma_2d(slot, &a.s0[m], full + s, (ks >> 2) * 16, r0);
+                        tma_2d(slot + 2048, S1, full + s, (ks >> 2) * 16, r1);
+                    }
+                    used |= 1u << s;
+                    last_ph = (last_ph & ~(1u << s)) | (ph << s);
+                    if (++s == kHStages) { s = 0; ph ^= 1; }
+                }
+            }
+            for (int t = 0; t < kHStages; ++t)
+                if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
+        }
+    } else if (warp >= 2 && warp < 2 + kConvWarps) {
+        // ------------------------------------------------ NVFP4 -> f16 converters
+        // thread c widens row c of both A operands: 64 values, 4 scale blocks,
+        // written as 8 16-byte chunks in the 128-byte-swizzle K-major layout.
+        const int c = threadIdx.x - 64;
+        int s = 0, kbg = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        const uint8_t *slot = scs;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item_h(a, item, EPI, it)) continue;
+            const int ks_n = it.K / kHBK;
+            for (int ks = 0; ks < ks_n; ++ks) {
+                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                uint8_t *st = smem + s * kHStageBytes;
+                if ((ks & 3) == 0) slot = scs + (kbg++ & 1) * kHScSlot;
+                const uint32_t rbase = (uint32_t)((c >> 3) * 1024 + (c & 7) * 128);
+#pragma unroll
+                for (int op = 0; op < 2; ++op) {
+                    const uint4 *cp = reinterpret_cast<const uint4 *>(st + op * kHCode + c * 32);
+                    const uint4 q0 = cp[0], q1 = cp[1];
+                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(slot + op * 2048 + c * 16 + (ks & 3) * 4);
+                    const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                    uint8_t *dst = st + 2 * kHCode + op * kHTile + rbase;
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk) {
+                        const uint32_t sc2 = e4m3x2_to_f16x2(((sw >> (8 * blk)) & 0xFFu) * 0x101u);
+                        uint32_t h[8];
+                        e2m1x8_to_f16x8(cw[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
+                        e2m1x8_to_f16x8(cw[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
+                        uint32_t o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[j]),
+                                                *reinterpret_cast<const __half2 *>(&sc2));
+                            o[j] = *reinterpret_cast<uint32_t *>(&v);
+                        }
+                        const int ch0 = 2 * blk, ch1 = 2 * blk + 1;
+                        *reinterpret_cast<uint4 *>(dst + ((ch0 ^ (c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4 *>(dst + ((ch1 ^ (c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(conv + s);
+                if (++s == kHStages) { s = 0; ph ^= 1; }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue (one lane)
+        if (lane == 0) {
+            int s = 0, buf = 0;
+            uint32_t ph = 0, aph[2] = {0, 0};
+            bool ok = true;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!mbar_wait(acc_empty + buf, aph[buf] ^ 1, a.err)) break;
+                aph[buf] ^= 1;
+                tc_fence_after();
+                const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
+                const uint32_t idesc = idesc_f16(32u << rows_class(it.valid));
+                const int ks_n = it.K / kHBK;
+                for (int ks = 0; ks < ks_n; ++ks) {
+                    if (!mbar_wait(conv + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t base = smem_u32(smem + s * kHStageBytes);
+                    const uint32_t a0 = base + 2 * kHCode, a1 = a0 + kHTile, bt = a1 + kHTile;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t accum = (ks | kk) ? 1u : 0u;
+                        const uint64_t bd = desc_sw128(bt + 32 * kk);
+                        mma_f16(d0, desc_sw128(a0 + 32 * kk), bd, idesc, accum);
+                        mma_f16(d1, desc_sw128(a1 + 32 * kk), bd, idesc, accum);
+                    }
+                    mma_commit(empty + s);
+                    if (++s == kHStages) { s = 0; ph ^= 1; }
+                }
+                if (!ok) break;
+                mma_commit(acc_full + buf);
+                buf ^= 1;
+            }
+            mma_commit(drain);
+            mbar_wait(drain, 0, a.err);
+        }
+    } else {
+        // ------------------------------------------------ epilogue (8 warps)
+        const int ew = warp - (2 + kConvWarps);
+        const int quad = warp & 3;
+        const int col0 = (ew >> 2) * 64;
+        int buf = 0;
+        uint32_t aph[2] = {0, 0};
+        const int xs = f16_shift(a.scratch->x_amax);
+        const float xunscale = __uint_as_float((uint32_t)(127 + xs) << 23);   // 2^s
+        bool range_bad = false;
+        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item_h(a, item, EPI, it)) continue;
+            if (!mbar_wait(acc_full + buf, aph[buf], a.err)) break;
+            aph[buf] ^= 1;
+            tc_fence_after();
+            const uint32_t lane_base = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+            const int m = it.sh ? 1 : 0;
+            const int e = it.sh ? 0 : it.e;
+            const int n_end = min(col0 + 64, it.valid);
+            if (EPI == kSwiGLU) {
+                const float sg = a.ts_a0[m][e] * xunscale, su = a.ts_a1[m][e] * xunscale;
+                const int feat = it.f * 128 + quad * 32 + lane;
+                for (int n0 = col0; n0 < n_end; n0 += 16) {
+                    float g[16], u[16];
+                    tmem_ld16_nowait(lane_base + n0, g);
+                    tmem_ld16_nowait(lane_base + 128 + n0, u);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (n0 + j < n_end) {
+                            const float gv = g[j] * sg, uv = u[j] * su;
+                            // SwiGLU output rounded to bf16 (W4A16), then held as f16 for the down MMA
+                            const float hb = __bfloat162float(__float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv));
+                            range_bad |= fabsf(hb) > 65504.0f;
+                            a.hout[(size_t)(it.row0 + n0 + j) * a.hstride + feat] = __float2half_rn(hb);
+                        }
+                    }
+                }
+            } else {
+                const float ds = a.ts_a0[m][e];
+                int tok[2];
+                float wgt[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = col0 + lane + 32 * q;
+                    tok[q] = 0;
+                    wgt[q] = 0.0f;
+                    if (n < it.valid) {
+                        const int pair = a.pad_pair[it.row0 + n];
+                        tok[q] = pair >= a.P ? pair - a.P : pair / a.k;
+                        wgt[q] = pair >= a.P ? 1.0f : a.wts[pair];
+                    }
+                }
+                const int j0 = it.f * 256 + quad * 32 + lane;
+                for (int n0 = col0; n0 < n_end; n0 += 16) {
+                    float y0[16], y1[16];
+                    tmem_ld16_nowait(lane_base + n0, y0);
+                    tmem_ld16_nowait(lane_base + 128 + n0, y1);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int cc = n0 + j - col0;
+                        const int t = __shfl_sync(0xffffffffu, tok[cc >> 5], cc & 31);
+                        const float wv = __shfl_sync(0xffffffffu, wgt[cc >> 5], cc & 31) * ds;
+                        if (n0 + j < n_end) {
+                            float *dst = a.acc + (size_t)t * a.H + j0;
+                            atomicAdd(dst, y0[j] * wv);
+                            atomicAdd(dst + 128, y1[j] * wv);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty + buf);
+            buf ^= 1;
+        }
+        if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(a.err, kErrDevice);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+    }
+}
+
+// x rows (bf16) -> padded per-expert f16 rows, times 2^-s (exact; s from the
+// batch amax so the values fit f16).
+__global__ void __launch_bounds__(256) k_permute_f16(const uint16_t *__restrict__ x, const int32_t *__restrict__ pad_pair,
+                                                     const int32_t *__restrict__ poff, const CallScratch *__restrict__ sc,
+                                                     int E, int H, int P, int k, __half *__restrict__ xp) {
+    const int rows = poff[E + 1];
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    const float scale = __uint_as_float((uint32_t)(127 - f16_shift(sc->x_amax)) << 23);   // 2^-s
+    for (int r = warp; r < rows; r += nwarps) {
+        const int pair = pad_pair[r];
+        if (pair < 0) continue;
+        const int t = pair >= P ? pair - P : pair / k;
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+        uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * H);
+        for (int i = lane; i < H / 8; i += 32) {
+            const uint4 q = src[i];
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                __half2 h = __floats2half2_rn(__uint_as_float(u[j] << 16) * scale, __uint_as_float(u[j] & 0xFFFF0000u) * scale);
+                o[j] = *reinterpret_cast<uint32_t *>(&h);
+            }
+            dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
     }
 }
 
@@ -442,17 +803,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 2-D uint8 tensor map: `rows` rows of `row_bytes` bytes (row stride
-// `stride`), box = box_bytes x box_rows.
-bool make_map(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint64_t stride,
-              uint32_t box_bytes, uint32_t box_rows, bool swizzle) {
+// 2-D tensor map of 1-byte (or, with u16, 2-byte) elements: `rows` rows of
+// `row_elems` elements (row stride `stride` bytes), box = box_elems x box_rows.
+bool make_map(CUtensorMap *m, const void *base, uint64_t row_elems, uint64_t rows, uint64_t stride,
+              uint32_t box_elems, uint32_t box_rows, bool swizzle, bool u16 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t dims[2] = {row_elems, rows};
     cuuint64_t strides[1] = {stride};
-    cuuint32_t box[2] = {box_bytes, box_rows};
+    cuuint32_t box[2] = {box_elems, box_rows};
     cuuint32_t es[2] = {1, 1};
-    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+    CUresult r = fn(m, u16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                    const_cast<void *>(base), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -466,7 +828,6 @@ constexpr size_t kSmemBytes = kStages * kStageBytes + 512 + 1024;
 // shared I) multiples of 256, scale rows 16-byte aligned.
 bool tc_supported(const Plan &p) {
     const moe_config &c = p.cfg;
-    if (c.mode != MOE_W4A4) return false;
     if (c.hidden % 256 || c.inter % 256) return false;
     if (c.has_shared && c.shared_inter % 256) return false;
     return encode_fn() != nullptr;
@@ -474,12 +835,91 @@ bool tc_supported(const Plan &p) {
 
 cudaError_t configure_tc(const Plan &) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_gemm_fp4<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_fp4<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_f16<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_f16<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
+    return e;
 }
 
-cudaError_t launch_ffn_tc(const Plan &p, const void *, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
+namespace {
+
+// W4A16 on the tensor cores (see k_gemm_f16).
+cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
+                              cudaStream_t st) {
+    const moe_config &c = p.cfg;
+    const int H = c.hidden, I = c.inter, E = c.num_experts;
+    const int Is = c.has_shared ? c.shared_inter : 0;
+    const int Imax = std::max(I, Is);
+    const ExpertPtrs &sp = s ? *s : r;
+    const int Is_ = s ? Is : I;
+    HcArgs a{};
+    a.tiles = p.tiles;
+    a.scratch = p.scratch;
+    a.E = E;
+    a.H = H;
+    a.I = I;
+    a.Is = Is;
+    a.hout = reinterpret_cast<__half *>(p.hbuf);
+    a.hstride = Imax;
+    a.pad_pair = p.pad_pair;
+    a.wts = p.wts;
+    a.P = T * c.top_k;
+    a.k = c.top_k;
+    a.acc = p.acc;
+    a.err = p.err;
+    bool ok = true;
+    if (part == 0) {
+        k_permute_f16<<<p.num_sms * 4, 256, 0, st>>>(static_cast<const uint16_t *>(x), p.pad_pair, p.poff, p.scratch,
+                                                     E, H, a.P, c.top_k, p.xp16);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 32, 128, false);
+        ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 32, 128, false);
+        ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.s1[0], r.us, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 32, 128, false);
+        ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 32, 128, false);
+        ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
+        ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
+        for (int k2 = 0; k2 < 3; ++k2)
+            ok &= make_map(&a.b[k2], p.xp16, H, p.rows_pad_max, (uint64_t)H * 2, 64, 32u << k2, true, true);
+        a.nf = Imax / 128;
+        a.ts_a0[0] = r.gts;
+        a.ts_a1[0] = r.uts;
+        a.ts_a0[1] = sp.gts;
+        a.ts_a1[1] = sp.uts;
+        if (!ok) return cudaErrorInvalidValue;
+        k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+        return cudaGetLastError();
+    }
+    ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 32, 128, false);
+    ok &= make_map(&a.s0[0], r.ds, I / 16, (uint64_t)E * H, I / 16, 16, 128, false);
+    ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 32, 128, false);
+    ok &= make_map(&a.s0[1], sp.ds, Is_ / 16, H, Is_ / 16, 16, 128, false);
+    a.a1[0] = a.a0[0];
+    a.a1[1] = a.a0[1];
+    a.s1[0] = a.s0[0];
+    a.s1[1] = a.s0[1];
+    for (int k2 = 0; k2 < 3; ++k2)
+        ok &= make_map(&a.b[k2], p.hbuf, Imax, p.rows_pad_max, (uint64_t)Imax * 2, 64, 32u << k2, true, true);
+    a.nf = H / 256;
+    a.ts_a0[0] = r.dts;
+    a.ts_a0[1] = sp.dts;
+    a.ts_a1[0] = r.dts;
+    a.ts_a1[1] = sp.dts;
+    if (!ok) return cudaErrorInvalidValue;
+    k_gemm_f16<kScatter><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
                           cudaStream_t st) {
+    if (p.cfg.mode == MOE_W4A16) return launch_ffn_tc_f16(p, x, T, r, s, part, st);
     const moe_config &c = p.cfg;
     const int H = c.hidden, I = c.inter, E = c.num_experts;
     const int Is = c.has_shared ? c.shared_inter : 0;

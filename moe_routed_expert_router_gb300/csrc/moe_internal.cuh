@@ -62,6 +62,7 @@ struct Plan {
     uint8_t *xp = nullptr;          // [rows_pad][H/2] permuted x codes (tensor-core path)
     uint8_t *xp_atoms = nullptr;    // [rows_pad/128][H/64][512] their scales, tensor-core layout
     uint8_t *hq_atoms = nullptr;    // [rows_pad/128][Imax/64][512] SwiGLU scales, tensor-core layout
+    __half *xp16 = nullptr;         // [rows_pad][H] permuted x as f16 (W4A16 tensor-core path)
     CallScratch *scratch = nullptr;
     float *xts = nullptr;           // [2] x tensor scale, spare
     uint8_t *xq = nullptr;          // [Tmax][H/2]

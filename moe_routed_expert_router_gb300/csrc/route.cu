@@ -489,7 +489,7 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias, int32_t *ids,
                           float *wts, cudaStream_t st) {
     const int H = p.cfg.hidden, E = p.cfg.num_experts;
-    unsigned int *amax = (p.cfg.mode == MOE_W4A4) ? &p.scratch->x_amax : nullptr;
+    unsigned int *amax = &p.scratch->x_amax;   // batch amax of x (W4A4 quantiser, f16 range of W4A16)
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     if (T <= 16 && H % kSmallSlab == 0) {
         const int ntg = (T + 7) / 8, epb = 8 / ntg;

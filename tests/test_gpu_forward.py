@@ -56,6 +56,39 @@ def test_w4a4_paths_against_oracle(path):
     _parity(case, plan)
 
 
+@pytest.mark.parametrize("path", ["cuda_core", "tensor_core"])
+def test_w4a16_paths_against_oracle(path):
+    w = synth.scaled(synth.WORKLOADS["prompt512_w4a16"], tokens=200, hidden=1024, experts=16, inter=512,
+                     shared_inter=256)
+    case = Case(w, 3)
+    plan = plan_for(w)
+    plan.set_path(moe.PATH_CUDA_CORE if path == "cuda_core" else moe.PATH_TENSOR_CORE)
+    _parity(case, plan)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_decode_w4a16_full_on_tensor_cores(seed):
+    w = synth.WORKLOADS["decode4_w4a16"]
+    case = Case(w, seed)
+    plan = plan_for(w)
+    plan.set_path(moe.PATH_TENSOR_CORE)
+    _parity(case, plan)
+
+
+def test_w4a16_tensor_core_path_matches_cuda_core_path():
+    w = synth.scaled(synth.WORKLOADS["prompt512_w4a16"], tokens=77, hidden=2048, experts=24, inter=768)
+    case = Case(w, 4)
+    p1, p2 = plan_for(w), plan_for(w)
+    p1.set_path(moe.PATH_CUDA_CORE)
+    p2.set_path(moe.PATH_TENSOR_CORE)
+    a, st1, _ = case.gpu_forward(p1)
+    b, st2, _ = case.gpu_forward(p2)
+    assert st1 == moe.OK and st2 == moe.OK
+    d = (a.float() - b.float()).abs()
+    rms = a.float().pow(2).mean().sqrt()
+    assert (d.max() / rms).item() < 2e-2 and (d.norm() / a.float().norm()).item() < 5e-3
+
+
 def test_tensor_core_path_matches_cuda_core_path():
     w = synth.scaled(synth.WORKLOADS["verify16_w4a4"], hidden=2048, experts=32, inter=768, shared_inter=512)
     w = synth.scaled(w, inter=512)
