@@ -13,6 +13,7 @@ namespace moe {
 size_t group_smem_bytes(int E);
 cudaError_t configure_group_kernel(int E);
 cudaError_t configure_tc(const Plan &p);
+cudaError_t configure_simt();
 bool tc_supported(const Plan &p);
 cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs &routed, const ExpertPtrs *shared,
                           int part, cudaStream_t st);
@@ -253,6 +254,7 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
     carve(p, real);
     cudaError_t e = cudaMemset(p.ws, 0, p.ws_bytes);
     if (e == cudaSuccess) e = moe::configure_group_kernel(cfg->num_experts);
+    if (e == cudaSuccess) e = moe::configure_simt();
     if (e == cudaSuccess && moe::tc_supported(p)) e = moe::configure_tc(p);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {

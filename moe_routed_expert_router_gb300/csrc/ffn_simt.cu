@@ -488,8 +488,6 @@ cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st)
         if (!pick_config(fixed, slot, 16, nw, slots) && !pick_config1(fixed, slot, nw, slots))
             return cudaErrorInvalidValue;
         const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
-        cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
         k_gateup_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
         return cudaGetLastError();
     }
@@ -497,13 +495,22 @@ cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st)
     const size_t fixed = (size_t)kChunkRows * Imax * 4, slot = (size_t)kDownRows * (Imax / 2 + Imax / 16);
     if (!pick_config(fixed, slot, 8, nw, slots) && !pick_config1(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
     const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
-    cudaError_t e = cudaFuncSetAttribute(k_down_stream<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     k_down_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+// Shared-memory limits of the streamed kernels, set once (plan creation) so
+// that moe_forward makes no configuration call and can be graph-captured.
+cudaError_t configure_simt() {
+    const int lim = (int)kSmemBudget;
+    cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    return e;
+}
 
 cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtrs &routed, const ExpertPtrs *shared,
                             int part, cudaStream_t st) {

@@ -31,12 +31,12 @@
 namespace moe {
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kBK = 256;                  // K values per pipeline stage
 constexpr int kRowBytes = kBK / 2;        // 128 code bytes per row per stage
 constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
-constexpr int kStageBytes = 3 * kTile + 5 * kSf;
+constexpr int kStageBytes = 3 * kTile + 3 * kSf;   // A0, A1, B codes; A0, A1 scales (re-laid in place); B scales
 constexpr int kEpiWarps = 8;                      // two per 32-lane TMEM quadrant
 constexpr int kThreads = 32 * (3 + kEpiWarps);    // producer, MMA, scale re-layout, epilogue
 
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     tma_2d(st + 2 * kTile, &a.b[rc], full + s, ks * kRowBytes, it.row0);
                     tma_2d(st + 3 * kTile, &a.s0[m], full + s, ks * 16, r0);
                     tma_2d(st + 3 * kTile + kSf, S1, full + s, ks * 16, r1);
-                    bulk_copy(st + 3 * kTile + 4 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
+                    bulk_copy(st + 3 * kTile + 2 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
                     used |= 1u << s;
                     last_ph = (last_ph & ~(1u << s)) | (ph << s);
                     if (++s == kStages) { s = 0; ph ^= 1; }
@@ -242,11 +242,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 uint8_t *st = smem + s * kStageBytes;
 #pragma unroll
                 for (int op = 0; op < 2; ++op) {
-                    const uint4 *src = reinterpret_cast<const uint4 *>(st + 3 * kTile + op * kSf);
-                    uint4 *dst = reinterpret_cast<uint4 *>(st + 3 * kTile + 2 * kSf + op * kSf);
+                    // in place: every lane reads its 4 rows, then (after the warp
+                    // has read everything) writes its 4 atom words
+                    uint4 *tile = reinterpret_cast<uint4 *>(st + 3 * kTile + op * kSf);
                     uint4 v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = src[lane + 32 * q];
+                    for (int q = 0; q < 4; ++q) v[q] = tile[lane + 32 * q];
+                    __syncwarp();
+                    uint4 *dst = tile;
                     dst[0 * 32 + lane] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
                     dst[1 * 32 + lane] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
                     dst[2 * 32 + lane] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
@@ -278,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     if (!mbar_wait(sf_ready + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t base = smem_u32(smem + s * kStageBytes);
-                    const uint32_t at0 = base + 3 * kTile + 2 * kSf, at1 = at0 + kSf, atb = at0 + 2 * kSf;
+                    const uint32_t at0 = base + 3 * kTile, at1 = at0 + kSf, atb = at0 + 2 * kSf;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         sf_copy(tmem + 256 + 4 * kk, desc_sf(at0 + 512 * kk));
@@ -401,29 +404,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ W4A16
-// W4A16 on the tensor cores (tcgen05 kind::f16, fp32 accumulators).  The
-// weights arrive as NVFP4 codes (TMA, 32 code bytes = 64 K values a row a
-// stage) and are widened in shared memory by four converter warps:
-// E2M1 -> f16 with cvt.rn.f16x2.e2m1x2, times the E4M3 block scale in f16.
-// code x scale has at most 6 significant bits, so the f16 weights are exact.
-// The activations are given as f16 rows: the permute kernel writes x * 2^-s,
-// with s the smallest power of two that keeps the batch amax inside f16
-// (s = 0 for ordinary activations), and the epilogue multiplies 2^s back.
-// There is no scale factor in tensor memory, so the two accumulator pairs
-// (gate, up: 2 x 128 columns) are double-buffered and the epilogue of one
-// item overlaps the MMAs of the next.
-constexpr int kHBK = 64;                         // K values per stage
-constexpr int kHCode = 128 * 32;                 // 4 KB: 128 rows x 32 code bytes
-constexpr int kHTile = 128 * 128;                // 16 KB: 128 rows x 64 f16, 128-byte swizzle
-constexpr int kHStages = 3;
-constexpr int kHStageBytes = 2 * kHCode + 3 * kHTile;   // A0, A1 codes; A0, A1 f16; B f16
-constexpr int kHScSlot = 2 * 2048;               // two [128 rows][16 B] scale tiles (K 256)
+// W4A16 on the tensor cores (tcgen05 kind::f16, fp32 accumulators).  Three
+// shared-memory rings:
+//   code ring   (3 x 36 KB): NVFP4 weight codes (128-byte swizzle) + plain
+//                scale tiles of both A operands, 256 K values a stage;
+//   B ring      (3 x 16 KB): f16 token rows, 64 K values a stage;
+//   f16 A ring  (2 x 32 KB): the weights widened to f16 (128-byte swizzle,
+//                K-major), 64 K values a slot.
+// Four converter warps widen E2M1 -> f16 (cvt.rn.f16x2.e2m1x2) and multiply by
+// the E4M3 block scale in f16; code x scale has at most 6 significant bits, so
+// the f16 weights are exact.  A code stage is released as soon as it is
+// converted, so the weight stream runs ahead of the MMAs.  The activations are
+// f16 rows: the permute kernel writes x * 2^-s, with s the smallest power of
+// two keeping the batch amax inside f16 (s = 0 for ordinary activations); the
+// epilogue multiplies 2^s back.  No scale factors live in tensor memory, so the
+// accumulator pairs (gate, up: 2 x 128 columns) are double-buffered and an
+// item's epilogue overlaps the next item's MMAs.
+constexpr int kHCK = 256;                        // K values per code stage
+constexpr int kHCodeTile = 128 * 128;            // 16 KB: 128 rows x 128 code bytes
+constexpr int kHCodeStage = 2 * kHCodeTile + 2 * 2048;   // A0, A1 codes + A0, A1 scales
+constexpr int kHCStages = 3;
+constexpr int kHBK = 64;                         // K values per MMA step
+constexpr int kHBTile = 128 * 128;               // 16 KB: up to 128 rows x 64 f16
+constexpr int kHBStages = 3;
+constexpr int kHATile = 128 * 128;               // 16 KB: 128 rows x 64 f16
+constexpr int kHAStages = 2;
 constexpr int kConvWarps = 4;
 constexpr int kHThreads = 32 * (2 + kConvWarps + kEpiWarps);
-constexpr size_t kHSmemBytes = kHStages * kHStageBytes + 2 * kHScSlot + 512 + 1024;
+constexpr size_t kHRingBytes = kHCStages * kHCodeStage + kHBStages * kHBTile + kHAStages * 2 * kHATile;
+constexpr size_t kHSmemBytes = kHRingBytes + 512 + 1024;
+static_assert(kHSmemBytes <= 227 * 1024, "W4A16 pipeline exceeds shared memory");
 
 struct HcArgs {
-    CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 32 B x 128 rows (gate/up or down)
+    CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 128 B x 128 rows, 128-byte swizzle
     CUtensorMap s0[2], s1[2];   // scales [rows][K/16], box 16 B x 128 rows
     CUtensorMap b[3];           // f16 token rows [rows_pad][Kdim], box 64 x (32/64/128), 128-byte swizzle
     const int4 *tiles;
@@ -473,31 +486,49 @@ __device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi
     return true;
 }
 
+__device__ __forceinline__ void h_rows(const HcArgs &a, const Item &it, int epi, int &r0, int &r1) {
+    if (epi == kSwiGLU) {
+        r0 = r1 = (it.sh ? 0 : it.e * a.I) + it.f * 128;
+    } else {
+        r0 = (it.sh ? 0 : it.e * a.H) + it.f * 256;
+        r1 = r0 + 128;
+    }
+}
+
+// One ring position: index in the ring and the parity of its current use.
+struct RingPos {
+    int s = 0;
+    uint32_t ph = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) { s = 0; ph ^= 1; }
+    }
+};
+
 template <int EPI>
 __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant__ HcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *scs = smem + kHStages * kHStageBytes;                       // scale ring, 2 slots
-    uint64_t *full = reinterpret_cast<uint64_t *>(scs + 2 * kHScSlot);
-    uint64_t *conv = full + kHStages;
-    uint64_t *empty = conv + kHStages;
-    uint64_t *acc_full = empty + kHStages;      // [2]
-    uint64_t *acc_empty = acc_full + 2;         // [2]
+    uint8_t *code_ring = smem;
+    uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
+    uint8_t *a_ring = b_ring + kHBStages * kHBTile;
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(a_ring + kHAStages * 2 * kHATile);
+    uint64_t *cempty = cfull + kHCStages;
+    uint64_t *bfull = cempty + kHCStages;
+    uint64_t *bempty = bfull + kHBStages;
+    uint64_t *afull = bempty + kHBStages;
+    uint64_t *aempty = afull + kHAStages;
+    uint64_t *acc_full = aempty + kHAStages;     // [2]
+    uint64_t *acc_empty = acc_full + 2;          // [2]
     uint64_t *drain = acc_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = a.scratch->n_tiles * a.nf;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kHStages; ++s) {
-            mbar_init(full + s, 1);
-            mbar_init(conv + s, kConvWarps);
-            mbar_init(empty + s, 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(acc_full + b, 1);
-            mbar_init(acc_empty + b, kEpiWarps);
-        }
+        for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, kConvWarps); }
+        for (int i = 0; i < kHBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 1); }
+        for (int i = 0; i < kHAStages; ++i) { mbar_init(afull + i, kConvWarps); mbar_init(aempty + i, 1); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -511,104 +542,116 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
         if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
+            // ---------------------------------------- producer of the code ring
+            RingPos c;
             bool ok = true;
             uint32_t used = 0, last_ph = 0;
-            int kbg = 0;   // 256-value scale blocks issued so far (scale ring slot = kbg & 1)
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item_h(a, item, EPI, it)) continue;
                 const int m = it.sh ? 1 : 0;
                 int r0, r1;
-                if (EPI == kSwiGLU) {
-                    r0 = r1 = (it.sh ? 0 : it.e * a.I) + it.f * 128;
-                } else {
-                    r0 = (it.sh ? 0 : it.e * a.H) + it.f * 256;
-                    r1 = r0 + 128;
-                }
+                h_rows(a, it, EPI, r0, r1);
                 const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
                 const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
-                const int rc = rows_class(it.valid);
-                const uint32_t b_bytes = (32u << rc) * 128u;
-                const int ks_n = it.K / kHBK;
-                for (int ks = 0; ks < ks_n; ++ks) {
-                    if (!mbar_wait(empty + s, ph ^ 1, a.err)) { ok = false; break; }
-                    uint8_t *st = smem + s * kHStageBytes;
-                    const bool sc = (ks & 3) == 0;
-                    mbar_expect_tx(full + s, 2 * kHCode + b_bytes + (sc ? kHScSlot : 0));
-                    tma_2d(st, &a.a0[m], full + s, ks * 32, r0);
-                    tma_2d(st + kHCode, A1, full + s, ks * 32, r1);
-                    tma_2d(st + 2 * kHCode + 2 * kHTile, &a.b[rc], full + s, ks * kHBK, it.row0);
-                    if (sc) {
-                        uint8_t *slot = scs + (kbg++ & 1) * kHScSlot;
-                        tma_2d(slot, &a.s0[m], full + s, (ks >> 2) * 16, r0);
-                        tma_2d(slot + 2048, S1, full + s, (ks >> 2) * 16, r1);
-                    }
-                    used |= 1u << s;
-                    last_ph = (last_ph & ~(1u << s)) | (ph << s);
-                    if (++s == kHStages) { s = 0; ph ^= 1; }
+                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                    if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
+                    uint8_t *st = code_ring + c.s * kHCodeStage;
+                    mbar_expect_tx(cfull + c.s, kHCodeStage);
+                    tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
+                    tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
+                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, kc * 16, r0);
+                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
+                    used |= 1u << c.s;
+                    last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
+                    c.next(kHCStages);
                 }
             }
-            for (int t = 0; t < kHStages; ++t)
-                if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
+            for (int t = 0; t < kHCStages; ++t)
+                if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
+        } else if (lane == 1) {
+            // ---------------------------------------- producer of the B ring
+            RingPos b;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int rc = rows_class(it.valid);
+                const uint32_t bytes = (32u << rc) * 128u;
+                for (int q = 0; q < it.K / kHBK; ++q) {
+                    if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
+                    mbar_expect_tx(bfull + b.s, bytes);
+                    tma_2d(b_ring + b.s * kHBTile, &a.b[rc], bfull + b.s, q * kHBK, it.row0);
+                    used |= 1u << b.s;
+                    last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
+                    b.next(kHBStages);
+                }
+            }
+            for (int t = 0; t < kHBStages; ++t)
+                if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
         }
     } else if (warp >= 2 && warp < 2 + kConvWarps) {
         // ------------------------------------------------ NVFP4 -> f16 converters
-        // thread c widens row c of both A operands: 64 values, 4 scale blocks,
+        // thread c widens row c of both A operands, 64 K values per A slot,
         // written as 8 16-byte chunks in the 128-byte-swizzle K-major layout.
         const int c = threadIdx.x - 64;
-        int s = 0, kbg = 0;
-        uint32_t ph = 0;
+        const uint32_t sw = (uint32_t)(c & 7);
+        RingPos cs, as;
         bool ok = true;
-        const uint8_t *slot = scs;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             Item it;
             if (!decode_item_h(a, item, EPI, it)) continue;
-            const int ks_n = it.K / kHBK;
-            for (int ks = 0; ks < ks_n; ++ks) {
-                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
-                uint8_t *st = smem + s * kHStageBytes;
-                if ((ks & 3) == 0) slot = scs + (kbg++ & 1) * kHScSlot;
-                const uint32_t rbase = (uint32_t)((c >> 3) * 1024 + (c & 7) * 128);
+            for (int kc = 0; ok && kc < it.K / kHCK; ++kc) {
+                if (!mbar_wait(cfull + cs.s, cs.ph, a.err)) { ok = false; break; }
+                const uint8_t *st = code_ring + cs.s * kHCodeStage;
+                for (int j = 0; j < kHCK / kHBK; ++j) {
+                    if (!mbar_wait(aempty + as.s, as.ph ^ 1, a.err)) { ok = false; break; }
 #pragma unroll
-                for (int op = 0; op < 2; ++op) {
-                    const uint4 *cp = reinterpret_cast<const uint4 *>(st + op * kHCode + c * 32);
-                    const uint4 q0 = cp[0], q1 = cp[1];
-                    const uint32_t sw = *reinterpret_cast<const uint32_t *>(slot + op * 2048 + c * 16 + (ks & 3) * 4);
-                    const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                    uint8_t *dst = st + 2 * kHCode + op * kHTile + rbase;
+                    for (int op = 0; op < 2; ++op) {
+                        // 32 code bytes of row c for step j: logical 16-byte chunks 2j, 2j+1
+                        const uint8_t *row = st + op * kHCodeTile + c * 128;
+                        const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * j) ^ sw) << 4));
+                        const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * j + 1) ^ sw) << 4));
+                        const uint32_t scw =
+                            *reinterpret_cast<const uint32_t *>(st + 2 * kHCodeTile + op * 2048 + c * 16 + j * 4);
+                        const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                        uint8_t *dst = a_ring + (as.s * 2 + op) * kHATile + (c >> 3) * 1024 + (c & 7) * 128;
 #pragma unroll
-                    for (int blk = 0; blk < 4; ++blk) {
-                        const uint32_t sc2 = e4m3x2_to_f16x2(((sw >> (8 * blk)) & 0xFFu) * 0x101u);
-                        uint32_t h[8];
-                        e2m1x8_to_f16x8(cw[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
-                        e2m1x8_to_f16x8(cw[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
-                        uint32_t o[8];
+                        for (int blk = 0; blk < 4; ++blk) {
+                            const uint32_t sc2 = e4m3x2_to_f16x2(((scw >> (8 * blk)) & 0xFFu) * 0x101u);
+                            uint32_t h[8];
+                            e2m1x8_to_f16x8(cw[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
+                            e2m1x8_to_f16x8(cw[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
+                            uint32_t o[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[j]),
-                                                *reinterpret_cast<const __half2 *>(&sc2));
-                            o[j] = *reinterpret_cast<uint32_t *>(&v);
+                            for (int q = 0; q < 8; ++q) {
+                                __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[q]),
+                                                    *reinterpret_cast<const __half2 *>(&sc2));
+                                o[q] = *reinterpret_cast<uint32_t *>(&v);
+                            }
+                            const uint32_t ch0 = 2 * blk, ch1 = 2 * blk + 1;
+                            *reinterpret_cast<uint4 *>(dst + ((ch0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+                            *reinterpret_cast<uint4 *>(dst + ((ch1 ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                         }
-                        const int ch0 = 2 * blk, ch1 = 2 * blk + 1;
-                        *reinterpret_cast<uint4 *>(dst + ((ch0 ^ (c & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                        *reinterpret_cast<uint4 *>(dst + ((ch1 ^ (c & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(afull + as.s);
+                    as.next(kHAStages);
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(conv + s);
-                if (++s == kHStages) { s = 0; ph ^= 1; }
+                if (lane == 0) mbar_arrive(cempty + cs.s);
+                cs.next(kHCStages);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue (one lane)
         if (lane == 0) {
-            int s = 0, buf = 0;
-            uint32_t ph = 0, aph[2] = {0, 0};
+            RingPos as, bs;
+            int buf = 0;
+            uint32_t aph[2] = {0, 0};
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
@@ -618,21 +661,25 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 tc_fence_after();
                 const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
                 const uint32_t idesc = idesc_f16(32u << rows_class(it.valid));
-                const int ks_n = it.K / kHBK;
-                for (int ks = 0; ks < ks_n; ++ks) {
-                    if (!mbar_wait(conv + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                for (int q = 0; q < it.K / kHBK; ++q) {
+                    if (!mbar_wait(afull + as.s, as.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
-                    const uint32_t base = smem_u32(smem + s * kHStageBytes);
-                    const uint32_t a0 = base + 2 * kHCode, a1 = a0 + kHTile, bt = a1 + kHTile;
+                    const uint32_t a0 = smem_u32(a_ring + (as.s * 2) * kHATile), a1 = a0 + kHATile;
+                    const uint32_t bt = smem_u32(b_ring + bs.s * kHBTile);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t accum = (ks | kk) ? 1u : 0u;
+                        const uint32_t accum = (q | kk) ? 1u : 0u;
                         const uint64_t bd = desc_sw128(bt + 32 * kk);
                         mma_f16(d0, desc_sw128(a0 + 32 * kk), bd, idesc, accum);
                         mma_f16(d1, desc_sw128(a1 + 32 * kk), bd, idesc, accum);
                     }
-                    mma_commit(empty + s);
-                    if (++s == kHStages) { s = 0; ph ^= 1; }
+                    mma_commit(aempty + as.s);
+                    mma_commit(bempty + bs.s);
+                    as.next(kHAStages);
+                    bs.next(kHBStages);
                 }
                 if (!ok) break;
                 mma_commit(acc_full + buf);
@@ -821,6 +868,7 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t row_elems, uint64_t row
 }
 
 constexpr size_t kSmemBytes = kStages * kStageBytes + 512 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "FP4 pipeline exceeds shared memory");
 
 }  // namespace
 
@@ -876,12 +924,12 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
                                                      E, H, a.P, c.top_k, p.xp16);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 32, 128, false);
-        ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 32, 128, false);
+        ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
+        ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
         ok &= make_map(&a.s1[0], r.us, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
-        ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 32, 128, false);
-        ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 32, 128, false);
+        ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 128, 128, true);
+        ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
         ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
         for (int k2 = 0; k2 < 3; ++k2)
@@ -895,9 +943,9 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
         return cudaGetLastError();
     }
-    ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 32, 128, false);
+    ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
     ok &= make_map(&a.s0[0], r.ds, I / 16, (uint64_t)E * H, I / 16, 16, 128, false);
-    ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 32, 128, false);
+    ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 128, 128, true);
     ok &= make_map(&a.s0[1], sp.ds, Is_ / 16, H, Is_ / 16, 16, 128, false);
     a.a1[0] = a.a0[0];
     a.a1[1] = a.a0[1];

@@ -117,107 +117,88 @@ __global__ void __launch_bounds__(256) k_router_small(const uint16_t *__restrict
 }
 
 // Large batches: a block computes 16 tokens x 32 experts with 8 warps (2 x 4
-// sub-tiles of 8 x 8).  Slabs of 256 positions are staged TRANSPOSED in shared
-// memory -- x as [h][16 tokens] bf16 (48-byte rows), the router weight as
-// [h][32 experts] fp32 (144-byte rows), the paddings keeping the lanes' 16-byte
-// reads conflict-free -- through registers (double-buffered), so that lane l
-// reads the 8 tokens' x and the 8 experts' weights of position 32j + l with one
-// and two 16-byte loads.
-constexpr int kRT = 16, kRE = 32, kRSlab = 256;
-constexpr int kXPitch = 24;    // bf16 per x row (16 used)
-constexpr int kWPitch = 36;    // floats per weight row (32 used)
-constexpr int kRouterTiledSmem = 2 * kRSlab * kXPitch * 2 + 2 * kRSlab * kWPitch * 4;
+// sub-tiles of 8 x 8).  Slabs of 128 positions of x (bf16) and of the router
+// rows (fp32) stream through a 4-deep cp.async ring in their natural layout;
+// in slab j lane l reads position 32i + l (i < 4) of each of its 8 tokens and
+// 8 experts, so every lane still walks h = l, l+32, l+64, ... in increasing
+// order, and a warp's reads are 32 consecutive elements (no bank conflicts).
+constexpr int kRT = 16, kRE = 32, kRSlab = 128, kRStages = 4;
+constexpr int kRXBytes = kRT * kRSlab * 2;          // 4 KB
+constexpr int kRWBytes = kRE * kRSlab * 4;          // 16 KB
+constexpr int kRouterTiledSmem = kRStages * (kRXBytes + kRWBytes);
 
-__global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
-                                                      const float *__restrict__ rw, const float *__restrict__ bias,
-                                                      int E, float *__restrict__ logits, int *err,
-                                                      unsigned int *x_amax) {
+__global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
+                                                         const float *__restrict__ rw, const float *__restrict__ bias,
+                                                         int E, float *__restrict__ logits, int *err,
+                                                         unsigned int *x_amax) {
     extern __shared__ __align__(16) uint8_t rsmem[];
-    uint16_t *xT = reinterpret_cast<uint16_t *>(rsmem);                          // [2][256][24]
-    float *wT = reinterpret_cast<float *>(rsmem + 2 * kRSlab * kXPitch * 2);     // [2][256][36]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.y * kRT, e0 = blockIdx.x * kRE;
     const int tw = (warp >> 2) * 8, ew = (warp & 3) * 8;
     const int slabs = H / kRSlab;
     const bool check = (blockIdx.x == 0);
-    uint4 xr[2];
-    float4 wr[8];
-    bool bad = false;
-    float amax = 0.0f;
-    auto fetch = [&](int s) {
+    auto xs = [&](int b) { return reinterpret_cast<uint16_t *>(rsmem + b * (kRXBytes + kRWBytes)); };
+    auto ws = [&](int b) { return reinterpret_cast<float *>(rsmem + b * (kRXBytes + kRWBytes) + kRXBytes); };
+    auto load = [&](int s) {
+        if (s < slabs) {
+            const int b = s % kRStages;
+            {   // x: 16 rows x 16 chunks of 8 bf16
+                const int row = tid >> 4, c = tid & 15;
+                const bool v = t0 + row < T;
+                cp_async16(xs(b) + row * kRSlab + c * 8, x + (size_t)(v ? t0 + row : 0) * H + s * kRSlab + c * 8, v);
+            }
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {  // 16 tokens x 32 chunks of 8 bf16; lanes walk the tokens
-            const int idx = tid + 256 * i, row = idx & 15, c = idx >> 4;
-            xr[i] = make_uint4(0, 0, 0, 0);
-            if (t0 + row < T) xr[i] = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + row) * H + s * kRSlab + c * 8));
-            if (check) {
-                const uint32_t u[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    bad |= bf16x2_bad(u[j]);
-                    amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
-                }
+            for (int i = 0; i < 4; ++i) {   // weights: 32 rows x 32 chunks of 4 floats
+                const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+                const bool v = e0 + row < E;
+                cp_async16(ws(b) + row * kRSlab + c * 4, rw + (size_t)(v ? e0 + row : 0) * H + s * kRSlab + c * 4, v);
             }
         }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {  // 32 experts x 64 chunks of 4 floats; lanes walk the experts
-            const int idx = tid + 256 * i, row = idx & 31, c = idx >> 5;
-            wr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (e0 + row < E) wr[i] = __ldg(reinterpret_cast<const float4 *>(rw + (size_t)(e0 + row) * H + s * kRSlab + c * 4));
-        }
-    };
-    auto store = [&](int b) {
-        uint16_t *xb = xT + b * kRSlab * kXPitch;
-        float *wb = wT + b * kRSlab * kWPitch;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            const int idx = tid + 256 * i, row = idx & 15, c = idx >> 4;
-            const uint32_t u[4] = {xr[i].x, xr[i].y, xr[i].z, xr[i].w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                xb[(c * 8 + 2 * j) * kXPitch + row] = (uint16_t)(u[j] & 0xFFFFu);
-                xb[(c * 8 + 2 * j + 1) * kXPitch + row] = (uint16_t)(u[j] >> 16);
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int idx = tid + 256 * i, row = idx & 31, c = idx >> 5;
-            wb[(c * 4 + 0) * kWPitch + row] = wr[i].x;
-            wb[(c * 4 + 1) * kWPitch + row] = wr[i].y;
-            wb[(c * 4 + 2) * kWPitch + row] = wr[i].z;
-            wb[(c * 4 + 3) * kWPitch + row] = wr[i].w;
-        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
     float acc[8][8];
 #pragma unroll
     for (int t = 0; t < 8; ++t)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
-    fetch(0);
-    store(0);
-    __syncthreads();
+    bool bad = false;
+    float amax = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kRStages - 1; ++s) load(s);
     for (int s = 0; s < slabs; ++s) {
-        const int b = s & 1;
-        if (s + 1 < slabs) fetch(s + 1);
-        const uint16_t *xb = xT + b * kRSlab * kXPitch;
-        const float *wb = wT + b * kRSlab * kWPitch;
-#pragma unroll 2
-        for (int j = 0; j < kRSlab / 32; ++j) {
-            const int h = 32 * j + lane;
-            const uint4 xq = *reinterpret_cast<const uint4 *>(xb + h * kXPitch + tw);
-            const float4 w0 = *reinterpret_cast<const float4 *>(wb + h * kWPitch + ew);
-            const float4 w1 = *reinterpret_cast<const float4 *>(wb + h * kWPitch + ew + 4);
-            const float xv[8] = {bf16_lo(xq.x), bf16_hi(xq.x), bf16_lo(xq.y), bf16_hi(xq.y),
-                                 bf16_lo(xq.z), bf16_hi(xq.z), bf16_lo(xq.w), bf16_hi(xq.w)};
-            const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        load(s + kRStages - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRStages - 1) : "memory");
+        __syncthreads();
+        const uint16_t *xb = xs(s % kRStages);
+        const float *wb = ws(s % kRStages);
+        if (check && (warp & 3) == 0) {   // warps of expert sub-tile 0 check their tokens once
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (t0 + tw + t >= T) break;
+#pragma unroll
+                for (int i = 0; i < kRSlab / 32; ++i) {
+                    const uint32_t u = xb[(tw + t) * kRSlab + 32 * i + lane];
+                    bad |= (u & 0x7F80u) == 0x7F80u;
+                    amax = fmaxf(amax, fabsf(__uint_as_float(u << 16)));
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRSlab / 32; ++i) {
+            const int h = 32 * i + lane;
+            float xv[8], wv[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) xv[t] = __uint_as_float((uint32_t)xb[(tw + t) * kRSlab + h] << 16);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) wv[e] = wb[(ew + e) * kRSlab + h];
 #pragma unroll
             for (int t = 0; t < 8; ++t)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(xv[t], wv[e], acc[t][e]);
         }
-        if (s + 1 < slabs) store(b ^ 1);
         __syncthreads();
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
     for (int t = 0; t < 8; ++t)
 #pragma unroll
@@ -239,8 +220,7 @@ __global__ void __launch_bounds__(256) k_router_tiled(const uint16_t *__restrict
         const int tg = t0 + tw + t, eg = e0 + ew + e;
         if (tg < T && eg < E) logits[(size_t)tg * E + eg] = bias ? v + bias[eg] : v;
     }
-    if (check) {
-        // fold every thread's check into the error word and the amax
+    if (check && (warp & 3) == 0) {
         if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
         if (x_amax) {
             amax = warp_max(amax);

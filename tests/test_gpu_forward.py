@@ -182,3 +182,22 @@ def test_host_checks():
     with pytest.raises(moe.MoeError) as e:
         plan.forward(mis.view(w.tokens, w.hidden), case.rw, case.bias, case.routed)
     assert e.value.status == moe.ERR_MISALIGNED
+
+
+@pytest.mark.parametrize("name", ["decode4_w4a16", "verify16_w4a4"])
+def test_forward_replays_from_a_cuda_graph(name):
+    w = synth.WORKLOADS[name]
+    case = Case(w, 0)
+    plan = plan_for(w)
+    out = torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda")
+    plan.forward(case.x, case.rw, case.bias, case.routed, case.shared, out=out)   # warm-up outside capture
+    assert plan.sync_status() == moe.OK
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        plan.forward(case.x, case.rw, case.bias, case.routed, case.shared, out=out)
+    out.zero_()
+    for _ in range(2):
+        g.replay()
+    assert plan.sync_status() == moe.OK
+    ok, stats = oracle.compare_output(bf16_bits(out), case.oracle_forward()["out"])
+    assert ok, stats
