@@ -165,7 +165,8 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     {
         Stage s(plan, MOE_STAGE_ROUTE, st);
-        if (s.done(moe::launch_router(p, x, T, rw, bias, p.ids, p.wts, st), 2) != cudaSuccess) return MOE_ERR_CUDA;
+        if (s.done(moe::launch_router(p, x, T, rw, bias, p.ids, p.wts, st), moe::router_launches(T)) != cudaSuccess)
+            return MOE_ERR_CUDA;
     }
     {
         Stage s(plan, MOE_STAGE_GROUP, st);
@@ -240,7 +241,8 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
                      (cfg->has_shared ? (T + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows : 0);
     p.rows_pad_max = (p.rows_pad_max + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows;
     p.chunks_max = p.pairs_max / moe::kChunkRows + E + 2 + (cfg->has_shared ? T / moe::kChunkRows + 1 : 0);
-    p.tiles_max = p.pairs_max / moe::kTileRows + E + 2 + (cfg->has_shared ? T / moe::kTileRows + 1 : 0);
+    p.tile_rows = cfg->mode == MOE_W4A16 ? 64 : moe::kTileRows;
+    p.tiles_max = p.pairs_max / p.tile_rows + E + 2 + (cfg->has_shared ? T / p.tile_rows + 1 : 0);
     Carver dry;
     carve(p, dry);
     p.ws_bytes = dry.off + 256;

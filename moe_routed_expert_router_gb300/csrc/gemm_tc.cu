@@ -244,16 +244,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 for (int op = 0; op < 2; ++op) {
                     // in place: every lane reads its 4 rows, then (after the warp
                     // has read everything) writes its 4 atom words
-                    uint4 *tile = reinterpret_cast<uint4 *>(st + 3 * kTile + op * kSf);
+                    const uint32_t tile = smem_u32(st + 3 * kTile + op * kSf);
                     uint4 v[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = tile[lane + 32 * q];
+                    for (int q = 0; q < 4; ++q) v[q] = lds128(tile + 16 * (lane + 32 * q));
                     __syncwarp();
-                    uint4 *dst = tile;
-                    dst[0 * 32 + lane] = make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-                    dst[1 * 32 + lane] = make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-                    dst[2 * 32 + lane] = make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-                    dst[3 * 32 + lane] = make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+                    sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
+                    sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
+                    sts128(tile + 16 * (2 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
+                    sts128(tile + 16 * (3 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
@@ -404,41 +403,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
 }
 
 // ------------------------------------------------------------------ W4A16
-// W4A16 on the tensor cores (tcgen05 kind::f16, fp32 accumulators).  Three
-// shared-memory rings:
-//   code ring   (3 x 36 KB): NVFP4 weight codes (128-byte swizzle) + plain
-//                scale tiles of both A operands, 256 K values a stage;
-//   B ring      (3 x 16 KB): f16 token rows, 64 K values a stage;
-//   f16 A ring  (2 x 32 KB): the weights widened to f16 (128-byte swizzle,
-//                K-major), 64 K values a slot.
-// Four converter warps widen E2M1 -> f16 (cvt.rn.f16x2.e2m1x2) and multiply by
+// W4A16 on the tensor cores (tcgen05 kind::f16, fp32 accumulators), with the
+// widened weights held in tensor memory: the MMA takes its A operand (128
+// weight rows x 16 K) from TMEM and its B operand (token rows) from shared
+// memory.  Shared memory then carries only the 4-bit codes and the f16 token
+// rows, so its bandwidth no longer bounds the weight stream.
+//   code ring  (4 x 36 KB, shared): NVFP4 codes of both A operands (128-byte
+//              swizzle) + their plain scale tiles, 256 K values a stage;
+//   B ring     (6 x 8 KB, shared): f16 token rows (up to 64), 64 K values a
+//              stage, 128-byte swizzle;
+//   A ring     (4 x 64 TMEM columns): both operands widened to f16, 64 K
+//              values a stage (row r in lane r, two K values a column);
+//   accumulators (2 x 128 TMEM columns): gate / up (or the two down-row
+//              halves), N <= 64 token columns each, double-buffered so an
+//              item's epilogue overlaps the next item's MMAs.
+// Sixteen converter warps, four per 32-lane quarter (operand x half of the
+// stage's K values), widen E2M1 -> f16 (cvt.rn.f16x2.e2m1x2) and multiply by
 // the E4M3 block scale in f16; code x scale has at most 6 significant bits, so
-// the f16 weights are exact.  A code stage is released as soon as it is
-// converted, so the weight stream runs ahead of the MMAs.  The activations are
-// f16 rows: the permute kernel writes x * 2^-s, with s the smallest power of
-// two keeping the batch amax inside f16 (s = 0 for ordinary activations); the
-// epilogue multiplies 2^s back.  No scale factors live in tensor memory, so the
-// accumulator pairs (gate, up: 2 x 128 columns) are double-buffered and an
-// item's epilogue overlaps the next item's MMAs.
+// the f16 weights are exact.  The activations are f16 rows: the permute kernel
+// writes x * 2^-s, with s the smallest power of two keeping the batch amax
+// inside f16 (s = 0 for ordinary activations); the epilogue multiplies 2^s
+// back.  A work item is (tile of up to 64 token rows of one expert, 128 weight
+// rows of each operand); the grouping kernel cuts W4A16 tiles at 64 rows.
 constexpr int kHCK = 256;                        // K values per code stage
 constexpr int kHCodeTile = 128 * 128;            // 16 KB: 128 rows x 128 code bytes
 constexpr int kHCodeStage = 2 * kHCodeTile + 2 * 2048;   // A0, A1 codes + A0, A1 scales
-constexpr int kHCStages = 3;
+constexpr int kHCStages = 4;
 constexpr int kHBK = 64;                         // K values per MMA step
-constexpr int kHBTile = 128 * 128;               // 16 KB: up to 128 rows x 64 f16
-constexpr int kHBStages = 3;
-constexpr int kHATile = 128 * 128;               // 16 KB: 128 rows x 64 f16
-constexpr int kHAStages = 2;
-constexpr int kConvWarps = 4;
-constexpr int kHThreads = 32 * (2 + kConvWarps + kEpiWarps);
-constexpr size_t kHRingBytes = kHCStages * kHCodeStage + kHBStages * kHBTile + kHAStages * 2 * kHATile;
+constexpr int kHBRows = 64;                      // token rows per tile (MMA N <= 64)
+constexpr int kHBTile = kHBRows * 128;           // 8 KB: 64 rows x 64 f16
+constexpr int kHBStages = 6;
+constexpr int kHAStages = 4;                     // TMEM A ring
+constexpr uint32_t kHACol0 = 256;                // first TMEM column of the A ring
+constexpr int kConvSplit = 2;                    // converter warps per (operand, 32-lane quarter)
+constexpr int kConvWarps = 8 * kConvSplit;
+constexpr int kConvCols = 32 / kConvSplit;       // TMEM columns (2 K values each) a converter fills per A stage
+static_assert(kConvSplit == 2, "the converter loop below is written for two K halves");
+constexpr int kHEpiWarps = 4;
+constexpr int kHThreads = 32 * (2 + kConvWarps + kHEpiWarps);
+constexpr size_t kHRingBytes = (size_t)kHCStages * kHCodeStage + (size_t)kHBStages * kHBTile;
 constexpr size_t kHSmemBytes = kHRingBytes + 512 + 1024;
 static_assert(kHSmemBytes <= 227 * 1024, "W4A16 pipeline exceeds shared memory");
+static_assert(kHACol0 + kHAStages * 64 <= 512, "W4A16 TMEM plan exceeds 512 columns");
 
 struct HcArgs {
     CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 128 B x 128 rows, 128-byte swizzle
     CUtensorMap s0[2], s1[2];   // scales [rows][K/16], box 16 B x 128 rows
-    CUtensorMap b[3];           // f16 token rows [rows_pad][Kdim], box 64 x (32/64/128), 128-byte swizzle
+    CUtensorMap b[2];           // f16 token rows [rows_pad][Kdim], box 64 x (32/64), 128-byte swizzle
     const int4 *tiles;
     const CallScratch *scratch;
     int E, H, I, Is, nf;
@@ -462,20 +473,32 @@ __device__ __forceinline__ uint32_t idesc_f16(uint32_t n) {
     return (1u << 4) | (0u << 7) | (0u << 10) | ((n >> 3) << 17) | ((128u >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// D[tmem] (+)= A[tmem] x B[smem descriptor]
+__device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
 
+// 32 lanes x 16 columns from v[0..15] (each thread: its lane).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+// Item = tile * nf + f: the tile's token rows against weight-row group f.
+// Returns false for a group past the expert's intermediate size.
 __device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi, Item &it) {
     const int4 t = a.tiles[item / a.nf];
     it.f = item % a.nf;
     it.e = t.x;
     it.row0 = t.y;
-    it.valid = t.z;
+    it.valid = min(t.z, kHBRows);
     it.sh = (t.x == a.E);
     const int I = it.sh ? a.Is : a.I;
     if (epi == kSwiGLU) {
@@ -510,8 +533,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *code_ring = smem;
     uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
-    uint8_t *a_ring = b_ring + kHBStages * kHBTile;
-    uint64_t *cfull = reinterpret_cast<uint64_t *>(a_ring + kHAStages * 2 * kHATile);
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(b_ring + kHBStages * kHBTile);
     uint64_t *cempty = cfull + kHCStages;
     uint64_t *bfull = cempty + kHCStages;
     uint64_t *bempty = bfull + kHBStages;
@@ -528,7 +550,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, kConvWarps); }
         for (int i = 0; i < kHBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 1); }
         for (int i = 0; i < kHAStages; ++i) { mbar_init(afull + i, kConvWarps); mbar_init(aempty + i, 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kEpiWarps); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kHEpiWarps); }
         mbar_init(drain, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -578,7 +600,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item_h(a, item, EPI, it)) continue;
-                const int rc = rows_class(it.valid);
+                const int rc = it.valid <= 32 ? 0 : 1;
                 const uint32_t bytes = (32u << rc) * 128u;
                 for (int q = 0; q < it.K / kHBK; ++q) {
                     if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
@@ -594,10 +616,17 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         }
     } else if (warp >= 2 && warp < 2 + kConvWarps) {
         // ------------------------------------------------ NVFP4 -> f16 converters
-        // thread c widens row c of both A operands, 64 K values per A slot,
-        // written as 8 16-byte chunks in the 128-byte-swizzle K-major layout.
-        const int c = threadIdx.x - 64;
+        // warp (operand op, K half hf, lane quarter q): thread row c = 32 q +
+        // lane of operand op.  Per code stage it loads its row's code chunks
+        // 2j + hf (j < 4) and scale bytes, then per A stage j widens those 32 K
+        // values (two scale blocks) into 16 TMEM columns of its lane.
+        const int cw = (warp - 2) >> 2;
+        const int op = cw & 1, hf = cw >> 1;
+        const int q = warp & 3;
+        const int c = q * 32 + lane;
         const uint32_t sw = (uint32_t)(c & 7);
+        const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + kHACol0 + op * 32 + hf * kConvCols;
+        const uint32_t ring0 = smem_u32(code_ring);
         RingPos cs, as;
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
@@ -605,45 +634,44 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             if (!decode_item_h(a, item, EPI, it)) continue;
             for (int kc = 0; ok && kc < it.K / kHCK; ++kc) {
                 if (!mbar_wait(cfull + cs.s, cs.ph, a.err)) { ok = false; break; }
-                const uint8_t *st = code_ring + cs.s * kHCodeStage;
+                const uint32_t st = ring0 + cs.s * kHCodeStage;
+                const uint32_t row = st + op * kHCodeTile + c * 128;
+                uint4 cq[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) cq[j] = lds128(row + (((uint32_t)(2 * j + hf) ^ sw) << 4));
+                const uint4 scv = lds128(st + 2 * kHCodeTile + op * 2048 + c * 16);
+                const uint32_t scw[4] = {scv.x, scv.y, scv.z, scv.w};
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cempty + cs.s);   // this warp's bytes are in registers
+                cs.next(kHCStages);
+#pragma unroll
                 for (int j = 0; j < kHCK / kHBK; ++j) {
-                    if (!mbar_wait(aempty + as.s, as.ph ^ 1, a.err)) { ok = false; break; }
+                    const uint32_t cw4[4] = {cq[j].x, cq[j].y, cq[j].z, cq[j].w};
+                    uint32_t o[kConvCols];
 #pragma unroll
-                    for (int op = 0; op < 2; ++op) {
-                        // 32 code bytes of row c for step j: logical 16-byte chunks 2j, 2j+1
-                        const uint8_t *row = st + op * kHCodeTile + c * 128;
-                        const uint4 q0 = *reinterpret_cast<const uint4 *>(row + (((2 * j) ^ sw) << 4));
-                        const uint4 q1 = *reinterpret_cast<const uint4 *>(row + (((2 * j + 1) ^ sw) << 4));
-                        const uint32_t scw =
-                            *reinterpret_cast<const uint32_t *>(st + 2 * kHCodeTile + op * 2048 + c * 16 + j * 4);
-                        const uint32_t cw[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                        uint8_t *dst = a_ring + (as.s * 2 + op) * kHATile + (c >> 3) * 1024 + (c & 7) * 128;
+                    for (int blk = 0; blk < 2; ++blk) {
+                        const uint32_t sb = (scw[j] >> (16 * hf + 8 * blk)) & 0xFFu;
+                        const uint32_t sc2 = e4m3x2_to_f16x2(sb * 0x101u);
+                        uint32_t h[8];
+                        e2m1x8_to_f16x8(cw4[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
+                        e2m1x8_to_f16x8(cw4[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
 #pragma unroll
-                        for (int blk = 0; blk < 4; ++blk) {
-                            const uint32_t sc2 = e4m3x2_to_f16x2(((scw >> (8 * blk)) & 0xFFu) * 0x101u);
-                            uint32_t h[8];
-                            e2m1x8_to_f16x8(cw[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
-                            e2m1x8_to_f16x8(cw[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
-                            uint32_t o[8];
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[q]),
-                                                    *reinterpret_cast<const __half2 *>(&sc2));
-                                o[q] = *reinterpret_cast<uint32_t *>(&v);
-                            }
-                            const uint32_t ch0 = 2 * blk, ch1 = 2 * blk + 1;
-                            *reinterpret_cast<uint4 *>(dst + ((ch0 ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-                            *reinterpret_cast<uint4 *>(dst + ((ch1 ^ sw) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+                        for (int e = 0; e < 8; ++e) {
+                            __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[e]),
+                                                *reinterpret_cast<const __half2 *>(&sc2));
+                            o[blk * 8 + e] = *reinterpret_cast<uint32_t *>(&v);
                         }
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    if (ok && !mbar_wait(aempty + as.s, as.ph ^ 1, a.err)) ok = false;
+                    if (ok) {
+                        tmem_st16(t_lane + as.s * 64, o);
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                        tc_fence_before();
+                    }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(afull + as.s);
+                    if (lane == 0 && ok) mbar_arrive(afull + as.s);
                     as.next(kHAStages);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(cempty + cs.s);
-                cs.next(kHCStages);
             }
         }
     } else if (warp == 1) {
@@ -651,30 +679,30 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         if (lane == 0) {
             RingPos as, bs;
             int buf = 0;
-            uint32_t aph[2] = {0, 0};
+            uint32_t aph = 0;   // bit b: parity of accumulator buffer b
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item_h(a, item, EPI, it)) continue;
-                if (!mbar_wait(acc_empty + buf, aph[buf] ^ 1, a.err)) break;
-                aph[buf] ^= 1;
+                if (!mbar_wait(acc_empty + buf, ((aph >> buf) & 1u) ^ 1u, a.err)) break;
+                aph ^= 1u << buf;
                 tc_fence_after();
-                const uint32_t d0 = tmem + buf * 256, d1 = d0 + 128;
-                const uint32_t idesc = idesc_f16(32u << rows_class(it.valid));
-                for (int q = 0; q < it.K / kHBK; ++q) {
+                const uint32_t d0 = tmem + buf * 128, d1 = d0 + 64;
+                const uint32_t idesc = idesc_f16(it.valid <= 32 ? 32u : 64u);
+                for (int qq = 0; qq < it.K / kHBK; ++qq) {
                     if (!mbar_wait(afull + as.s, as.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(a_ring + (as.s * 2) * kHATile), a1 = a0 + kHATile;
+                    const uint32_t at = tmem + kHACol0 + as.s * 64;
                     const uint32_t bt = smem_u32(b_ring + bs.s * kHBTile);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t accum = (q | kk) ? 1u : 0u;
+                        const uint32_t accum = (qq | kk) ? 1u : 0u;
                         const uint64_t bd = desc_sw128(bt + 32 * kk);
-                        mma_f16(d0, desc_sw128(a0 + 32 * kk), bd, idesc, accum);
-                        mma_f16(d1, desc_sw128(a1 + 32 * kk), bd, idesc, accum);
+                        mma_f16_ts(d0, at + 8 * kk, bd, idesc, accum);
+                        mma_f16_ts(d1, at + 32 + 8 * kk, bd, idesc, accum);
                     }
                     mma_commit(aempty + as.s);
                     mma_commit(bempty + bs.s);
@@ -689,32 +717,30 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             mbar_wait(drain, 0, a.err);
         }
     } else {
-        // ------------------------------------------------ epilogue (8 warps)
-        const int ew = warp - (2 + kConvWarps);
+        // ------------------------------------------------ epilogue (4 warps)
         const int quad = warp & 3;
-        const int col0 = (ew >> 2) * 64;
         int buf = 0;
-        uint32_t aph[2] = {0, 0};
+        uint32_t aph = 0;   // bit b: parity of accumulator buffer b
         const int xs = f16_shift(a.scratch->x_amax);
         const float xunscale = __uint_as_float((uint32_t)(127 + xs) << 23);   // 2^s
         bool range_bad = false;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             Item it;
             if (!decode_item_h(a, item, EPI, it)) continue;
-            if (!mbar_wait(acc_full + buf, aph[buf], a.err)) break;
-            aph[buf] ^= 1;
+            if (!mbar_wait(acc_full + buf, (aph >> buf) & 1u, a.err)) break;
+            aph ^= 1u << buf;
             tc_fence_after();
-            const uint32_t lane_base = tmem + buf * 256 + ((uint32_t)(quad * 32) << 16);
+            const uint32_t lane_base = tmem + buf * 128 + ((uint32_t)(quad * 32) << 16);
             const int m = it.sh ? 1 : 0;
             const int e = it.sh ? 0 : it.e;
-            const int n_end = min(col0 + 64, it.valid);
+            const int n_end = it.valid;
             if (EPI == kSwiGLU) {
                 const float sg = a.ts_a0[m][e] * xunscale, su = a.ts_a1[m][e] * xunscale;
                 const int feat = it.f * 128 + quad * 32 + lane;
-                for (int n0 = col0; n0 < n_end; n0 += 16) {
+                for (int n0 = 0; n0 < n_end; n0 += 16) {
                     float g[16], u[16];
                     tmem_ld16_nowait(lane_base + n0, g);
-                    tmem_ld16_nowait(lane_base + 128 + n0, u);
+                    tmem_ld16_nowait(lane_base + 64 + n0, u);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -732,28 +758,28 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 int tok[2];
                 float wgt[2];
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int n = col0 + lane + 32 * q;
-                    tok[q] = 0;
-                    wgt[q] = 0.0f;
+                for (int qd = 0; qd < 2; ++qd) {
+                    const int n = lane + 32 * qd;
+                    tok[qd] = 0;
+                    wgt[qd] = 0.0f;
                     if (n < it.valid) {
                         const int pair = a.pad_pair[it.row0 + n];
-                        tok[q] = pair >= a.P ? pair - a.P : pair / a.k;
-                        wgt[q] = pair >= a.P ? 1.0f : a.wts[pair];
+                        tok[qd] = pair >= a.P ? pair - a.P : pair / a.k;
+                        wgt[qd] = pair >= a.P ? 1.0f : a.wts[pair];
                     }
                 }
                 const int j0 = it.f * 256 + quad * 32 + lane;
-                for (int n0 = col0; n0 < n_end; n0 += 16) {
+                for (int n0 = 0; n0 < n_end; n0 += 16) {
                     float y0[16], y1[16];
                     tmem_ld16_nowait(lane_base + n0, y0);
-                    tmem_ld16_nowait(lane_base + 128 + n0, y1);
+                    tmem_ld16_nowait(lane_base + 64 + n0, y1);
                     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const int cc = n0 + j - col0;
-                        const int t = __shfl_sync(0xffffffffu, tok[cc >> 5], cc & 31);
-                        const float wv = __shfl_sync(0xffffffffu, wgt[cc >> 5], cc & 31) * ds;
-                        if (n0 + j < n_end) {
+                        const int cc = n0 + j;
+                        const int t = __shfl_sync(0xffffffffu, (cc >> 5) ? tok[1] : tok[0], cc & 31);
+                        const float wv = __shfl_sync(0xffffffffu, (cc >> 5) ? wgt[1] : wgt[0], cc & 31) * ds;
+                        if (cc < n_end) {
                             float *dst = a.acc + (size_t)t * a.H + j0;
                             atomicAdd(dst, y0[j] * wv);
                             atomicAdd(dst + 128, y1[j] * wv);
@@ -932,7 +958,7 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
         ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
-        for (int k2 = 0; k2 < 3; ++k2)
+        for (int k2 = 0; k2 < 2; ++k2)
             ok &= make_map(&a.b[k2], p.xp16, H, p.rows_pad_max, (uint64_t)H * 2, 64, 32u << k2, true, true);
         a.nf = Imax / 128;
         a.ts_a0[0] = r.gts;
@@ -951,7 +977,7 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.a1[1] = a.a0[1];
     a.s1[0] = a.s0[0];
     a.s1[1] = a.s0[1];
-    for (int k2 = 0; k2 < 3; ++k2)
+    for (int k2 = 0; k2 < 2; ++k2)
         ok &= make_map(&a.b[k2], p.hbuf, Imax, p.rows_pad_max, (uint64_t)Imax * 2, 64, 32u << k2, true, true);
     a.nf = H / 256;
     a.ts_a0[0] = r.dts;

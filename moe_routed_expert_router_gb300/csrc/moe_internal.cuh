@@ -31,7 +31,7 @@ struct CallScratch {
     unsigned int hs_amax;       // same for the shared expert's rows
     int n_chunks;               // CUDA-core work chunks
     int n_tiles;                // tensor-core tiles (gate/up)
-    int n_active;               // experts with at least one pair
+    int route_done;             // router blocks finished (the last one runs top-k)
     int n_chunks_routed;        // chunks of routed experts (the shared expert's follow)
     int pad;
 };
@@ -57,8 +57,9 @@ struct Plan {
     int32_t *inv = nullptr;         // [P] pair -> padded row
     int32_t *pad_pair = nullptr;    // [rows_pad] pair at a padded row (-1 pad, >= P shared token)
     int4 *chunks = nullptr;         // [chunks_max] {expert, first padded row, rows, 0}
-    int4 *tiles = nullptr;          // [tiles_max] {expert, first padded row, valid rows, 0}, 128-row tiles
+    int4 *tiles = nullptr;          // [tiles_max] {expert, first padded row, valid rows, 0}
     int64_t tiles_max = 0;
+    int tile_rows = kTileRows;      // rows a tensor-core tile covers: 128 (W4A4) or 64 (W4A16)
     uint8_t *xp = nullptr;          // [rows_pad][H/2] permuted x codes (tensor-core path)
     uint8_t *xp_atoms = nullptr;    // [rows_pad/128][H/64][512] their scales, tensor-core layout
     uint8_t *hq_atoms = nullptr;    // [rows_pad/128][Imax/64][512] SwiGLU scales, tensor-core layout
@@ -181,6 +182,17 @@ constexpr uint64_t kWaitNs = 1000000000ull;  // bound on any single mbarrier wai
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+// Explicit shared-memory accesses (32-bit shared addresses), for buffers whose
+// pointer the compiler cannot trace back to shared memory.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ void sts128(uint32_t a, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
 __device__ __forceinline__ uint64_t now_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -238,6 +250,7 @@ struct ExpertPtrs {
     const float *gts, *uts, *dts;
 };
 
+int router_launches(int T);
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias,
                           int32_t *ids, float *wts, cudaStream_t st);
 cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out,

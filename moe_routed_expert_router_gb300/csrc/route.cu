@@ -30,92 +30,6 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool vali
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(n) : "memory");
 }
 
-// Small batches (T <= 16): 8 warps a block, warp w takes expert
-// e0 + w / ntg and tokens (w % ntg) * 8 .. +8, ntg = ceil(T / 8).  Slabs of
-// 256 positions of the block's router rows and of x are double-buffered in
-// shared memory (cp.async); every lane then reads its positions from there.
-constexpr int kSmallSlab = 256;
-
-__global__ void __launch_bounds__(256) k_router_small(const uint16_t *__restrict__ x, int T, int H,
-                                                      const float *__restrict__ rw, const float *__restrict__ bias,
-                                                      int E, float *__restrict__ logits, int *err,
-                                                      unsigned int *x_amax) {
-    __shared__ __align__(16) float wsm[2][8][kSmallSlab];        // 16 KB
-    __shared__ __align__(16) uint16_t xsm[2][16][kSmallSlab];    // 16 KB
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int ntg = (T + 7) / 8, epb = 8 / ntg;
-    const int e0 = blockIdx.x * epb;
-    const int ew = warp / ntg, t0 = (warp % ntg) * 8;
-    const int e = e0 + ew;
-    const int slabs = H / kSmallSlab;
-    const bool check = (blockIdx.x == 0);
-    auto load = [&](int s, int b) {
-        // router rows: epb rows x 256 floats = epb * 64 chunks of 16 B
-        for (int idx = tid; idx < epb * (kSmallSlab / 4); idx += 256) {
-            const int r = idx / (kSmallSlab / 4), c = idx % (kSmallSlab / 4);
-            const bool v = e0 + r < E;
-            cp_async16(&wsm[b][r][c * 4], rw + (size_t)(v ? e0 + r : 0) * H + s * kSmallSlab + c * 4, v);
-        }
-        // x rows: T rows x 256 bf16 = T * 32 chunks
-        for (int idx = tid; idx < T * (kSmallSlab / 8); idx += 256) {
-            const int r = idx / (kSmallSlab / 8), c = idx % (kSmallSlab / 8);
-            cp_async16(&xsm[b][r][c * 8], x + (size_t)r * H + s * kSmallSlab + c * 8, true);
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");
-    };
-    float acc[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) acc[t] = 0.0f;
-    bool bad = false;
-    float amax = 0.0f;
-    load(0, 0);
-    for (int s = 0; s < slabs; ++s) {
-        const int b = s & 1;
-        if (s + 1 < slabs) {
-            load(s + 1, b ^ 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-        }
-        __syncthreads();
-        if (check && warp == 0) {  // x check and amax: warp 0 of block 0 reads every token once
-            for (int idx = lane; idx < T * (kSmallSlab / 2); idx += 32) {
-                const uint32_t u = reinterpret_cast<const uint32_t *>(&xsm[b][0][0])[idx];
-                bad |= bf16x2_bad(u);
-                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u)), fabsf(bf16_hi(u))));
-            }
-        }
-        if (e < E) {
-#pragma unroll 4
-            for (int j = 0; j < kSmallSlab / 32; ++j) {
-                const int h = 32 * j + lane;
-                const float wv = wsm[b][ew][h];
-#pragma unroll
-                for (int t = 0; t < 8; ++t)
-                    if (t0 + t < T) acc[t] = fmaf(__uint_as_float((uint32_t)xsm[b][t0 + t][h] << 16), wv, acc[t]);
-            }
-        }
-        __syncthreads();
-    }
-    if (e < E) {
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            if (t0 + t >= T) break;
-            float v = acc[t];
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) logits[(size_t)(t0 + t) * E + e] = bias ? v + bias[e] : v;
-        }
-    }
-    if (check && warp == 0) {
-        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(err, kErrNonFinite);
-        if (x_amax) {
-            amax = warp_max(amax);
-            if (lane == 0) atomic_max_nonneg(x_amax, amax);
-        }
-    }
-}
-
 // Large batches: a block computes 16 tokens x 32 experts with 8 warps (2 x 4
 // sub-tiles of 8 x 8).  Slabs of 128 positions of x (bf16) and of the router
 // rows (fp32) stream through a 4-deep cp.async ring in their natural layout;
@@ -229,22 +143,20 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
     }
 }
 
-// One warp per token: top-k by logit (ties -> lower id), then the weights.
-// NPL logits per lane (expert lane + 32*i).
+// Top-k of token t by logit (ties -> lower id), then the weights; one warp,
+// NPL logits per lane (expert lane + 32*i).  Logits are read through L2 (they
+// may come from other blocks of the same launch).
 template <int NPL>
-__global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ logits, int T, int E, int k,
-                                                     int kind, int renorm, int32_t *__restrict__ ids,
-                                                     float *__restrict__ wts, int32_t *__restrict__ counts,
-                                                     int *err) {
+__device__ __forceinline__ void topk_token(const float *__restrict__ logits, int t, int E, int k, int kind, int renorm,
+                                           int32_t *__restrict__ ids, float *__restrict__ wts,
+                                           int32_t *__restrict__ counts, int *err) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
-    if (t >= T) return;
     const float NEG = -__int_as_float(0x7f800000);
     float v[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         int e = lane + 32 * i;
-        v[i] = (e < E) ? logits[(size_t)t * E + e] : NEG;
+        v[i] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : NEG;
     }
     uint32_t taken = 0;
 #pragma unroll
@@ -303,6 +215,114 @@ __global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ l
     if (lane < k) wts[(size_t)t * k + lane] = num / den;
 }
 
+// One warp per token.
+template <int NPL>
+__global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ logits, int T, int E, int k,
+                                                     int kind, int renorm, int32_t *__restrict__ ids,
+                                                     float *__restrict__ wts, int32_t *__restrict__ counts,
+                                                     int *err) {
+    const int t = blockIdx.x * 4 + (threadIdx.x >> 5);
+    if (t >= T) return;
+    topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
+}
+
+// Decode-sized batches (T <= 16), router and top-k in one launch: block e
+// computes expert e's logit for every token.  The router row (H fp32) is
+// staged in shared memory at once, x (all T rows) streams through a 4-deep
+// cp.async ring of 256-position slabs; warp t walks token t, lane l taking
+// positions 32j + l in increasing j.  Each block also checks a 1/E slice of x
+// (non-finite values, amax).  The last block to finish (a ticket in the
+// per-call scratch) runs the top-k for all tokens, one warp a token.
+constexpr int kDecodeRouterThreads = 512;
+constexpr int kDSlab = 256, kDStages = 4;
+
+size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * kDSlab * 2; }
+
+template <int NPL>
+__global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
+    const uint16_t *__restrict__ x, int T, int H, const float *__restrict__ rw, const float *__restrict__ bias,
+    int E, int k, int kind, int renorm, float *__restrict__ logits, int32_t *__restrict__ ids,
+    float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err) {
+    extern __shared__ __align__(16) float wrow[];     // [H], then x slabs [kDStages][T][kDSlab] bf16
+    uint16_t *xs = reinterpret_cast<uint16_t *>(wrow + H);
+    __shared__ float s_amax[kDecodeRouterThreads / 32];
+    __shared__ int s_bad[kDecodeRouterThreads / 32];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int e = blockIdx.x;
+    const int slabs = H / kDSlab;
+    for (int c = tid; c < H / 4; c += kDecodeRouterThreads) cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
+    auto load_x = [&](int sl) {
+        if (sl < slabs) {
+            uint16_t *dst = xs + (size_t)(sl % kDStages) * T * kDSlab;
+            for (int idx = tid; idx < T * (kDSlab / 8); idx += kDecodeRouterThreads) {
+                const int r = idx / (kDSlab / 8), c = idx % (kDSlab / 8);
+                cp_async16(dst + r * kDSlab + c * 8, x + (size_t)r * H + sl * kDSlab + c * 8, true);
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");   // group 0 also carries the router row
+    };
+#pragma unroll
+    for (int sl = 0; sl < kDStages - 1; ++sl) load_x(sl);
+    {   // this block's slice of x: non-finite check and amax
+        const int nchunks = T * H / 8;
+        const int per = (nchunks + gridDim.x - 1) / gridDim.x;
+        const int c0 = blockIdx.x * per, c1 = min(nchunks, c0 + per);
+        bool bad = false;
+        float amax = 0.0f;
+        for (int c = c0 + tid; c < c1; c += kDecodeRouterThreads) {
+            const uint4 q = __ldg(reinterpret_cast<const uint4 *>(x) + c);
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                bad |= bf16x2_bad(u[i]);
+                amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(u[i])), fabsf(bf16_hi(u[i]))));
+            }
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        amax = warp_max(amax);
+        if (lane == 0) { s_amax[warp] = amax; s_bad[warp] = bad; }
+    }
+    float acc = 0.0f;
+    for (int sl = 0; sl < slabs; ++sl) {
+        load_x(sl + kDStages - 1);
+        asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
+        __syncthreads();
+        if (warp < T) {
+            const uint16_t *xr = xs + (size_t)(sl % kDStages) * T * kDSlab + warp * kDSlab;
+            const float *wr = wrow + sl * kDSlab;
+#pragma unroll
+            for (int j = 0; j < kDSlab / 32; ++j)
+                acc = fmaf(__uint_as_float((uint32_t)xr[32 * j + lane] << 16), wr[32 * j + lane], acc);
+        }
+        __syncthreads();
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    if (warp == 0) {
+        float m = lane < kDecodeRouterThreads / 32 ? s_amax[lane] : 0.0f;
+        int b = lane < kDecodeRouterThreads / 32 ? s_bad[lane] : 0;
+        m = warp_max(m);
+        b = __any_sync(0xffffffffu, b);
+        if (lane == 0) {
+            if (b) atomicOr(err, kErrNonFinite);
+            if (m > 0.0f) atomic_max_nonneg(&sc->x_amax, m);
+        }
+    }
+    if (warp < T) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) logits[(size_t)warp * E + e] = bias ? acc + bias[e] : acc;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&sc->route_done, 1) == (int)gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int t = warp; t < T; t += kDecodeRouterThreads / 32)
+        topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
+}
+
 // Single-block grouping (1024 threads).  Stable counting sort of the pairs
 // p = t*k + j by expert: each of the 32 warps owns a contiguous segment of
 // pairs, counts it per expert, the per-(warp, expert) bases are scanned, and a
@@ -317,61 +337,62 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
                                                 int4 *__restrict__ tiles,
                                                 CallScratch *scratch, int32_t *__restrict__ offsets_out,
                                                 int32_t *__restrict__ sorted_out, int build_work, int rows_cap,
-                                                int *err) {
+                                                int tile_rows, int *err) {
     extern __shared__ int smem[];
     int *wc = smem;                        // [32][E]
     int *s_off = smem + 32 * E;            // [E+1]
     int *s_poff = s_off + (E + 1);         // [E+2]
     int *s_cb = s_poff + (E + 2);          // [E+2] chunk bases
     int *s_tb = s_cb + (E + 2);            // [E+2] tile bases
-    __shared__ int s_warp[32][3];
+    __shared__ int s_warp[32][4];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
-    // exclusive scans over experts of (count, padded count, chunks)
-    int c = 0, pc = 0, nc = 0;
+    // exclusive scans over experts of (count, padded count, chunks, tiles)
+    int c = 0, pc = 0, nc = 0, nt = 0;
     if (tid < E) {
         c = counts[tid];
         pc = (c + kTileRows - 1) / kTileRows * kTileRows;
         nc = (c + kChunkRows - 1) / kChunkRows;
+        nt = (c + tile_rows - 1) / tile_rows;
     }
-    int a = c, b = pc, d = nc;
+    int a = c, b = pc, d = nc, f = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o),
-            yd = __shfl_up_sync(0xffffffffu, d, o);
-        if (lane >= o) { a += ya; b += yb; d += yd; }
+            yd = __shfl_up_sync(0xffffffffu, d, o), yf = __shfl_up_sync(0xffffffffu, f, o);
+        if (lane >= o) { a += ya; b += yb; d += yd; f += yf; }
     }
-    if (lane == 31) { s_warp[warp][0] = a; s_warp[warp][1] = b; s_warp[warp][2] = d; }
+    if (lane == 31) { s_warp[warp][0] = a; s_warp[warp][1] = b; s_warp[warp][2] = d; s_warp[warp][3] = f; }
     __syncthreads();
     if (warp == 0) {
-        int wa = s_warp[lane][0], wb = s_warp[lane][1], wd = s_warp[lane][2];
+        int wa = s_warp[lane][0], wb = s_warp[lane][1], wd = s_warp[lane][2], wf = s_warp[lane][3];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int ya = __shfl_up_sync(0xffffffffu, wa, o), yb = __shfl_up_sync(0xffffffffu, wb, o),
-                yd = __shfl_up_sync(0xffffffffu, wd, o);
-            if (lane >= o) { wa += ya; wb += yb; wd += yd; }
+                yd = __shfl_up_sync(0xffffffffu, wd, o), yf = __shfl_up_sync(0xffffffffu, wf, o);
+            if (lane >= o) { wa += ya; wb += yb; wd += yd; wf += yf; }
         }
-        s_warp[lane][0] = wa; s_warp[lane][1] = wb; s_warp[lane][2] = wd;
+        s_warp[lane][0] = wa; s_warp[lane][1] = wb; s_warp[lane][2] = wd; s_warp[lane][3] = wf;
     }
     __syncthreads();
     const int ba = warp ? s_warp[warp - 1][0] : 0, bb = warp ? s_warp[warp - 1][1] : 0,
-              bd = warp ? s_warp[warp - 1][2] : 0;
+              bd = warp ? s_warp[warp - 1][2] : 0, bf = warp ? s_warp[warp - 1][3] : 0;
     if (tid < E) {
         s_off[tid] = ba + a - c;
         s_poff[tid] = bb + b - pc;
         s_cb[tid] = bd + d - nc;
-        s_tb[tid] = (bb + b - pc) / kTileRows;   // a padded segment holds count/128 (rounded up) tiles
+        s_tb[tid] = bf + f - nt;
     }
     if (tid == 0) {
-        int tot_a = s_warp[31][0], tot_b = s_warp[31][1], tot_d = s_warp[31][2];
+        int tot_a = s_warp[31][0], tot_b = s_warp[31][1], tot_d = s_warp[31][2], tot_f = s_warp[31][3];
         s_off[E] = tot_a;
         s_poff[E] = tot_b;
         s_poff[E + 1] = tot_b + (has_shared ? (T + kTileRows - 1) / kTileRows * kTileRows : 0);
         s_cb[E] = tot_d;
         s_cb[E + 1] = tot_d + (has_shared ? (T + kChunkRows - 1) / kChunkRows : 0);
-        s_tb[E] = tot_b / kTileRows;
-        s_tb[E + 1] = s_poff[E + 1] / kTileRows;
+        s_tb[E] = tot_f;
+        s_tb[E + 1] = tot_f + (has_shared ? (T + tile_rows - 1) / tile_rows : 0);
         if (tot_a != P) atomicOr(err, kErrDevice);
     }
     __syncthreads();
@@ -440,27 +461,22 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         int sh_rows = s_poff[E + 1] - s_poff[E];
         for (int q = tid; q < sh_rows; q += 1024) pad_pair[s_poff[E] + q] = (q < T) ? P + q : -1;
     }
-    // CUDA-core work chunks: up to kChunkRows rows of one expert each
-    for (int e = tid; e <= E; e += 1024) {
-        int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (has_shared ? T : 0);
-        int cb = s_cb[e];
-        for (int q = 0; q * kChunkRows < cnt; ++q)
+    // CUDA-core work chunks (up to kChunkRows rows of one expert) and
+    // tensor-core tiles (tile_rows padded rows of one expert, inside its
+    // 128-row-aligned segment): one warp an expert, its lanes writing
+    // consecutive entries
+    for (int e = warp; e <= E; e += 32) {
+        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (has_shared ? T : 0);
+        const int cb = s_cb[e], tb = s_tb[e];
+        for (int q = lane; q * kChunkRows < cnt; q += 32)
             chunks[cb + q] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
-    }
-    // tensor-core tiles: 128 padded rows of one expert each
-    for (int e = tid; e <= E; e += 1024) {
-        int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (has_shared ? T : 0);
-        int tb = s_tb[e];
-        for (int q = 0; q * kTileRows < cnt; ++q)
-            tiles[tb + q] = make_int4(e, s_poff[e] + q * kTileRows, min(kTileRows, cnt - q * kTileRows), 0);
+        for (int q = lane; q * tile_rows < cnt; q += 32)
+            tiles[tb + q] = make_int4(e, s_poff[e] + q * tile_rows, min(tile_rows, cnt - q * tile_rows), 0);
     }
     if (tid == 0) {
         scratch->n_tiles = s_tb[E + 1];
         scratch->n_chunks = s_cb[E + 1];
         scratch->n_chunks_routed = s_cb[E];
-        int na = 0;
-        for (int e = 0; e < E; ++e) na += (s_off[e + 1] > s_off[e]);
-        scratch->n_active = na;
     }
 }
 
@@ -468,20 +484,29 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
 
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias, int32_t *ids,
                           float *wts, cudaStream_t st) {
-    const int H = p.cfg.hidden, E = p.cfg.num_experts;
-    unsigned int *amax = &p.scratch->x_amax;   // batch amax of x (W4A4 quantiser, f16 range of W4A16)
+    const int H = p.cfg.hidden, E = p.cfg.num_experts, k = p.cfg.top_k;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
-    if (T <= 16 && H % kSmallSlab == 0) {
-        const int ntg = (T + 7) / 8, epb = 8 / ntg;
-        k_router_small<<<(E + epb - 1) / epb, 256, 0, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
-    } else {
-        dim3 g((E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
-        k_router_tiled<<<g, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
+    const int npl = (E + 31) / 32;
+    if (T <= kDecodeRouterThreads / 32 && H % 256 == 0) {
+        const size_t smem = decode_router_smem(H, T);
+#define MOE_DEC(N)                                                                                           \
+    k_router_decode<N><<<E, kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router,          \
+                                                              p.cfg.renormalize, p.logits, ids, wts, p.counts, \
+                                                              p.scratch, p.err)
+        if (npl <= 1) MOE_DEC(1);
+        else if (npl <= 2) MOE_DEC(2);
+        else if (npl <= 4) MOE_DEC(4);
+        else if (npl <= 8) MOE_DEC(8);
+        else if (npl <= 16) MOE_DEC(16);
+        else MOE_DEC(32);
+#undef MOE_DEC
+        return cudaGetLastError();
     }
+    unsigned int *amax = &p.scratch->x_amax;   // batch amax of x (W4A4 quantiser, f16 range of W4A16)
+    dim3 gt((E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
+    k_router_tiled<<<gt, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int k = p.cfg.top_k;
-    const int npl = (E + 31) / 32;
     dim3 g((T + 3) / 4);
 #define MOE_TOPK(N) k_router_topk<N><<<g, 128, 0, st>>>(p.logits, T, E, k, p.cfg.router, p.cfg.renormalize, ids, wts, p.counts, p.err)
     if (npl <= 1) MOE_TOPK(1);
@@ -494,11 +519,20 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     return cudaGetLastError();
 }
 
+// Kernels launch_router issues for T tokens (hidden is always a multiple of 256).
+int router_launches(int T) { return T <= kDecodeRouterThreads / 32 ? 1 : 2; }
+
 size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (size_t)E + 8); }
 
 cudaError_t configure_group_kernel(int E) {
     cudaError_t e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
     if (e != cudaSuccess) return e;
+    const int dec = (int)decode_router_smem(8192, kDecodeRouterThreads / 32);
+    for (auto f : {k_router_decode<1>, k_router_decode<2>, k_router_decode<4>, k_router_decode<8>,
+                   k_router_decode<16>, k_router_decode<32>}) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
+        if (e != cudaSuccess) return e;
+    }
     return cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(E));
 }
 
@@ -508,7 +542,7 @@ cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offs
     size_t smem = group_smem_bytes(E);
     k_group<<<1, 1024, smem, st>>>(ids, T * k, E, T, k, p.cfg.has_shared, p.counts, p.offsets, p.poff, p.sorted,
                                    p.inv, p.pad_pair, p.chunks, p.tiles, p.scratch, offsets_out, sorted_out,
-                                   build_work ? 1 : 0, (int)p.rows_pad_max, p.err);
+                                   build_work ? 1 : 0, (int)p.rows_pad_max, p.tile_rows, p.err);
     return cudaGetLastError();
 }
 

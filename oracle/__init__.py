@@ -190,6 +190,65 @@ def dequantize(codes, scales, ts) -> np.ndarray:
     return e2m1_table()[q] * s * float(ts)
 
 
+# Decisions of the quantiser that lie this close to their rounding boundary
+# (relative to the E4M3 argument for a scale, to the block's largest |x/den|
+# for a code) are the ones a different fp32 summation order of the quantised
+# value can flip: 2^-16 is 16 times the fp32 error of the GEMM sums that feed
+# the W4A4 SwiGLU quantiser.
+FLIP_MARGIN = 2.0 ** -16
+_E2M1_MIDS = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0])
+_E2M1_STEP = np.array([0.5, 0.5, 0.5, 0.5, 1.0, 1.0, 2.0])   # gap between the two codes around each midpoint
+
+
+def quant_decisions(x, ts: float, margin: float = FLIP_MARGIN):
+    """NVFP4-quantise fp32 rows x with tensor scale ts (the c-4 rule) and bound
+    what the near-boundary decisions could change.
+
+    Returns (deq, flip, n): deq = the dequantised values (FP64); flip = per
+    element, |change| of the dequantised value if every decision within
+    `margin` of its boundary went the other way (a block scale: the block
+    re-quantised with the neighbouring E4M3 scale; a code: the neighbouring
+    E2M1 value); n = the number of such decisions.  This is the band that the
+    "f64 oracle with a band for sums whose order is the hardware's" of
+    "bloomery 0.3.9" (New) calls for, applied where that order decides an
+    integer."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    R, C = x.shape
+    codes, scales, ts = quantize(x, ts)
+    deq = dequantize(codes, scales, ts)
+    flip = np.zeros((R, C), np.float64)
+    if R == 0:
+        return deq, flip, 0
+    ts32 = np.float32(ts)
+    xb = x.reshape(R, C // 16, 16)
+    bamax = np.abs(xb).max(axis=2)
+    q = (bamax / np.float32(6.0)).astype(np.float32) / ts32 if ts32 > 0 else np.zeros_like(bamax)
+    pos = np.unique(e4m3_table()[:127])            # finite E4M3 values >= 0, ascending
+    mids = (pos[1:] + pos[:-1]) / 2
+    qd = q.astype(np.float64)
+    j = np.clip(np.searchsorted(mids, qd), 1, len(mids) - 1)
+    near = np.where(np.abs(qd - mids[j - 1]) <= np.abs(qd - mids[j]), j - 1, j)   # nearest midpoint
+    s_nom = e4m3_table()[scales.astype(np.int64)]
+    s_alt = np.where(s_nom == pos[near], pos[near + 1], pos[near])
+    den = (s_nom.astype(np.float32) * ts32).astype(np.float32)
+    live = den > 0
+    scale_flag = live & (np.abs(qd - mids[near]) < margin * qd)
+    # codes: |x/den| near an E2M1 midpoint, relative to the block's largest |x/den|
+    with np.errstate(divide="ignore", invalid="ignore"):
+        v = np.abs(xb / np.where(live, den, np.float32(1))[..., None]).astype(np.float64)
+    dist = np.abs(v[..., None] - _E2M1_MIDS)
+    m = dist.argmin(axis=-1)
+    vmax = v.max(axis=2, keepdims=True)
+    code_flag = live[..., None] & (dist.min(axis=-1) < margin * vmax)
+    fb = flip.reshape(R, C // 16, 16)
+    fb += np.where(code_flag, _E2M1_STEP[m] * (s_nom * float(ts))[..., None], 0.0)   # dequantised as dequantize() does
+    for r, b in zip(*np.nonzero(scale_flag)):
+        d_alt = np.float32(np.float32(s_alt[r, b]) * ts32)         # the quantiser's fp32 divisor
+        alt = e2m1_table()[e2m1_from_f32(xb[r, b] / d_alt)] * (s_alt[r, b] * float(ts))
+        fb[r, b] += np.abs(alt - deq[r, 16 * b:16 * b + 16])
+    return deq, flip, int(code_flag.sum() + scale_flag.sum())
+
+
 # ------------------------------------------------------------------ router
 
 def router_logits(x_bf16: np.ndarray, router_w: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
@@ -286,21 +345,26 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         return bf16_to_f64(f64_to_bf16(h))
 
     def quant_h(h_all):
-        """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax."""
+        """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax.
+        Also returns, per matrix, the flip band of its near-boundary decisions."""
         h32 = [h.astype(np.float32) for h in h_all]
         amax = max((float(np.max(np.abs(h))) for h in h32 if h.size), default=0.0)
         ts = float(np.float32(np.float32(amax) / np.float32(2688.0)))
-        return [dequantize(*quantize(h, ts)[:2], ts) if h.size else h.astype(np.float64)
-                for h in h32], ts
+        qs = [quant_decisions(h, ts) for h in h32]
+        return [q[0] for q in qs], ts, [q[1] for q in qs], sum(q[2] for q in qs)
 
     active = [e for e in range(E) if offsets[e + 1] > offsets[e]]
     hs = {}
     for e in active:
         pr = rows[offsets[e]:offsets[e + 1]]
         hs[e] = up_part(expert(e), xin[pr // k])
+    band = np.zeros((T, H), np.float64)    # W4A4: what near-boundary h decisions could move
+    flips = {}
+    n_flip = 0
     if mode == MODE_W4A4:
-        qh, ts_h = quant_h([hs[e] for e in active])
+        qh, ts_h, fl, n_flip = quant_h([hs[e] for e in active])
         hs = dict(zip(active, qh))
+        flips = dict(zip(active, fl))
         res["h_ts"] = ts_h
     else:
         hs = {e: round_h_bf16(h) for e, h in hs.items()}
@@ -310,27 +374,43 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         pr = rows[offsets[e]:offsets[e + 1]]
         y = down_part(expert(e), hs[e])
         np.add.at(out, pr // k, wflat[pr][:, None] * y)
+        if e in flips and flips[e].any():
+            _, _, (dc, ds, dts) = expert(e)
+            np.add.at(band, pr // k, np.abs(wflat[pr])[:, None] * (flips[e] @ np.abs(dequantize(dc, ds, dts)).T))
 
     if shared is not None:
         hsh = up_part(shared, xin)
         if mode == MODE_W4A4:
-            (hsh,), ts_s = quant_h([hsh])
+            (hsh,), ts_s, (fs,), ns = quant_h([hsh])
+            n_flip += ns
             res["shared_h_ts"] = ts_s
+            if fs.any():
+                _, _, (dc, ds, dts) = shared
+                band += fs @ np.abs(dequantize(dc, ds, dts)).T
         else:
             hsh = round_h_bf16(hsh)
         out += down_part(shared, hsh)
 
     res["out"] = out
+    res["band"] = band
+    res["h_flips"] = n_flip
     res["out_bf16"] = f64_to_bf16(out)
     return res
 
 
-def compare_output(got_bf16: np.ndarray, ref_f64: np.ndarray):
-    """Output tolerance: max|d| <= 2e-2 * RMS(ref) and ||d||_2 / ||ref||_2 <= 5e-3."""
+def compare_output(got_bf16: np.ndarray, ref_f64: np.ndarray, band: np.ndarray | None = None):
+    """Output tolerance: |d| <= 2e-2 * RMS(ref) (+ band) element-wise and
+    ||d||_2 / ||ref||_2 <= 5e-3.  `band` (W4A4) is forward()'s bound on what
+    the SwiGLU quantiser's near-boundary decisions can move; it is zero where
+    no such decision touches an output."""
     got = bf16_to_f64(got_bf16)
-    d = got - ref_f64
+    d = np.abs(got - ref_f64)
     rms = float(np.sqrt(np.mean(ref_f64 ** 2)))
-    max_abs = float(np.max(np.abs(d)))
+    max_abs = float(np.max(d)) if d.size else 0.0
     rel_l2 = float(np.linalg.norm(d) / max(np.linalg.norm(ref_f64), 1e-300))
-    ok = (max_abs <= 2e-2 * rms) and (rel_l2 <= 5e-3) and bool(np.all(np.isfinite(got)))
-    return ok, dict(max_abs=max_abs, rms=rms, max_abs_over_rms=max_abs / max(rms, 1e-300), rel_l2=rel_l2)
+    lim = 2e-2 * rms + (0.0 if band is None else band)
+    beyond = d > lim
+    ok = (not bool(beyond.any())) and (rel_l2 <= 5e-3) and bool(np.all(np.isfinite(got)))
+    excess = d - 2e-2 * rms
+    return ok, dict(max_abs=max_abs, rms=rms, max_abs_over_rms=max_abs / max(rms, 1e-300), rel_l2=rel_l2,
+                    inside_band_only=int(((excess > 0) & ~beyond).sum()), beyond=int(beyond.sum()))

@@ -19,7 +19,8 @@ def _parity(case: Case, plan=None):
     out, st, plan = case.gpu_forward(plan)
     assert st == moe.OK, moe.STATUS[st]
     ref = case.oracle_forward()
-    ok, stats = oracle.compare_output(bf16_bits(out), ref["out"])
+    ok, stats = oracle.compare_output(bf16_bits(out), ref["out"], ref["band"])
+    stats["h_flips"] = ref["h_flips"]
     assert ok, stats
     return out, ref, stats
 
@@ -132,6 +133,22 @@ def test_every_token_on_one_expert():
     assert ref["offsets"][5] == 0 and ref["offsets"][6] == 40
 
 
+@pytest.mark.parametrize("mode,T", [("w4a16", 64), ("w4a16", 65), ("w4a16", 129), ("w4a4", 128), ("w4a4", 129)])
+def test_tile_boundaries_on_tensor_cores(mode, T):
+    # every token on experts 2 and 6: each holds T rows, cut into 64-row
+    # (W4A16) or 128-row (W4A4) tiles with a ragged last one
+    base = synth.WORKLOADS["tiny_w4a16"] if mode == "w4a16" else synth.WORKLOADS["verify16_w4a4"]
+    w = synth.scaled(base, tokens=T, hidden=512, experts=8, top_k=2, inter=256, shared_inter=256)
+    case = Case(w, T)
+    case.bias = torch.full((w.experts,), -30.0, device="cuda")
+    case.bias[2] = 30.0
+    case.bias[6] = 29.0
+    plan = plan_for(w)
+    plan.set_path(moe.PATH_TENSOR_CORE)
+    _, ref, _ = _parity(case, plan)
+    assert ref["offsets"][3] - ref["offsets"][2] == T and ref["offsets"][7] - ref["offsets"][6] == T
+
+
 def test_k_equals_e():
     w = synth.scaled(synth.WORKLOADS["tiny_w4a16"], top_k=8)
     _parity(Case(w, 5))
@@ -158,7 +175,7 @@ def test_forward_host_matches_device_path():
     plan.forward_host(xh, case.rw, case.bias, case.routed, case.shared, oh)
     assert plan.sync_status() == moe.OK
     ref = case.oracle_forward()
-    ok, stats = oracle.compare_output(bf16_bits(oh), ref["out"])
+    ok, stats = oracle.compare_output(bf16_bits(oh), ref["out"], ref["band"])
     assert ok, stats
 
 
@@ -199,5 +216,6 @@ def test_forward_replays_from_a_cuda_graph(name):
     for _ in range(2):
         g.replay()
     assert plan.sync_status() == moe.OK
-    ok, stats = oracle.compare_output(bf16_bits(out), case.oracle_forward()["out"])
+    ref = case.oracle_forward()
+    ok, stats = oracle.compare_output(bf16_bits(out), ref["out"], ref["band"])
     assert ok, stats

@@ -54,14 +54,15 @@ def test_route_ties_go_to_the_lower_expert():
                 assert pos[lo] < pos[hi]
 
 
+@pytest.mark.parametrize("T", [5, 20])   # the decode-sized (fused top-k) and the tiled router
 @pytest.mark.parametrize("kind,renorm", [("softmax", False), ("sigmoid", False), ("sigmoid", True)])
-def test_route_normalisation_policies(kind, renorm):
-    w = synth.scaled(synth.WORKLOADS["decode4_w4a16"], tokens=20, router=kind, renormalize=renorm)
+def test_route_normalisation_policies(kind, renorm, T):
+    w = synth.scaled(synth.WORKLOADS["decode4_w4a16"], tokens=T, router=kind, renormalize=renorm)
     _check(w, synth.activations(w, 2, device="cuda"), synth.router_weight(w, 2, "cuda"), None)
 
 
 def test_route_k_equals_e_and_single_expert():
-    for E, k in ((8, 8), (1, 1)):
+    for E, k in ((8, 8), (1, 1), (1024, 32)):
         w = synth.scaled(synth.WORKLOADS["tiny_w4a16"], experts=E, top_k=k)
         _check(w, synth.activations(w, 3, device="cuda"), synth.router_weight(w, 3, "cuda"), None)
 

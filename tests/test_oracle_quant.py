@@ -68,3 +68,57 @@ def test_quantiser_is_idempotent_on_its_grid():
     q2 = oracle.unpack_codes(c2).reshape(8, -1, 16)
     assert same_scale.mean() > 0.9
     assert np.array_equal(q1[same_scale], q2[same_scale])
+
+
+# ---- the W4A4 flip band (near-boundary quantiser decisions)
+
+def test_flip_band_is_empty_far_from_boundaries():
+    # every value exactly on an E2M1 point of a power-of-two scale; the scale
+    # argument (bamax/6)/ts = 2 is itself an E4M3 value
+    ts = 1.0
+    x = np.array([[6.0, -4.0, 3.0, 2.0, 1.5, 1.0, 0.5, 0.0, -6.0, 4.0, -3.0, 2.0, -1.5, 1.0, -0.5, 0.0]]) * 2.0
+    deq, flip, n = oracle.quant_decisions(x.astype(np.float32), ts)
+    assert n == 0 and not flip.any()
+    np.testing.assert_array_equal(deq, x)
+
+
+def test_flip_band_of_a_code_on_a_midpoint():
+    # scale 2 (as above); one value at 2.5 * den, halfway between codes 2 and 3
+    x = np.array([[12.0] + [1.0] * 14 + [5.0]], np.float32)    # 5.0 / 2 = 2.5
+    deq, flip, n = oracle.quant_decisions(x, 1.0)
+    assert n == 1
+    assert deq[0, 15] == 4.0                  # RNE: 2.5 -> 2 (even), times den 2
+    np.testing.assert_array_equal(flip[0, :15], 0.0)
+    assert flip[0, 15] == 2.0                 # the other side: code 3, one step (1.0) x den 2
+
+
+def test_flip_band_of_a_scale_on_a_midpoint():
+    # (bamax/6)/ts = 12.75/6 = 2.125, halfway between E4M3 2.0 and 2.25: RNE
+    # keeps 2.0; the band is the block re-quantised with 2.25
+    x = np.array([[12.75, 3.0, -1.0, 7.0] + [0.0] * 12], np.float32)
+    deq, flip, n = oracle.quant_decisions(x, 1.0)
+    assert n >= 1
+    nom = oracle.dequantize(*oracle.quantize(x, 1.0)[:2], 1.0)
+    np.testing.assert_array_equal(deq, nom)
+    alt = oracle.e2m1_table()[oracle.e2m1_from_f32(x / np.float32(2.25))] * 2.25
+    assert np.all(flip[0] >= np.abs(alt - nom[0]) - 1e-12)
+    assert np.any(flip[0] > 0)                # the elements that move carry the band
+
+
+def test_flip_band_covers_every_flip_of_small_perturbations():
+    rng = np.random.default_rng(21)
+    x = (rng.standard_normal((256, 1024)) * rng.uniform(0.01, 3.0, (256, 1))).astype(np.float32)
+    ts = float(np.float32(oracle.tensor_scale(x) * 1.37))
+    deq, flip, n = oracle.quant_decisions(x, ts)
+    moved = np.zeros_like(deq)
+    # perturbations 4x inside the band's margin (2^-16)
+    for dx, dts in ((2.0 ** -18, 0.0), (-2.0 ** -18, 0.0), (0.0, 2.0 ** -18), (0.0, -2.0 ** -18)):
+        x2 = (x.astype(np.float64) * (1 + dx)).astype(np.float32)
+        t2 = float(np.float32(ts * (1 + dts)))
+        d2 = oracle.dequantize(*oracle.quantize(x2, t2)[:2], t2)
+        # compare at the nominal scale: changes of the decisions, not of ts itself
+        moved = np.maximum(moved, np.abs(d2 * (ts / t2) - deq))
+    changed = moved > 1e-6 * np.abs(deq).max()
+    assert changed.sum() >= 5, "the perturbations should flip a few decisions in 256K values"
+    assert np.all(flip[changed] >= moved[changed] * (1 - 1e-12))
+    assert n < 0.01 * x.size                 # few decisions sit that close to a boundary
