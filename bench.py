@@ -260,7 +260,7 @@ def run_ours(args, w, world, rank, local):
                     renormalize=w.renormalize, mode=moe.W4A4 if w.mode == "w4a4" else moe.W4A16,
                     has_shared=w.shared_inter > 0, shared_inter=w.shared_inter)
     plan.set_path({"auto": moe.PATH_AUTO, "cuda_core": moe.PATH_CUDA_CORE,
-                   "tensor_core": moe.PATH_TENSOR_CORE}[args.path])
+                   "tensor_core": moe.PATH_TENSOR_CORE, "warp_mma": moe.PATH_WARP_MMA}[args.path])
     ids_list = [plan.route(i.x, i.rw, i.bias)["topk_ids"].cpu().numpy() for i in insts]
     gu_bytes, dn_bytes, flops, distinct = algorithmic(w, ids_list)
     outs = [torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda") for _ in insts]
@@ -399,7 +399,7 @@ def main():
     ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core"],
+    ap.add_argument("--path", default="auto", choices=["auto", "cuda_core", "tensor_core", "warp_mma"],
                     help="expert-FFN implementation (moe_plan_set_path)")
     ap.add_argument("--override", default="",
                     help="comma-separated workload fields for a scaled-down profiling run, e.g. tokens=1024,experts=64")

@@ -178,15 +178,21 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream);
  * "counts", "padded_offsets".  Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 
-/* Expert-FFN implementation moe_forward uses: AUTO picks the tensor-core
- * grouped GEMMs (tcgen05) for W4A4 batches of 64 or more (token, expert)
- * pairs when the shapes allow (H, I multiples of 256) and the CUDA-core
- * weight-streaming kernels otherwise.  Both compute the same function. */
-typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_CUDA_CORE = 1, MOE_PATH_TENSOR_CORE = 2 } moe_path;
+/* Expert-FFN implementation moe_forward uses.  CUDA_CORE: weight-streaming
+ * kernels on the CUDA cores (any shape).  TENSOR_CORE: grouped GEMMs on the
+ * 5th-generation tensor cores (tcgen05; W4A4 block-scaled FP4, W4A16 with the
+ * weights widened to f16 in tensor memory).  WARP_MMA (W4A16 only): the
+ * weights widened in registers straight into warp-level f16 MMAs, for tiles
+ * of up to 32 token rows.  AUTO picks WARP_MMA for W4A16, the tcgen05 GEMMs
+ * for W4A4 batches of 64 or more (token, expert) pairs, and CUDA_CORE
+ * otherwise; the tensor paths need H and I multiples of 256.  All compute the
+ * same function (the tolerance of the parity tests covers their different
+ * summation orders). */
+typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_CUDA_CORE = 1, MOE_PATH_TENSOR_CORE = 2, MOE_PATH_WARP_MMA = 3 } moe_path;
 
 /* Select the expert-FFN implementation for later calls on this plan.
- * MOE_ERR_UNSUPPORTED_SHAPE if MOE_PATH_TENSOR_CORE is asked for a plan whose
- * mode or shapes it does not cover. */
+ * MOE_ERR_UNSUPPORTED_SHAPE if MOE_PATH_TENSOR_CORE or MOE_PATH_WARP_MMA is
+ * asked for a plan whose mode or shapes it does not cover. */
 moe_status moe_plan_set_path(moe_plan plan, int32_t path);
 
 /* Stages of moe_forward, for moe_plan_read_profile. */

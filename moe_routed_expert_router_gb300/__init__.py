@@ -29,7 +29,7 @@ EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_route", "moe_forward", "m
            "moe_quantize_act", "moe_quantize_nvfp4", "moe_plan_sync_status", "moe_plan_debug_buffer",
            "moe_plan_set_profiling", "moe_plan_read_profile", "moe_plan_set_path", "moe_plan_check_timeout",
            "moe_route_static", "moe_status_string", "moe_version"]
-PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_WARP_MMA = 0, 1, 2, 3
 STAGES = ["route", "group", "quant_x", "permute", "gate_up", "quant_h", "down", "finalize"]
 
 

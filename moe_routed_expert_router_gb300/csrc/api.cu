@@ -15,8 +15,9 @@ cudaError_t configure_group_kernel(int E);
 cudaError_t configure_tc(const Plan &p);
 cudaError_t configure_simt();
 bool tc_supported(const Plan &p);
+bool warp_mma_supported(const Plan &p);
 cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs &routed, const ExpertPtrs *shared,
-                          int part, cudaStream_t st);
+                          int part, cudaStream_t st, bool warp_mma);
 }  // namespace moe
 
 using moe::Plan;
@@ -180,11 +181,17 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     moe::ExpertPtrs r = ptrs(*routed), sh{};
     if (shared) sh = ptrs(*shared);
     const moe::ExpertPtrs *shp = shared ? &sh : nullptr;
-    const bool tc = plan->path == MOE_PATH_TENSOR_CORE ||
-                    (plan->path == MOE_PATH_AUTO && moe::tc_supported(p) && T * p.cfg.top_k >= 64);
+    // engine: CUDA-core streaming kernels, tcgen05 grouped GEMMs, or (W4A16)
+    // warp-level MMAs fed from registers
+    bool wm = plan->path == MOE_PATH_WARP_MMA;
+    bool tc = wm || plan->path == MOE_PATH_TENSOR_CORE;
+    if (plan->path == MOE_PATH_AUTO) {
+        wm = moe::warp_mma_supported(p);
+        tc = wm || (moe::tc_supported(p) && T * p.cfg.top_k >= 64);
+    }
     {
         Stage s(plan, MOE_STAGE_GATE_UP, st);
-        e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
+        e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st, wm) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
         if (s.done(e, tc ? 2 : 1) != cudaSuccess) return MOE_ERR_CUDA;
     }
     if (p.cfg.mode == MOE_W4A4) {
@@ -193,7 +200,7 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     }
     {
         Stage s(plan, MOE_STAGE_DOWN, st);
-        e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 1, st) : moe::launch_ffn_simt(p, x, T, r, shp, 1, st);
+        e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 1, st, wm) : moe::launch_ffn_simt(p, x, T, r, shp, 1, st);
         if (s.done(e, 1) != cudaSuccess) return MOE_ERR_CUDA;
     }
     Stage s(plan, MOE_STAGE_FINALIZE, st);
@@ -241,7 +248,7 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
                      (cfg->has_shared ? (T + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows : 0);
     p.rows_pad_max = (p.rows_pad_max + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows;
     p.chunks_max = p.pairs_max / moe::kChunkRows + E + 2 + (cfg->has_shared ? T / moe::kChunkRows + 1 : 0);
-    p.tile_rows = cfg->mode == MOE_W4A16 ? 64 : moe::kTileRows;
+    p.tile_rows = cfg->mode == MOE_W4A16 ? 32 : moe::kTileRows;
     p.tiles_max = p.pairs_max / p.tile_rows + E + 2 + (cfg->has_shared ? T / p.tile_rows + 1 : 0);
     Carver dry;
     carve(p, dry);
@@ -269,8 +276,9 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
 }
 
 moe_status moe_plan_set_path(moe_plan plan, int32_t path) {
-    if (!plan || path < MOE_PATH_AUTO || path > MOE_PATH_TENSOR_CORE) return MOE_ERR_INVALID_ARG;
+    if (!plan || path < MOE_PATH_AUTO || path > MOE_PATH_WARP_MMA) return MOE_ERR_INVALID_ARG;
     if (path == MOE_PATH_TENSOR_CORE && !moe::tc_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (path == MOE_PATH_WARP_MMA && !moe::warp_mma_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     plan->path = path;
     return MOE_OK;
 }

@@ -410,8 +410,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
 // rows, so its bandwidth no longer bounds the weight stream.
 //   code ring  (4 x 36 KB, shared): NVFP4 codes of both A operands (128-byte
 //              swizzle) + their plain scale tiles, 256 K values a stage;
-//   B ring     (6 x 8 KB, shared): f16 token rows (up to 64), 64 K values a
-//              stage, 128-byte swizzle;
+//   B ring     (4 x 16 KB, shared): f16 token rows, 128-byte swizzle, in
+//              boxes of 64 K values; a stage holds 512, 256 or 128 K values
+//              for tiles of up to 16, 32 or 64 rows (MMA N = 16, 32, 64);
 //   A ring     (4 x 64 TMEM columns): both operands widened to f16, 64 K
 //              values a stage (row r in lane r, two K values a column);
 //   accumulators (2 x 128 TMEM columns): gate / up (or the two down-row
@@ -431,8 +432,8 @@ constexpr int kHCodeStage = 2 * kHCodeTile + 2 * 2048;   // A0, A1 codes + A0, A
 constexpr int kHCStages = 4;
 constexpr int kHBK = 64;                         // K values per MMA step
 constexpr int kHBRows = 64;                      // token rows per tile (MMA N <= 64)
-constexpr int kHBTile = kHBRows * 128;           // 8 KB: 64 rows x 64 f16
-constexpr int kHBStages = 6;
+constexpr int kHBTile = 16384;                   // B stage: 16 KB of f16 token rows
+constexpr int kHBStages = 4;
 constexpr int kHAStages = 4;                     // TMEM A ring
 constexpr uint32_t kHACol0 = 256;                // first TMEM column of the A ring
 constexpr int kConvSplit = 2;                    // converter warps per (operand, 32-lane quarter)
@@ -449,7 +450,7 @@ static_assert(kHACol0 + kHAStages * 64 <= 512, "W4A16 TMEM plan exceeds 512 colu
 struct HcArgs {
     CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 128 B x 128 rows, 128-byte swizzle
     CUtensorMap s0[2], s1[2];   // scales [rows][K/16], box 16 B x 128 rows
-    CUtensorMap b[2];           // f16 token rows [rows_pad][Kdim], box 64 x (32/64), 128-byte swizzle
+    CUtensorMap b[3];           // f16 token rows [rows_pad][Kdim], box 64 x (16/32/64), 128-byte swizzle
     const int4 *tiles;
     const CallScratch *scratch;
     int E, H, I, Is, nf;
@@ -490,6 +491,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
           "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
+
+// Token-row class of a tile: 0, 1, 2 for up to 16, 32, 64 rows; the MMA N is
+// 16 << class and a B stage holds (8 >> class) boxes of 64 K values.
+__device__ __forceinline__ int hrows_class(int valid) { return valid <= 16 ? 0 : (valid <= 32 ? 1 : 2); }
 
 // Item = tile * nf + f: the tile's token rows against weight-row group f.
 // Returns false for a group past the expert's intermediate size.
@@ -600,12 +605,15 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item_h(a, item, EPI, it)) continue;
-                const int rc = it.valid <= 32 ? 0 : 1;
-                const uint32_t bytes = (32u << rc) * 128u;
-                for (int q = 0; q < it.K / kHBK; ++q) {
+                const int rc = hrows_class(it.valid);
+                const int rows = 16 << rc, boxes = 8 >> rc, nq = it.K / kHBK;
+                for (int q0 = 0; q0 < nq; q0 += boxes) {
+                    const int nb = min(boxes, nq - q0);   // the item's last stage may hold fewer boxes
                     if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
-                    mbar_expect_tx(bfull + b.s, bytes);
-                    tma_2d(b_ring + b.s * kHBTile, &a.b[rc], bfull + b.s, q * kHBK, it.row0);
+                    mbar_expect_tx(bfull + b.s, (uint32_t)(nb * rows * 128));
+                    for (int bx = 0; bx < nb; ++bx)
+                        tma_2d(b_ring + b.s * kHBTile + bx * rows * 128, &a.b[rc], bfull + b.s,
+                               (q0 + bx) * kHBK, it.row0);
                     used |= 1u << b.s;
                     last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
                     b.next(kHBStages);
@@ -688,15 +696,18 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 aph ^= 1u << buf;
                 tc_fence_after();
                 const uint32_t d0 = tmem + buf * 128, d1 = d0 + 64;
-                const uint32_t idesc = idesc_f16(it.valid <= 32 ? 32u : 64u);
-                for (int qq = 0; qq < it.K / kHBK; ++qq) {
-                    if (!mbar_wait(afull + as.s, as.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) {
+                const int rc = hrows_class(it.valid);
+                const int rows = 16 << rc, boxes = 8 >> rc, nq = it.K / kHBK;
+                const uint32_t idesc = idesc_f16((uint32_t)rows);
+                for (int qq = 0; qq < nq; ++qq) {
+                    const int bx = qq % boxes;
+                    if (!mbar_wait(afull + as.s, as.ph, a.err) || (bx == 0 && !mbar_wait(bfull + bs.s, bs.ph, a.err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     const uint32_t at = tmem + kHACol0 + as.s * 64;
-                    const uint32_t bt = smem_u32(b_ring + bs.s * kHBTile);
+                    const uint32_t bt = smem_u32(b_ring + bs.s * kHBTile) + bx * rows * 128;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (qq | kk) ? 1u : 0u;
@@ -705,9 +716,11 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                         mma_f16_ts(d1, at + 32 + 8 * kk, bd, idesc, accum);
                     }
                     mma_commit(aempty + as.s);
-                    mma_commit(bempty + bs.s);
                     as.next(kHAStages);
-                    bs.next(kHBStages);
+                    if (bx == boxes - 1 || qq == nq - 1) {
+                        mma_commit(bempty + bs.s);
+                        bs.next(kHBStages);
+                    }
                 }
                 if (!ok) break;
                 mma_commit(acc_full + buf);
@@ -800,6 +813,261 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
     }
+}
+
+// ------------------------------------------------------------------ W4A16, register path
+// W4A16 for tiles of up to 32 token rows (decode and short prompts): E2M1
+// codes are widened in registers straight into the A fragments of warp-level
+// f16 MMAs (m16n8k16, fp32 accumulation), so no widened copy of the weights
+// is ever stored.  The weight codes and scales arrive through the same TMA
+// code ring as the tcgen05 kernel (4 x 36 KB, 128 weight rows of two operands,
+// 256 K values a stage); the f16 token rows through a 3-stage ring (256 K
+// values a stage).  Sixteen compute warps: warp (row group rg, operand op)
+// owns 16 rows of one operand and all K.
+//
+// K order inside a 64-value super-block: lane quad q (lane & 3) holds the 16
+// consecutive K values 16q .. 16q+15, i.e. exactly one scale block, so each
+// lane scales its codes with one E4M3 value a row; MMA m (0..3) takes K values
+// 16q + 4m + {0,1} as fragment columns 2q, 2q+1 and 16q + 4m + {2,3} as 2q+8,
+// 2q+9.  The token-row fragments use the same map, so the sum is the same dot
+// product in another order.
+constexpr int kRThreads = 32 * (1 + 16);
+constexpr int kRBStages = 3;
+constexpr int kRBTile = 32 * 512;                 // 16 KB: up to 32 token rows x 256 K f16
+constexpr int kRXchg = 8 * 4 * 32 * 4 * 4;        // 16 KB: up-operand accumulators handed to the gate warps
+constexpr size_t kRSmemBytes = (size_t)kHCStages * kHCodeStage + (size_t)kRBStages * kRBTile + kRXchg + 512 + 1024;
+static_assert(kRSmemBytes <= 227 * 1024, "register-path pipeline exceeds shared memory");
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int NT>
+__device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int rg, int lane, float (&acc)[4][4]) {
+    const int g = lane >> 2, q = lane & 3;
+    const int r0 = rg * 16 + g, r1 = r0 + 8;
+    const uint32_t crow0 = st + op * kHCodeTile + r0 * 128, crow1 = st + op * kHCodeTile + r1 * 128;
+    const uint4 sv0 = lds128(st + 2 * kHCodeTile + op * 2048 + r0 * 16);
+    const uint4 sv1 = lds128(st + 2 * kHCodeTile + op * 2048 + r1 * 16);
+    const uint32_t sw0[4] = {sv0.x, sv0.y, sv0.z, sv0.w}, sw1[4] = {sv1.x, sv1.y, sv1.z, sv1.w};
+#pragma unroll
+    for (int sb = 0; sb < 4; ++sb) {
+        const uint32_t ch = (uint32_t)(2 * sb + (q >> 1));
+        uint2 c0, c1;
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c0.x), "=r"(c0.y) : "r"(crow0 + ((ch ^ (uint32_t)(r0 & 7)) << 4) + (q & 1) * 8) : "memory");
+        asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c1.x), "=r"(c1.y) : "r"(crow1 + ((ch ^ (uint32_t)(r1 & 7)) << 4) + (q & 1) * 8) : "memory");
+        // scale bytes of block 4 sb + q for rows r0 (low) and r1 (high)
+        const uint32_t s2 = ((sw0[sb] >> (8 * q)) & 0xFFu) | (((sw1[sb] >> (8 * q)) & 0xFFu) << 8);
+        const uint32_t sc = e4m3x2_to_f16x2(s2);
+        __half2 sc0 = __low2half2(*reinterpret_cast<const __half2 *>(&sc));
+        __half2 sc1 = __high2half2(*reinterpret_cast<const __half2 *>(&sc));
+        uint32_t h0[8], h1[8];
+        e2m1x8_to_f16x8(c0.x, *reinterpret_cast<uint32_t(*)[4]>(h0));
+        e2m1x8_to_f16x8(c0.y, *reinterpret_cast<uint32_t(*)[4]>(h0 + 4));
+        e2m1x8_to_f16x8(c1.x, *reinterpret_cast<uint32_t(*)[4]>(h1));
+        e2m1x8_to_f16x8(c1.y, *reinterpret_cast<uint32_t(*)[4]>(h1 + 4));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            __half2 v0 = __hmul2(*reinterpret_cast<const __half2 *>(&h0[i]), sc0);
+            __half2 v1 = __hmul2(*reinterpret_cast<const __half2 *>(&h1[i]), sc1);
+            h0[i] = *reinterpret_cast<uint32_t *>(&v0);
+            h1[i] = *reinterpret_cast<uint32_t *>(&v1);
+        }
+        // token-row fragments: row n = 8 nt + g, K values 64 sb + 16 q .. +16 (box sb of the stage)
+        uint4 bx[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = nt * 8 + g;
+            const uint32_t brow = bst + (uint32_t)sb * (NT > 2 ? 32 : 16) * 128 + n * 128;
+            bx[nt][0] = lds128(brow + (((uint32_t)(2 * q) ^ (uint32_t)(n & 7)) << 4));
+            bx[nt][1] = lds128(brow + (((uint32_t)(2 * q + 1) ^ (uint32_t)(n & 7)) << 4));
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const uint32_t a[4] = {h0[2 * m], h1[2 * m], h0[2 * m + 1], h1[2 * m + 1]};
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint4 &b = bx[nt][m >> 1];
+                mma16816(acc[nt], a, (m & 1) ? b.z : b.x, (m & 1) ? b.w : b.y);
+            }
+        }
+    }
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *code_ring = smem;
+    uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
+    float *xchg = reinterpret_cast<float *>(b_ring + kRBStages * kRBTile);
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
+    uint64_t *cempty = cfull + kHCStages;
+    uint64_t *bfull = cempty + kHCStages;
+    uint64_t *bempty = bfull + kRBStages;
+    uint64_t *xfull = bempty + kRBStages;        // [8] up accumulators written (SwiGLU)
+    uint64_t *xempty = xfull + 8;                // [8] and read
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = a.scratch->n_tiles * a.nf;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
+        for (int i = 0; i < kRBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
+        for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------- producer of the code ring
+            RingPos c;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int m = it.sh ? 1 : 0;
+                int r0, r1;
+                h_rows(a, it, EPI, r0, r1);
+                const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
+                const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
+                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                    if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
+                    uint8_t *st = code_ring + c.s * kHCodeStage;
+                    mbar_expect_tx(cfull + c.s, kHCodeStage);
+                    tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
+                    tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
+                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, kc * 16, r0);
+                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
+                    used |= 1u << c.s;
+                    last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
+                    c.next(kHCStages);
+                }
+            }
+            for (int t = 0; t < kHCStages; ++t)
+                if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
+        } else if (lane == 1) {
+            // ---------------------------------------- producer of the token-row ring
+            RingPos b;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int rc = it.valid <= 16 ? 0 : 1;
+                const int rows = 16 << rc;
+                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                    if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
+                    mbar_expect_tx(bfull + b.s, (uint32_t)(4 * rows * 128));
+                    for (int bx = 0; bx < 4; ++bx)
+                        tma_2d(b_ring + b.s * kRBTile + bx * rows * 128, &a.b[rc], bfull + b.s, kc * kHCK + bx * 64,
+                               it.row0);
+                    used |= 1u << b.s;
+                    last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
+                    b.next(kRBStages);
+                }
+            }
+            for (int t = 0; t < kRBStages; ++t)
+                if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------- compute warps
+    const int cw = warp - 1, rg = cw & 7, op = cw >> 3;
+    const int g = lane >> 2, q = lane & 3;
+    const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
+    const int xs = f16_shift(a.scratch->x_amax);
+    const float xunscale = __uint_as_float((uint32_t)(127 + xs) << 23);   // 2^s
+    RingPos cs, bs;
+    uint32_t xph = 0;
+    bool ok = true, range_bad = false;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        Item it;
+        if (!decode_item_h(a, item, EPI, it)) continue;
+        const int nt_n = (it.valid + 7) >> 3;
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+        for (int kc = 0; kc < it.K / kHCK; ++kc) {
+            if (!mbar_wait(cfull + cs.s, cs.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) { ok = false; break; }
+            const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * kRBTile;
+            switch (nt_n) {
+                case 1: reg_stage<1>(st, bst, op, rg, lane, acc); break;
+                case 2: reg_stage<2>(st, bst, op, rg, lane, acc); break;
+                case 3: reg_stage<3>(st, bst, op, rg, lane, acc); break;
+                default: reg_stage<4>(st, bst, op, rg, lane, acc); break;
+            }
+            __syncwarp();
+            if (lane == 0) { mbar_arrive(cempty + cs.s); mbar_arrive(bempty + bs.s); }
+            cs.next(kHCStages);
+            bs.next(kRBStages);
+        }
+        if (!ok) break;
+        const int m = it.sh ? 1 : 0;
+        const int e = it.sh ? 0 : it.e;
+        if (EPI == kSwiGLU) {
+            float *slot = xchg + (size_t)rg * (4 * 32 * 4);
+            if (op == 1) {   // up warp: hand the accumulators to the gate warp of the same rows
+                if (!mbar_wait(xempty + rg, xph ^ 1, a.err)) { ok = false; break; }
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+                    if (nt < nt_n)
+                        *reinterpret_cast<float4 *>(slot + (nt * 32 + lane) * 4) =
+                            make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xfull + rg);
+            } else {
+                if (!mbar_wait(xfull + rg, xph, a.err)) { ok = false; break; }
+                const float sg = a.ts_a0[m][e] * xunscale, su = a.ts_a1[m][e] * xunscale;
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    if (nt >= nt_n) break;
+                    const float4 u4 = *reinterpret_cast<const float4 *>(slot + (nt * 32 + lane) * 4);
+                    const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int n = nt * 8 + 2 * q + (i & 1);
+                        const int feat = it.f * 128 + rg * 16 + g + (i >> 1) * 8;
+                        if (n < it.valid) {
+                            const float gv = acc[nt][i] * sg, uv = u[i] * su;
+                            // SwiGLU output rounded to bf16 (W4A16), held as f16 for the down product
+                            const float hb = __bfloat162float(__float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv));
+                            range_bad |= fabsf(hb) > 65504.0f;
+                            a.hout[(size_t)(it.row0 + n) * a.hstride + feat] = __float2half_rn(hb);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xempty + rg);
+            }
+            xph ^= 1;
+        } else {
+            const float ds = a.ts_a0[m][e];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                if (nt >= nt_n) break;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int n = nt * 8 + 2 * q + (i & 1);
+                    if (n < it.valid) {
+                        const int pair = a.pad_pair[it.row0 + n];
+                        const int t = pair >= a.P ? pair - a.P : pair / a.k;
+                        const float wv = (pair >= a.P ? 1.0f : a.wts[pair]) * ds;
+                        const int j = it.f * 256 + op * 128 + rg * 16 + g + (i >> 1) * 8;
+                        atomicAdd(a.acc + (size_t)t * a.H + j, acc[nt][i] * wv);
+                    }
+                }
+            }
+        }
+    }
+    if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(a.err, kErrDevice);
 }
 
 // x rows (bf16) -> padded per-expert f16 rows, times 2^-s (exact; s from the
@@ -915,14 +1183,24 @@ cudaError_t configure_tc(const Plan &) {
         e = cudaFuncSetAttribute(k_gemm_f16<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_gemm_f16<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_reg<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_reg<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
     return e;
+}
+
+// Shapes the register-path W4A16 kernels take: those of the tcgen05 kernels,
+// with tiles of at most 32 token rows.
+bool warp_mma_supported(const Plan &p) {
+    return p.cfg.mode == MOE_W4A16 && p.tile_rows <= 32 && tc_supported(p);
 }
 
 namespace {
 
 // W4A16 on the tensor cores (see k_gemm_f16).
 cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool warp_mma) {
     const moe_config &c = p.cfg;
     const int H = c.hidden, I = c.inter, E = c.num_experts;
     const int Is = c.has_shared ? c.shared_inter : 0;
@@ -958,15 +1236,18 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
         ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
-        for (int k2 = 0; k2 < 2; ++k2)
-            ok &= make_map(&a.b[k2], p.xp16, H, p.rows_pad_max, (uint64_t)H * 2, 64, 32u << k2, true, true);
+        for (int k2 = 0; k2 < 3; ++k2)
+            ok &= make_map(&a.b[k2], p.xp16, H, p.rows_pad_max, (uint64_t)H * 2, 64, 16u << k2, true, true);
         a.nf = Imax / 128;
         a.ts_a0[0] = r.gts;
         a.ts_a1[0] = r.uts;
         a.ts_a0[1] = sp.gts;
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
-        k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+        if (warp_mma)
+            k_gemm_reg<kSwiGLU><<<p.num_sms, kRThreads, kRSmemBytes, st>>>(a);
+        else
+            k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
         return cudaGetLastError();
     }
     ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
@@ -977,23 +1258,26 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.a1[1] = a.a0[1];
     a.s1[0] = a.s0[0];
     a.s1[1] = a.s0[1];
-    for (int k2 = 0; k2 < 2; ++k2)
-        ok &= make_map(&a.b[k2], p.hbuf, Imax, p.rows_pad_max, (uint64_t)Imax * 2, 64, 32u << k2, true, true);
+    for (int k2 = 0; k2 < 3; ++k2)
+        ok &= make_map(&a.b[k2], p.hbuf, Imax, p.rows_pad_max, (uint64_t)Imax * 2, 64, 16u << k2, true, true);
     a.nf = H / 256;
     a.ts_a0[0] = r.dts;
     a.ts_a0[1] = sp.dts;
     a.ts_a1[0] = r.dts;
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
-    k_gemm_f16<kScatter><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+    if (warp_mma)
+        k_gemm_reg<kScatter><<<p.num_sms, kRThreads, kRSmemBytes, st>>>(a);
+    else
+        k_gemm_f16<kScatter><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
-                          cudaStream_t st) {
-    if (p.cfg.mode == MOE_W4A16) return launch_ffn_tc_f16(p, x, T, r, s, part, st);
+                          cudaStream_t st, bool warp_mma) {
+    if (p.cfg.mode == MOE_W4A16) return launch_ffn_tc_f16(p, x, T, r, s, part, st, warp_mma);
     const moe_config &c = p.cfg;
     const int H = c.hidden, I = c.inter, E = c.num_experts;
     const int Is = c.has_shared ? c.shared_inter : 0;

@@ -228,11 +228,12 @@ __global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ l
 
 // Decode-sized batches (T <= 16), router and top-k in one launch: block e
 // computes expert e's logit for every token.  The router row (H fp32) is
-// staged in shared memory at once, x (all T rows) streams through a 4-deep
-// cp.async ring of 256-position slabs; warp t walks token t, lane l taking
-// positions 32j + l in increasing j.  Each block also checks a 1/E slice of x
-// (non-finite values, amax).  The last block to finish (a ticket in the
-// per-call scratch) runs the top-k for all tokens, one warp a token.
+// staged in shared memory once; warp t streams token t's x row through its own
+// 4-deep cp.async ring of 256-position slabs (one 16-byte copy a lane a slab,
+// no block barrier), lane l taking positions 32j + l in increasing j.  Each
+// block also checks a 1/E slice of x (non-finite values, amax).  The last
+// block to finish (a ticket in the per-call scratch) runs the top-k for all
+// tokens, one warp a token.
 constexpr int kDecodeRouterThreads = 512;
 constexpr int kDSlab = 256, kDStages = 4;
 
@@ -243,8 +244,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     const uint16_t *__restrict__ x, int T, int H, const float *__restrict__ rw, const float *__restrict__ bias,
     int E, int k, int kind, int renorm, float *__restrict__ logits, int32_t *__restrict__ ids,
     float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err) {
-    extern __shared__ __align__(16) float wrow[];     // [H], then x slabs [kDStages][T][kDSlab] bf16
-    uint16_t *xs = reinterpret_cast<uint16_t *>(wrow + H);
+    extern __shared__ __align__(16) float wrow[];     // [H], then per-token x rings [T][kDStages][kDSlab] bf16
     __shared__ float s_amax[kDecodeRouterThreads / 32];
     __shared__ int s_bad[kDecodeRouterThreads / 32];
     __shared__ int s_last;
@@ -252,18 +252,17 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     const int e = blockIdx.x;
     const int slabs = H / kDSlab;
     for (int c = tid; c < H / 4; c += kDecodeRouterThreads) cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
-    auto load_x = [&](int sl) {
-        if (sl < slabs) {
-            uint16_t *dst = xs + (size_t)(sl % kDStages) * T * kDSlab;
-            for (int idx = tid; idx < T * (kDSlab / 8); idx += kDecodeRouterThreads) {
-                const int r = idx / (kDSlab / 8), c = idx % (kDSlab / 8);
-                cp_async16(dst + r * kDSlab + c * 8, x + (size_t)r * H + sl * kDSlab + c * 8, true);
-            }
-        }
-        asm volatile("cp.async.commit_group;" ::: "memory");   // group 0 also carries the router row
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + H) + (size_t)warp * kDStages * kDSlab;
+    const uint16_t *xr = x + (size_t)warp * H;
+    auto load_x = [&](int sl) {   // warp-private: lane l copies positions 8l .. 8l+7 of the slab
+        if (sl < slabs) cp_async16(ring + (sl % kDStages) * kDSlab + 8 * lane, xr + sl * kDSlab + 8 * lane, true);
+        asm volatile("cp.async.commit_group;" ::: "memory");
     };
+    if (warp < T) {
 #pragma unroll
-    for (int sl = 0; sl < kDStages - 1; ++sl) load_x(sl);
+        for (int sl = 0; sl < kDStages - 1; ++sl) load_x(sl);
+    }
     {   // this block's slice of x: non-finite check and amax
         const int nchunks = T * H / 8;
         const int per = (nchunks + gridDim.x - 1) / gridDim.x;
@@ -283,21 +282,10 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         amax = warp_max(amax);
         if (lane == 0) { s_amax[warp] = amax; s_bad[warp] = bad; }
     }
-    float acc = 0.0f;
-    for (int sl = 0; sl < slabs; ++sl) {
-        load_x(sl + kDStages - 1);
-        asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
-        __syncthreads();
-        if (warp < T) {
-            const uint16_t *xr = xs + (size_t)(sl % kDStages) * T * kDSlab + warp * kDSlab;
-            const float *wr = wrow + sl * kDSlab;
-#pragma unroll
-            for (int j = 0; j < kDSlab / 32; ++j)
-                acc = fmaf(__uint_as_float((uint32_t)xr[32 * j + lane] << 16), wr[32 * j + lane], acc);
-        }
-        __syncthreads();
-    }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // the router row is the oldest commit group of every thread
+    if (warp < T) asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
     if (warp == 0) {
         float m = lane < kDecodeRouterThreads / 32 ? s_amax[lane] : 0.0f;
         int b = lane < kDecodeRouterThreads / 32 ? s_bad[lane] : 0;
@@ -309,6 +297,19 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         }
     }
     if (warp < T) {
+        float acc = 0.0f;
+        for (int sl = 0; sl < slabs; ++sl) {
+            load_x(sl + kDStages - 1);
+            asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
+            __syncwarp();
+            const uint16_t *xs = ring + (sl % kDStages) * kDSlab;
+            const float *wr = wrow + sl * kDSlab;
+#pragma unroll
+            for (int j = 0; j < kDSlab / 32; ++j)
+                acc = fmaf(__uint_as_float((uint32_t)xs[32 * j + lane] << 16), wr[32 * j + lane], acc);
+            __syncwarp();   // every lane is done with the slot before it is refilled
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
         if (lane == 0) logits[(size_t)warp * E + e] = bias ? acc + bias[e] : acc;

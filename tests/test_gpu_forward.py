@@ -57,23 +57,42 @@ def test_w4a4_paths_against_oracle(path):
     _parity(case, plan)
 
 
-@pytest.mark.parametrize("path", ["cuda_core", "tensor_core"])
+PATHS = {"cuda_core": moe.PATH_CUDA_CORE, "tensor_core": moe.PATH_TENSOR_CORE, "warp_mma": moe.PATH_WARP_MMA}
+
+
+@pytest.mark.parametrize("path", ["cuda_core", "tensor_core", "warp_mma"])
 def test_w4a16_paths_against_oracle(path):
     w = synth.scaled(synth.WORKLOADS["prompt512_w4a16"], tokens=200, hidden=1024, experts=16, inter=512,
                      shared_inter=256)
     case = Case(w, 3)
     plan = plan_for(w)
-    plan.set_path(moe.PATH_CUDA_CORE if path == "cuda_core" else moe.PATH_TENSOR_CORE)
+    plan.set_path(PATHS[path])
     _parity(case, plan)
 
 
+@pytest.mark.parametrize("path", ["tensor_core", "warp_mma"])
 @pytest.mark.parametrize("seed", [0, 1])
-def test_decode_w4a16_full_on_tensor_cores(seed):
+def test_decode_w4a16_full_on_tensor_paths(seed, path):
     w = synth.WORKLOADS["decode4_w4a16"]
     case = Case(w, seed)
     plan = plan_for(w)
-    plan.set_path(moe.PATH_TENSOR_CORE)
+    plan.set_path(PATHS[path])
     _parity(case, plan)
+
+
+def test_w4a16_warp_mma_matches_cuda_core_path():
+    w = synth.scaled(synth.WORKLOADS["prompt512_w4a16"], tokens=77, hidden=2048, experts=24, inter=768,
+                     shared_inter=512)
+    case = Case(w, 6)
+    p1, p2 = plan_for(w), plan_for(w)
+    p1.set_path(moe.PATH_CUDA_CORE)
+    p2.set_path(moe.PATH_WARP_MMA)
+    a, st1, _ = case.gpu_forward(p1)
+    b, st2, _ = case.gpu_forward(p2)
+    assert st1 == moe.OK and st2 == moe.OK
+    d = (a.float() - b.float()).abs()
+    rms = a.float().pow(2).mean().sqrt()
+    assert (d.max() / rms).item() < 2e-2 and (d.norm() / a.float().norm()).item() < 5e-3
 
 
 def test_w4a16_tensor_core_path_matches_cuda_core_path():
@@ -133,9 +152,13 @@ def test_every_token_on_one_expert():
     assert ref["offsets"][5] == 0 and ref["offsets"][6] == 40
 
 
-@pytest.mark.parametrize("mode,T", [("w4a16", 64), ("w4a16", 65), ("w4a16", 129), ("w4a4", 128), ("w4a4", 129)])
-def test_tile_boundaries_on_tensor_cores(mode, T):
-    # every token on experts 2 and 6: each holds T rows, cut into 64-row
+@pytest.mark.parametrize("mode,T,path", [("w4a16", 32, "tensor_core"), ("w4a16", 33, "tensor_core"),
+                                         ("w4a16", 65, "tensor_core"), ("w4a16", 16, "warp_mma"),
+                                         ("w4a16", 17, "warp_mma"), ("w4a16", 33, "warp_mma"),
+                                         ("w4a16", 129, "warp_mma"), ("w4a4", 128, "tensor_core"),
+                                         ("w4a4", 129, "tensor_core")])
+def test_tile_boundaries_on_tensor_cores(mode, T, path):
+    # every token on experts 2 and 6: each holds T rows, cut into 32-row
     # (W4A16) or 128-row (W4A4) tiles with a ragged last one
     base = synth.WORKLOADS["tiny_w4a16"] if mode == "w4a16" else synth.WORKLOADS["verify16_w4a4"]
     w = synth.scaled(base, tokens=T, hidden=512, experts=8, top_k=2, inter=256, shared_inter=256)
@@ -144,7 +167,7 @@ def test_tile_boundaries_on_tensor_cores(mode, T):
     case.bias[2] = 30.0
     case.bias[6] = 29.0
     plan = plan_for(w)
-    plan.set_path(moe.PATH_TENSOR_CORE)
+    plan.set_path(PATHS[path])
     _, ref, _ = _parity(case, plan)
     assert ref["offsets"][3] - ref["offsets"][2] == T and ref["offsets"][7] - ref["offsets"][6] == T
 
