@@ -66,8 +66,15 @@ class ClockSampler:
         os.close(fd)
         self.f = open(self.path, "w")
         self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
-                                      "--format=csv,noheader,nounits", "-lms", "100"],
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        # let the sampler finish starting up (it opens the driver) before anything is timed
+        t_end = time.time() + 10.0
+        while time.time() < t_end and self.proc.poll() is None:
+            self.f.flush()
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:

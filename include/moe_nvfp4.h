@@ -183,9 +183,10 @@ moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, si
  * 5th-generation tensor cores (tcgen05; W4A4 block-scaled FP4, W4A16 with the
  * weights widened to f16 in tensor memory).  WARP_MMA (W4A16 only): the
  * weights widened in registers straight into warp-level f16 MMAs, for tiles
- * of up to 32 token rows.  AUTO picks WARP_MMA for W4A16, the tcgen05 GEMMs
- * for W4A4 batches of 64 or more (token, expert) pairs, and CUDA_CORE
- * otherwise; the tensor paths need H and I multiples of 256.  All compute the
+ * of up to 32 token rows.  AUTO picks WARP_MMA for W4A16 batches with fewer
+ * than 2 (token, expert) pairs an expert on average (decode), the tcgen05
+ * GEMMs for larger W4A16 batches and for W4A4 batches of 64 or more pairs,
+ * and CUDA_CORE otherwise; the tensor paths need H and I multiples of 256.  All compute the
  * same function (the tolerance of the parity tests covers their different
  * summation orders). */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_CUDA_CORE = 1, MOE_PATH_TENSOR_CORE = 2, MOE_PATH_WARP_MMA = 3 } moe_path;
@@ -197,7 +198,7 @@ moe_status moe_plan_set_path(moe_plan plan, int32_t path);
 
 /* Stages of moe_forward, for moe_plan_read_profile. */
 typedef enum {
-    MOE_STAGE_ROUTE = 0,      /* logits + top-k (2 kernels) */
+    MOE_STAGE_ROUTE = 0,      /* logits + top-k (one kernel for T <= 16, else two) */
     MOE_STAGE_GROUP = 1,      /* histogram scan, stable placement, work lists */
     MOE_STAGE_QUANT_X = 2,    /* W4A4 activation quantisation */
     MOE_STAGE_PERMUTE = 3,    /* gather of activations into per-expert tiles */

@@ -169,6 +169,18 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
         if (s.done(moe::launch_router(p, x, T, rw, bias, p.ids, p.wts, st), moe::router_launches(T)) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
+    // engine: CUDA-core streaming kernels, tcgen05 grouped GEMMs, or (W4A16)
+    // warp-level MMAs fed from registers; AUTO takes the warp MMAs when the
+    // batch leaves fewer than two rows an expert on average (decode)
+    bool wm = plan->path == MOE_PATH_WARP_MMA;
+    bool tc = wm || plan->path == MOE_PATH_TENSOR_CORE;
+    if (plan->path == MOE_PATH_AUTO) {
+        wm = moe::warp_mma_supported(p) && T * p.cfg.top_k < 2 * p.cfg.num_experts;
+        tc = wm || (moe::tc_supported(p) && (p.cfg.mode == MOE_W4A16 || T * p.cfg.top_k >= 64));
+    }
+    // rows a tensor-core tile covers: 32 for the warp MMAs, 64 for the W4A16
+    // tcgen05 GEMMs, 128 for the W4A4 ones
+    p.tile_rows = p.cfg.mode == MOE_W4A4 ? moe::kTileRows : (wm ? 32 : 64);
     {
         Stage s(plan, MOE_STAGE_GROUP, st);
         if (s.done(moe::launch_group(p, T, p.ids, nullptr, nullptr, true, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
@@ -181,14 +193,6 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     moe::ExpertPtrs r = ptrs(*routed), sh{};
     if (shared) sh = ptrs(*shared);
     const moe::ExpertPtrs *shp = shared ? &sh : nullptr;
-    // engine: CUDA-core streaming kernels, tcgen05 grouped GEMMs, or (W4A16)
-    // warp-level MMAs fed from registers
-    bool wm = plan->path == MOE_PATH_WARP_MMA;
-    bool tc = wm || plan->path == MOE_PATH_TENSOR_CORE;
-    if (plan->path == MOE_PATH_AUTO) {
-        wm = moe::warp_mma_supported(p);
-        tc = wm || (moe::tc_supported(p) && T * p.cfg.top_k >= 64);
-    }
     {
         Stage s(plan, MOE_STAGE_GATE_UP, st);
         e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st, wm) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
@@ -248,7 +252,7 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
                      (cfg->has_shared ? (T + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows : 0);
     p.rows_pad_max = (p.rows_pad_max + moe::kTileRows - 1) / moe::kTileRows * moe::kTileRows;
     p.chunks_max = p.pairs_max / moe::kChunkRows + E + 2 + (cfg->has_shared ? T / moe::kChunkRows + 1 : 0);
-    p.tile_rows = cfg->mode == MOE_W4A16 ? 32 : moe::kTileRows;
+    p.tile_rows = cfg->mode == MOE_W4A16 ? 32 : moe::kTileRows;   // the smallest tiles a call may use
     p.tiles_max = p.pairs_max / p.tile_rows + E + 2 + (cfg->has_shared ? T / p.tile_rows + 1 : 0);
     Carver dry;
     carve(p, dry);

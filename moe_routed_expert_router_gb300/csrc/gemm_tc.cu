@@ -897,87 +897,12 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
     }
 }
 
+// Compute warps of k_gemm_reg (warps 1..16).
 template <int EPI>
-__global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *code_ring = smem;
-    uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
-    float *xchg = reinterpret_cast<float *>(b_ring + kRBStages * kRBTile);
-    uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
-    uint64_t *cempty = cfull + kHCStages;
-    uint64_t *bfull = cempty + kHCStages;
-    uint64_t *bempty = bfull + kRBStages;
-    uint64_t *xfull = bempty + kRBStages;        // [8] up accumulators written (SwiGLU)
-    uint64_t *xempty = xfull + 8;                // [8] and read
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
+                                            float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
+                                            uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
     const int n_items = a.scratch->n_tiles * a.nf;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
-        for (int i = 0; i < kRBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
-        for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------------------------------- producer of the code ring
-            RingPos c;
-            bool ok = true;
-            uint32_t used = 0, last_ph = 0;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-                Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
-                const int m = it.sh ? 1 : 0;
-                int r0, r1;
-                h_rows(a, it, EPI, r0, r1);
-                const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
-                const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
-                for (int kc = 0; kc < it.K / kHCK; ++kc) {
-                    if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
-                    uint8_t *st = code_ring + c.s * kHCodeStage;
-                    mbar_expect_tx(cfull + c.s, kHCodeStage);
-                    tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
-                    tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
-                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, kc * 16, r0);
-                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
-                    used |= 1u << c.s;
-                    last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
-                    c.next(kHCStages);
-                }
-            }
-            for (int t = 0; t < kHCStages; ++t)
-                if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
-        } else if (lane == 1) {
-            // ---------------------------------------- producer of the token-row ring
-            RingPos b;
-            bool ok = true;
-            uint32_t used = 0, last_ph = 0;
-            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-                Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
-                const int rc = it.valid <= 16 ? 0 : 1;
-                const int rows = 16 << rc;
-                for (int kc = 0; kc < it.K / kHCK; ++kc) {
-                    if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
-                    mbar_expect_tx(bfull + b.s, (uint32_t)(4 * rows * 128));
-                    for (int bx = 0; bx < 4; ++bx)
-                        tma_2d(b_ring + b.s * kRBTile + bx * rows * 128, &a.b[rc], bfull + b.s, kc * kHCK + bx * 64,
-                               it.row0);
-                    used |= 1u << b.s;
-                    last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
-                    b.next(kRBStages);
-                }
-            }
-            for (int t = 0; t < kRBStages; ++t)
-                if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
-        }
-        return;
-    }
-
-    // ---------------------------------------------------- compute warps
     const int cw = warp - 1, rg = cw & 7, op = cw >> 3;
     const int g = lane >> 2, q = lane & 3;
     const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
@@ -1068,6 +993,88 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
         }
     }
     if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(a.err, kErrDevice);
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *code_ring = smem;
+    uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
+    float *xchg = reinterpret_cast<float *>(b_ring + kRBStages * kRBTile);
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
+    uint64_t *cempty = cfull + kHCStages;
+    uint64_t *bfull = cempty + kHCStages;
+    uint64_t *bempty = bfull + kRBStages;
+    uint64_t *xfull = bempty + kRBStages;        // [8] up accumulators written (SwiGLU)
+    uint64_t *xempty = xfull + 8;                // [8] and read
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_items = a.scratch->n_tiles * a.nf;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
+        for (int i = 0; i < kRBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
+        for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------- producer of the code ring
+            RingPos c;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int m = it.sh ? 1 : 0;
+                int r0, r1;
+                h_rows(a, it, EPI, r0, r1);
+                const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
+                const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
+                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                    if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
+                    uint8_t *st = code_ring + c.s * kHCodeStage;
+                    mbar_expect_tx(cfull + c.s, kHCodeStage);
+                    tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
+                    tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
+                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, kc * 16, r0);
+                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
+                    used |= 1u << c.s;
+                    last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
+                    c.next(kHCStages);
+                }
+            }
+            for (int t = 0; t < kHCStages; ++t)
+                if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
+        } else if (lane == 1) {
+            // ---------------------------------------- producer of the token-row ring
+            RingPos b;
+            bool ok = true;
+            uint32_t used = 0, last_ph = 0;
+            for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+                Item it;
+                if (!decode_item_h(a, item, EPI, it)) continue;
+                const int rc = it.valid <= 16 ? 0 : 1;
+                const int rows = 16 << rc;
+                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                    if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
+                    mbar_expect_tx(bfull + b.s, (uint32_t)(4 * rows * 128));
+                    for (int bx = 0; bx < 4; ++bx)
+                        tma_2d(b_ring + b.s * kRBTile + bx * rows * 128, &a.b[rc], bfull + b.s, kc * kHCK + bx * 64,
+                               it.row0);
+                    used |= 1u << b.s;
+                    last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
+                    b.next(kRBStages);
+                }
+            }
+            for (int t = 0; t < kRBStages; ++t)
+                if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
+        }
+    } else {
+        reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty);
+    }
 }
 
 // x rows (bf16) -> padded per-expert f16 rows, times 2^-s (exact; s from the
@@ -1190,11 +1197,9 @@ cudaError_t configure_tc(const Plan &) {
     return e;
 }
 
-// Shapes the register-path W4A16 kernels take: those of the tcgen05 kernels,
-// with tiles of at most 32 token rows.
-bool warp_mma_supported(const Plan &p) {
-    return p.cfg.mode == MOE_W4A16 && p.tile_rows <= 32 && tc_supported(p);
-}
+// Shapes the register-path W4A16 kernels take: those of the tcgen05 kernels
+// (the caller cuts their tiles at 32 token rows).
+bool warp_mma_supported(const Plan &p) { return p.cfg.mode == MOE_W4A16 && tc_supported(p); }
 
 namespace {
 

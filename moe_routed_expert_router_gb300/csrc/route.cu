@@ -143,8 +143,18 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
     }
 }
 
+// Order-preserving map of an fp32 logit to an unsigned key (larger logit ->
+// larger key); NaN maps to 0, below every other value, and is never chosen.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    const uint32_t b = __float_as_uint(v);
+    if (v != v) return 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
 // Top-k of token t by logit (ties -> lower id), then the weights; one warp,
-// NPL logits per lane (expert lane + 32*i).  Logits are read through L2 (they
+// NPL logits per lane (expert lane + 32*i).  Each round every lane offers its
+// best remaining (key, id); redux.sync takes the warp's largest key, then the
+// smallest id among the lanes offering it.  Logits are read through L2 (they
 // may come from other blocks of the same launch).
 template <int NPL>
 __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int t, int E, int k, int kind, int renorm,
@@ -153,42 +163,44 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int
     const int lane = threadIdx.x & 31;
     const float NEG = -__int_as_float(0x7f800000);
     float v[NPL];
+    uint32_t key[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         int e = lane + 32 * i;
         v[i] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : NEG;
+        key[i] = (e < E) ? logit_key(v[i]) : 0u;
     }
-    uint32_t taken = 0;
-#pragma unroll
-    for (int i = 0; i < NPL; ++i)
-        if (lane + 32 * i >= E) taken |= 1u << i;
     float mine = 0.0f;  // lane j keeps the logit of slot j
     for (int j = 0; j < k; ++j) {
-        float bv = NEG;
+        uint32_t bk = 0u;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            if (taken & (1u << i)) continue;
-            int e = lane + 32 * i;
-            if (bi == 0x7fffffff || v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            bool take = (oi != 0x7fffffff) && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-            if (take) { bv = ov; bi = oi; }
-        }
-        if (bi == 0x7fffffff || bi >= E) {  // only NaN logits left
+        for (int i = 0; i < NPL; ++i)
+            if (key[i] > bk) { bk = key[i]; bi = lane + 32 * i; }   // i ascending: ties keep the lower id
+        const uint32_t wk = __reduce_max_sync(0xffffffffu, bk);
+        int wi = (int)__reduce_min_sync(0xffffffffu, (bk == wk && wk != 0u) ? (uint32_t)bi : 0x7fffffffu);
+        float wv;
+        if (wk == 0u || wi >= E) {  // only NaN logits left
             if (lane == 0) atomicOr(err, kErrDevice);
-            bi = 0;
-            bv = 0.0f;
+            wi = 0;
+            wv = 0.0f;
+        } else {
+            wv = __shfl_sync(0xffffffffu, v[0], wi & 31);
+#pragma unroll
+            for (int i = 1; i < NPL; ++i) {
+                const float o = __shfl_sync(0xffffffffu, v[i], wi & 31);
+                if ((wi >> 5) == i) wv = o;
+            }
+            if ((wi & 31) == lane) {
+#pragma unroll
+                for (int i = 0; i < NPL; ++i)
+                    if ((wi >> 5) == i) key[i] = 0u;
+            }
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == j) mine = bv;
+        if (lane == j) mine = wv;
         if (lane == 0) {
-            ids[(size_t)t * k + j] = bi;
-            if (counts) atomicAdd(counts + bi, 1);
+            ids[(size_t)t * k + j] = wi;
+            if (counts) atomicAdd(counts + wi, 1);
         }
     }
     float num = 0.0f, den;
@@ -229,15 +241,18 @@ __global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ l
 // Decode-sized batches (T <= 16), router and top-k in one launch: block e
 // computes expert e's logit for every token.  The router row (H fp32) is
 // staged in shared memory once; warp t streams token t's x row through its own
-// 4-deep cp.async ring of 256-position slabs (one 16-byte copy a lane a slab,
-// no block barrier), lane l taking positions 32j + l in increasing j.  Each
+// 4-deep cp.async ring of 1024-position slabs (512 for T > 8, so two blocks
+// fit an SM; the last slab ragged; 16-byte copies, no block barrier), lane l
+// taking positions 32j + l in increasing j.  Each
 // block also checks a 1/E slice of x (non-finite values, amax).  The last
 // block to finish (a ticket in the per-call scratch) runs the top-k for all
 // tokens, one warp a token.
 constexpr int kDecodeRouterThreads = 512;
-constexpr int kDSlab = 256, kDStages = 4;
+constexpr int kDSlab = 1024, kDStages = 4;
 
-size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * kDSlab * 2; }
+__host__ __device__ __forceinline__ int decode_slab(int T) { return T <= 8 ? kDSlab : kDSlab / 2; }
+
+size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * decode_slab(T) * 2; }
 
 template <int NPL>
 __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
@@ -250,13 +265,19 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int e = blockIdx.x;
-    const int slabs = H / kDSlab;
+    const int slab = decode_slab(T);
+    const int slabs = (H + slab - 1) / slab;
     for (int c = tid; c < H / 4; c += kDecodeRouterThreads) cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
     asm volatile("cp.async.commit_group;" ::: "memory");
-    uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + H) + (size_t)warp * kDStages * kDSlab;
+    uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + H) + (size_t)warp * kDStages * slab;
     const uint16_t *xr = x + (size_t)warp * H;
-    auto load_x = [&](int sl) {   // warp-private: lane l copies positions 8l .. 8l+7 of the slab
-        if (sl < slabs) cp_async16(ring + (sl % kDStages) * kDSlab + 8 * lane, xr + sl * kDSlab + 8 * lane, true);
+    auto load_x = [&](int sl) {   // warp-private: lane l copies 16-byte chunks lane + 32i of the slab
+        if (sl < slabs) {
+            for (int i = 0; i < slab / 256; ++i) {
+                const int c = lane + 32 * i;
+                if (sl * slab + 8 * c < H) cp_async16(ring + (sl % kDStages) * slab + 8 * c, xr + sl * slab + 8 * c, true);
+            }
+        }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
     if (warp < T) {
@@ -302,11 +323,21 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
             load_x(sl + kDStages - 1);
             asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
             __syncwarp();
-            const uint16_t *xs = ring + (sl % kDStages) * kDSlab;
-            const float *wr = wrow + sl * kDSlab;
+            const uint16_t *xs = ring + (sl % kDStages) * slab;
+            const float *wr = wrow + sl * slab;
+            const int len = min(slab, H - sl * slab);   // a multiple of 256
+#pragma unroll 4
+            for (int j0 = 0; j0 < len / 32; j0 += 8) {   // loads of the group issue ahead of its FMA chain
+                uint32_t xv[8];
+                float wv[8];
 #pragma unroll
-            for (int j = 0; j < kDSlab / 32; ++j)
-                acc = fmaf(__uint_as_float((uint32_t)xs[32 * j + lane] << 16), wr[32 * j + lane], acc);
+                for (int j = 0; j < 8; ++j) {
+                    xv[j] = xs[32 * (j0 + j) + lane];
+                    wv[j] = wr[32 * (j0 + j) + lane];
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc = fmaf(__uint_as_float(xv[j] << 16), wv[j], acc);
+            }
             __syncwarp();   // every lane is done with the slot before it is refilled
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
