@@ -138,6 +138,21 @@ def build_weights(moe, w, seed):
     return routed, shared
 
 
+def ncu_traffic(key: str, workload: str):
+    """DRAM bytes (read + write) of one launch of a stage's kernel, from the
+    committed ncu summary table profiles/dram_traffic.txt (lines
+    "stage:path workload bytes"); None when no capture covers it."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.txt")
+    try:
+        for line in open(path):
+            f = line.split("#")[0].split()
+            if len(f) >= 3 and f[0] == key and f[1] == workload:
+                return int(float(f[2]))
+    except OSError:
+        pass
+    return None
+
+
 def algorithmic(w, ids_list):
     """Per-step algorithmic bytes of the gate/up and down kernels and flops,
     averaged over the instances (distinct experts touched come from routing)."""
@@ -337,9 +352,16 @@ def run_ours(args, w, world, rank, local):
     if dom in alg:
         ach = alg[dom] / (per_launch[dom] / 1e3) / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": ncu_traffic(f"{dom}:{args.path}", w.name),
                 "peak_source": pk["source"], "algorithmic_bytes_per_launch": round(alg[dom]),
                 "avg_launch_us": round(per_launch[dom] * 1e3, 2)}
+        if w.mode == "w4a4":
+            # the FP4 tensor roof beside the HBM one: dense NVFP4 peak = measured bf16 x 6 (nominal ratio)
+            fl = flops * (2.0 / 3.0 if dom == "gate_up" else 1.0 / 3.0)
+            tf = fl / (per_launch[dom] / 1e3) / 1e12
+            roof["fp4_tflops"] = round(tf, 1)
+            roof["fp4_peak_tflops"] = round(pk["bf16_tflops"] * 6, 1)
+            roof["fp4_frac"] = round(tf / (pk["bf16_tflops"] * 6), 4)
     launches = sum(v[1] for v in prof.values())
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
