@@ -65,6 +65,7 @@ struct TcArgs {
     int P, k;
     float *acc;             // G2 output [T][H]
     int *err;
+    int colfirst;           // down items column group first (large T; see decode_item)
 };
 
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
@@ -130,11 +131,19 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float *v) {
 
 struct Item {
     int e, row0, valid, f, sh, K;
+    int kc0, kc1;   // code stages [kc0, kc1) of K this item covers (split-K down items)
 };
 
+// Items run tile by tile (one tile's token rows against every weight group).
+// For many tokens the down items run column group by column group instead, so
+// the scatter-add into the fp32 accumulator touches a [T][256] slice of it at
+// a time and the slice stays in L2 (for few tokens that order would make the
+// CTAs running at the same time add into the same few addresses).
 __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, Item &it) {
-    const int4 t = a.tiles[item / a.nf];
-    it.f = item % a.nf;
+    const int nt = a.scratch->n_tiles;
+    const bool cf = epi == kScatter && a.colfirst;
+    const int4 t = a.tiles[cf ? item % nt : item / a.nf];
+    it.f = cf ? item / nt : item % a.nf;
     it.e = t.x;
     it.row0 = t.y;
     it.valid = t.z;
@@ -462,6 +471,7 @@ struct HcArgs {
     int P, k;
     float *acc;
     int *err;
+    int colfirst;           // down items column group first (large T; see decode_item_h)
 };
 
 // f16 scale exponent s of the activations: x * 2^-s keeps amax below 2^15.
@@ -496,22 +506,36 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 // 16 << class and a B stage holds (8 >> class) boxes of 64 K values.
 __device__ __forceinline__ int hrows_class(int valid) { return valid <= 16 ? 0 : (valid <= 32 ? 1 : 2); }
 
-// Item = tile * nf + f: the tile's token rows against weight-row group f.
-// Returns false for a group past the expert's intermediate size.
-__device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi, Item &it) {
-    const int4 t = a.tiles[item / a.nf];
-    it.f = item % a.nf;
+// Item = (tile * nf + f) * ks + kh: the tile's token rows against weight-row
+// group f, part kh of K (down items only are split).  For many tokens the
+// down items run column group first, (kh * nf + f) * n_tiles + tile, so the
+// accumulator slice being added into stays in L2 (see decode_item).  Returns
+// false for a group past the expert's intermediate size or an empty part of K.
+__device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi, int ks, Item &it) {
+    const int nt = a.scratch->n_tiles;
+    int tile, kh = 0;
+    if (epi == kScatter && a.colfirst) {
+        tile = item % nt;
+        const int rest = item / nt;
+        it.f = rest % a.nf;
+        kh = rest / a.nf;
+    } else {
+        kh = item % ks;
+        tile = (item / ks) / a.nf;
+        it.f = (item / ks) % a.nf;
+    }
+    const int4 t = a.tiles[tile];
     it.e = t.x;
     it.row0 = t.y;
     it.valid = min(t.z, kHBRows);
     it.sh = (t.x == a.E);
     const int I = it.sh ? a.Is : a.I;
-    if (epi == kSwiGLU) {
-        it.K = a.H;
-        return it.f * 128 < I;
-    }
-    it.K = I;
-    return true;
+    it.K = epi == kSwiGLU ? a.H : I;
+    const int stages = it.K / kHCK, per = (stages + ks - 1) / ks;
+    it.kc0 = kh * per;
+    it.kc1 = min(stages, it.kc0 + per);
+    if (epi == kSwiGLU) return it.f * 128 < I;
+    return it.kc0 < it.kc1;
 }
 
 __device__ __forceinline__ void h_rows(const HcArgs &a, const Item &it, int epi, int &r0, int &r1) {
@@ -550,6 +574,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ks = 1;   // no split of K here
     const int n_items = a.scratch->n_tiles * a.nf;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, kConvWarps); }
@@ -576,13 +601,13 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!decode_item_h(a, item, EPI, ks, it)) continue;
                 const int m = it.sh ? 1 : 0;
                 int r0, r1;
                 h_rows(a, it, EPI, r0, r1);
                 const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
                 const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
-                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                for (int kc = it.kc0; kc < it.kc1; ++kc) {
                     if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
                     uint8_t *st = code_ring + c.s * kHCodeStage;
                     mbar_expect_tx(cfull + c.s, kHCodeStage);
@@ -604,7 +629,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!decode_item_h(a, item, EPI, ks, it)) continue;
                 const int rc = hrows_class(it.valid);
                 const int rows = 16 << rc, boxes = 8 >> rc, nq = it.K / kHBK;
                 for (int q0 = 0; q0 < nq; q0 += boxes) {
@@ -639,8 +664,8 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         bool ok = true;
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             Item it;
-            if (!decode_item_h(a, item, EPI, it)) continue;
-            for (int kc = 0; ok && kc < it.K / kHCK; ++kc) {
+            if (!decode_item_h(a, item, EPI, ks, it)) continue;
+            for (int kc = it.kc0; ok && kc < it.kc1; ++kc) {
                 if (!mbar_wait(cfull + cs.s, cs.ph, a.err)) { ok = false; break; }
                 const uint32_t st = ring0 + cs.s * kHCodeStage;
                 const uint32_t row = st + op * kHCodeTile + c * 128;
@@ -691,7 +716,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
             bool ok = true;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!decode_item_h(a, item, EPI, ks, it)) continue;
                 if (!mbar_wait(acc_empty + buf, ((aph >> buf) & 1u) ^ 1u, a.err)) break;
                 aph ^= 1u << buf;
                 tc_fence_after();
@@ -739,7 +764,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         bool range_bad = false;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
             Item it;
-            if (!decode_item_h(a, item, EPI, it)) continue;
+            if (!decode_item_h(a, item, EPI, ks, it)) continue;
             if (!mbar_wait(acc_full + buf, (aph >> buf) & 1u, a.err)) break;
             aph ^= 1u << buf;
             tc_fence_after();
@@ -825,12 +850,12 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
 // values a stage).  Sixteen compute warps: warp (row group rg, operand op)
 // owns 16 rows of one operand and all K.
 //
-// K order inside a 64-value super-block: lane quad q (lane & 3) holds the 16
-// consecutive K values 16q .. 16q+15, i.e. exactly one scale block, so each
-// lane scales its codes with one E4M3 value a row; MMA m (0..3) takes K values
-// 16q + 4m + {0,1} as fragment columns 2q, 2q+1 and 16q + 4m + {2,3} as 2q+8,
-// 2q+9.  The token-row fragments use the same map, so the sum is the same dot
-// product in another order.
+// K order inside a 128-value group: lane quad q (lane & 3) holds the 32
+// consecutive K values 32q .. 32q+31, i.e. exactly two scale blocks, so a lane
+// scales each of its codes with one E4M3 value a row and block; MMA m (0..3)
+// of block b takes K values 32q + 16b + 4m + {0,1} as fragment columns 2q,
+// 2q+1 and 32q + 16b + 4m + {2,3} as 2q+8, 2q+9.  The token-row fragments use
+// the same map, so the sum is the same dot product in another order.
 constexpr int kRThreads = 32 * (1 + 16);
 constexpr int kRBStages = 3;
 constexpr int kRBTile = 32 * 512;                 // 16 KB: up to 32 token rows x 256 K f16
@@ -902,7 +927,8 @@ template <int EPI>
 __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
                                             float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
                                             uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
-    const int n_items = a.scratch->n_tiles * a.nf;
+    const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
+    const int n_items = a.scratch->n_tiles * a.nf * ks;
     const int cw = warp - 1, rg = cw & 7, op = cw >> 3;
     const int g = lane >> 2, q = lane & 3;
     const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
@@ -913,14 +939,14 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
     bool ok = true, range_bad = false;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item it;
-        if (!decode_item_h(a, item, EPI, it)) continue;
+        if (!decode_item_h(a, item, EPI, ks, it)) continue;
         const int nt_n = (it.valid + 7) >> 3;
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
-        for (int kc = 0; kc < it.K / kHCK; ++kc) {
+        for (int kc = it.kc0; kc < it.kc1; ++kc) {
             if (!mbar_wait(cfull + cs.s, cs.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) { ok = false; break; }
             const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * kRBTile;
             switch (nt_n) {
@@ -1010,7 +1036,8 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
     uint64_t *xempty = xfull + 8;                // [8] and read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = a.scratch->n_tiles * a.nf;
+    const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
+    const int n_items = a.scratch->n_tiles * a.nf * ks;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
         for (int i = 0; i < kRBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
@@ -1027,13 +1054,13 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!decode_item_h(a, item, EPI, ks, it)) continue;
                 const int m = it.sh ? 1 : 0;
                 int r0, r1;
                 h_rows(a, it, EPI, r0, r1);
                 const CUtensorMap *A1 = (EPI == kSwiGLU) ? &a.a1[m] : &a.a0[m];
                 const CUtensorMap *S1 = (EPI == kSwiGLU) ? &a.s1[m] : &a.s0[m];
-                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                for (int kc = it.kc0; kc < it.kc1; ++kc) {
                     if (!mbar_wait(cempty + c.s, c.ph ^ 1, a.err)) { ok = false; break; }
                     uint8_t *st = code_ring + c.s * kHCodeStage;
                     mbar_expect_tx(cfull + c.s, kHCodeStage);
@@ -1055,10 +1082,10 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, it)) continue;
+                if (!decode_item_h(a, item, EPI, ks, it)) continue;
                 const int rc = it.valid <= 16 ? 0 : 1;
                 const int rows = 16 << rc;
-                for (int kc = 0; kc < it.K / kHCK; ++kc) {
+                for (int kc = it.kc0; kc < it.kc1; ++kc) {
                     if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
                     mbar_expect_tx(bfull + b.s, (uint32_t)(4 * rows * 128));
                     for (int bx = 0; bx < 4; ++bx)
@@ -1224,6 +1251,7 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.pad_pair = p.pad_pair;
     a.wts = p.wts;
     a.P = T * c.top_k;
+    a.colfirst = T >= 128;
     a.k = c.top_k;
     a.acc = p.acc;
     a.err = p.err;
@@ -1303,6 +1331,7 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
     a.pad_pair = p.pad_pair;
     a.wts = p.wts;
     a.P = T * c.top_k;
+    a.colfirst = T >= 128;
     a.k = c.top_k;
     a.acc = p.acc;
     a.err = p.err;

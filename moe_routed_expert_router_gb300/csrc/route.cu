@@ -24,6 +24,17 @@ __device__ __forceinline__ bool bf16x2_bad(uint32_t u) {
     return ((u & 0x7F80u) == 0x7F80u) | ((u & 0x7F800000u) == 0x7F800000u);
 }
 
+// Two independent IEEE fp32 FMAs (round to nearest) in one instruction:
+// (a.x*b.x + c.x, a.y*b.y + c.y), each exactly fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;"
+        : "=l"(r)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&r);
+}
+
 __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool valid) {
     const uint32_t d = smem_u32(dst);
     const int n = valid ? 16 : 0;
@@ -70,11 +81,11 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    float acc[8][8];
+    float2 acc2[8][4];   // (token t, experts 2p and 2p+1): two chains in one packed FMA
 #pragma unroll
     for (int t = 0; t < 8; ++t)
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t][e] = 0.0f;
+        for (int p = 0; p < 4; ++p) acc2[t][p] = make_float2(0.0f, 0.0f);
     bool bad = false;
     float amax = 0.0f;
 #pragma unroll
@@ -100,24 +111,27 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
 #pragma unroll
         for (int i = 0; i < kRSlab / 32; ++i) {
             const int h = 32 * i + lane;
-            float xv[8], wv[8];
+            float xv[8];
+            float2 wv[4];
 #pragma unroll
             for (int t = 0; t < 8; ++t) xv[t] = __uint_as_float((uint32_t)xb[(tw + t) * kRSlab + h] << 16);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) wv[e] = wb[(ew + e) * kRSlab + h];
+            for (int p = 0; p < 4; ++p)
+                wv[p] = make_float2(wb[(ew + 2 * p) * kRSlab + h], wb[(ew + 2 * p + 1) * kRSlab + h]);
 #pragma unroll
             for (int t = 0; t < 8; ++t)
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(xv[t], wv[e], acc[t][e]);
+                for (int p = 0; p < 4; ++p) acc2[t][p] = ffma2(make_float2(xv[t], xv[t]), wv[p], acc2[t][p]);
         }
         __syncthreads();
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
+    float acc[8][8];
 #pragma unroll
     for (int t = 0; t < 8; ++t)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float v = acc[t][e];
+            float v = (e & 1) ? acc2[t][e >> 1].y : acc2[t][e >> 1].x;
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = v + __shfl_xor_sync(0xffffffffu, v, o);
             acc[t][e] = v;
