@@ -196,7 +196,7 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     {
         Stage s(plan, MOE_STAGE_GATE_UP, st);
         e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st, wm) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
-        if (s.done(e, tc ? 2 : 1) != cudaSuccess) return MOE_ERR_CUDA;
+        if (s.done(e, (tc && !wm) ? 2 : 1) != cudaSuccess) return MOE_ERR_CUDA;   // + the permute launch
     }
     if (p.cfg.mode == MOE_W4A4) {
         Stage s(plan, MOE_STAGE_QUANT_H, st);

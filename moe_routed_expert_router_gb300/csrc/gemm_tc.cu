@@ -472,6 +472,10 @@ struct HcArgs {
     float *acc;
     int *err;
     int colfirst;           // down items column group first (large T; see decode_item_h)
+    // warp-MMA engine: ring geometry chosen per launch, and the raw activations
+    // the gate/up launch gathers its token rows from (no separate permute)
+    int rcst, rbst, rbslot;
+    const uint16_t *x;
 };
 
 // f16 scale exponent s of the activations: x * 2^-s keeps amax below 2^15.
@@ -856,11 +860,16 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
 // of block b takes K values 32q + 16b + 4m + {0,1} as fragment columns 2q,
 // 2q+1 and 32q + 16b + 4m + {2,3} as 2q+8, 2q+9.  The token-row fragments use
 // the same map, so the sum is the same dot product in another order.
-constexpr int kRThreads = 32 * (1 + 16);
-constexpr int kRBStages = 3;
-constexpr int kRBTile = 32 * 512;                 // 16 KB: up to 32 token rows x 256 K f16
+constexpr int kRThreads = 32 * (2 + 16);          // TMA producer, token-row gatherer, 16 compute warps
 constexpr int kRXchg = 8 * 4 * 32 * 4 * 4;        // 16 KB: up-operand accumulators handed to the gate warps
-constexpr size_t kRSmemBytes = (size_t)kHCStages * kHCodeStage + (size_t)kRBStages * kRBTile + kRXchg + 512 + 1024;
+// Ring geometry a launch picks: with at most 16 tokens every tile has at most
+// 16 rows, so token-row slots of 8 KB leave room for a fifth weight stage.
+struct RegRings { int cst, bst, bslot; };
+constexpr RegRings kRegSmall{5, 3, 16 * 512}, kRegLarge{4, 3, 32 * 512};
+constexpr size_t reg_smem(RegRings r) {
+    return (size_t)r.cst * kHCodeStage + (size_t)r.bst * r.bslot + kRXchg + 512 + 1024;
+}
+constexpr size_t kRSmemBytes = reg_smem(kRegSmall) > reg_smem(kRegLarge) ? reg_smem(kRegSmall) : reg_smem(kRegLarge);
 static_assert(kRSmemBytes <= 227 * 1024, "register-path pipeline exceeds shared memory");
 
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -929,7 +938,7 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
                                             uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
     const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
     const int n_items = a.scratch->n_tiles * a.nf * ks;
-    const int cw = warp - 1, rg = cw & 7, op = cw >> 3;
+    const int cw = warp - 2, rg = cw & 7, op = cw >> 3;
     const int g = lane >> 2, q = lane & 3;
     const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
     const int xs = f16_shift(a.scratch->x_amax);
@@ -948,7 +957,7 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
         for (int kc = it.kc0; kc < it.kc1; ++kc) {
             if (!mbar_wait(cfull + cs.s, cs.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) { ok = false; break; }
-            const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * kRBTile;
+            const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * a.rbslot;
             switch (nt_n) {
                 case 1: reg_stage<1>(st, bst, op, rg, lane, acc); break;
                 case 2: reg_stage<2>(st, bst, op, rg, lane, acc); break;
@@ -957,8 +966,8 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             }
             __syncwarp();
             if (lane == 0) { mbar_arrive(cempty + cs.s); mbar_arrive(bempty + bs.s); }
-            cs.next(kHCStages);
-            bs.next(kRBStages);
+            cs.next(a.rcst);
+            bs.next(a.rbst);
         }
         if (!ok) break;
         const int m = it.sh ? 1 : 0;
@@ -1021,26 +1030,98 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
     if (__any_sync(0xffffffffu, range_bad) && lane == 0) atomicOr(a.err, kErrDevice);
 }
 
+// Token-row gatherer of the gate/up launch (one warp): builds each 256-value
+// K stage of the tile's f16 token rows straight from x (bf16 -> f16 x 2^-s,
+// exact), in the 128-byte-swizzled box layout the compute warps read.
+template <int EPI>
+__device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b_ring, uint64_t *bfull,
+                                           uint64_t *bempty, int n_items, int ks) {
+    const float scale = __uint_as_float((uint32_t)(127 - f16_shift(a.scratch->x_amax)) << 23);   // 2^-s
+    RingPos b;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        Item it;
+        if (!decode_item_h(a, item, EPI, ks, it)) continue;
+        const int rows = it.valid <= 16 ? 16 : 32;
+        int tok = 0;   // lane n < valid: token of row n
+        if (lane < it.valid) {
+            const int pair = a.pad_pair[it.row0 + lane];
+            tok = pair >= a.P ? pair - a.P : pair / a.k;
+        }
+        // lane c copies chunk c (8 K values kc*256 + 8c .. +8) of every row, 512
+        // contiguous bytes a row.  The first four rows (all of a decode tile) of
+        // the next stage are loaded while the current one is converted.
+        uint4 nx[4];
+        auto load8 = [&](int kc, int n0, uint4 (&v)[4]) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = __shfl_sync(0xffffffffu, tok, (n0 + j) & 31);
+                if (n0 + j < it.valid)
+                    v[j] = __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.H + kc * kHCK + 8 * lane));
+            }
+        };
+        auto store8 = [&](uint32_t slot, int n0, const uint4 (&v)[4]) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + j;
+                if (n < it.valid) {
+                    const uint32_t u[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                    uint32_t o[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        __half2 h = __floats2half2_rn(__uint_as_float(u[q] << 16) * scale,
+                                                      __uint_as_float(u[q] & 0xFFFF0000u) * scale);
+                        o[q] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    const uint32_t box = (uint32_t)(lane >> 3), ch = (uint32_t)(lane & 7) ^ (uint32_t)(n & 7);
+                    sts128(slot + box * rows * 128 + n * 128 + (ch << 4), make_uint4(o[0], o[1], o[2], o[3]));
+                }
+            }
+        };
+        load8(it.kc0, 0, nx);
+        for (int kc = it.kc0; kc < it.kc1; ++kc) {
+            uint4 cur[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) cur[j] = nx[j];
+            if (kc + 1 < it.kc1) load8(kc + 1, 0, nx);
+            if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) ok = false;
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const uint32_t slot = smem_u32(b_ring + b.s * a.rbslot);
+            store8(slot, 0, cur);
+            for (int n0 = 4; n0 < it.valid; n0 += 4) {   // rows beyond four: loaded in place
+                uint4 v[4];
+                load8(kc, n0, v);
+                store8(slot, n0, v);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bfull + b.s);
+            b.next(a.rbst);
+        }
+    }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *code_ring = smem;
-    uint8_t *b_ring = code_ring + kHCStages * kHCodeStage;
-    float *xchg = reinterpret_cast<float *>(b_ring + kRBStages * kRBTile);
+    uint8_t *b_ring = code_ring + (size_t)a.rcst * kHCodeStage;
+    float *xchg = reinterpret_cast<float *>(b_ring + (size_t)a.rbst * a.rbslot);
     uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
-    uint64_t *cempty = cfull + kHCStages;
-    uint64_t *bfull = cempty + kHCStages;
-    uint64_t *bempty = bfull + kRBStages;
-    uint64_t *xfull = bempty + kRBStages;        // [8] up accumulators written (SwiGLU)
+    uint64_t *cempty = cfull + a.rcst;
+    uint64_t *bfull = cempty + a.rcst;
+    uint64_t *bempty = bfull + a.rbst;
+    uint64_t *xfull = bempty + a.rbst;           // [8] up accumulators written (SwiGLU)
     uint64_t *xempty = xfull + 8;                // [8] and read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
     const int n_items = a.scratch->n_tiles * a.nf * ks;
+    const bool gather = EPI == kSwiGLU && a.x != nullptr;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
-        for (int i = 0; i < kRBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
+        for (int i = 0; i < a.rcst; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
+        for (int i = 0; i < a.rbst; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
         for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -1070,13 +1151,13 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                     tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
                     used |= 1u << c.s;
                     last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
-                    c.next(kHCStages);
+                    c.next(a.rcst);
                 }
             }
-            for (int t = 0; t < kHCStages; ++t)
+            for (int t = 0; t < a.rcst; ++t)
                 if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
-        } else if (lane == 1) {
-            // ---------------------------------------- producer of the token-row ring
+        } else if (lane == 1 && !gather) {
+            // ---------------------------------------- TMA producer of the token-row ring
             RingPos b;
             bool ok = true;
             uint32_t used = 0, last_ph = 0;
@@ -1089,16 +1170,18 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                     if (!mbar_wait(bempty + b.s, b.ph ^ 1, a.err)) { ok = false; break; }
                     mbar_expect_tx(bfull + b.s, (uint32_t)(4 * rows * 128));
                     for (int bx = 0; bx < 4; ++bx)
-                        tma_2d(b_ring + b.s * kRBTile + bx * rows * 128, &a.b[rc], bfull + b.s, kc * kHCK + bx * 64,
+                        tma_2d(b_ring + b.s * a.rbslot + bx * rows * 128, &a.b[rc], bfull + b.s, kc * kHCK + bx * 64,
                                it.row0);
                     used |= 1u << b.s;
                     last_ph = (last_ph & ~(1u << b.s)) | (b.ph << b.s);
-                    b.next(kRBStages);
+                    b.next(a.rbst);
                 }
             }
-            for (int t = 0; t < kRBStages; ++t)
+            for (int t = 0; t < a.rbst; ++t)
                 if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
         }
+    } else if (warp == 1) {
+        if (gather) reg_gather<EPI>(a, lane, b_ring, bfull, bempty, n_items, ks);
     } else {
         reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty);
     }
@@ -1255,12 +1338,21 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.k = c.top_k;
     a.acc = p.acc;
     a.err = p.err;
+    const RegRings rr = T <= 16 ? kRegSmall : kRegLarge;   // T <= 16: every tile has at most 16 rows
+    a.rcst = rr.cst;
+    a.rbst = rr.bst;
+    a.rbslot = rr.bslot;
+    const size_t rsmem = reg_smem(rr);
     bool ok = true;
     if (part == 0) {
-        k_permute_f16<<<p.num_sms * 4, 256, 0, st>>>(static_cast<const uint16_t *>(x), p.pad_pair, p.poff, p.scratch,
-                                                     E, H, a.P, c.top_k, p.xp16);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        if (warp_mma) {
+            a.x = static_cast<const uint16_t *>(x);   // the gate/up launch gathers its token rows itself
+        } else {
+            k_permute_f16<<<p.num_sms * 4, 256, 0, st>>>(static_cast<const uint16_t *>(x), p.pad_pair, p.poff,
+                                                         p.scratch, E, H, a.P, c.top_k, p.xp16);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
         ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
         ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
         ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
@@ -1278,7 +1370,7 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
         if (warp_mma)
-            k_gemm_reg<kSwiGLU><<<p.num_sms, kRThreads, kRSmemBytes, st>>>(a);
+            k_gemm_reg<kSwiGLU><<<p.num_sms, kRThreads, rsmem, st>>>(a);
         else
             k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
         return cudaGetLastError();
@@ -1300,7 +1392,7 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
     if (warp_mma)
-        k_gemm_reg<kScatter><<<p.num_sms, kRThreads, kRSmemBytes, st>>>(a);
+        k_gemm_reg<kScatter><<<p.num_sms, kRThreads, rsmem, st>>>(a);
     else
         k_gemm_f16<kScatter><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
     return cudaGetLastError();
