@@ -164,11 +164,7 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     Plan &p = plan->p;
     cudaError_t e = cudaMemsetAsync(p.scratch, 0, scratch_bytes(p), st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    {
-        Stage s(plan, MOE_STAGE_ROUTE, st);
-        if (s.done(moe::launch_router(p, x, T, rw, bias, p.ids, p.wts, st), moe::router_launches(T)) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    }
+
     // engine: CUDA-core streaming kernels, tcgen05 grouped GEMMs, or (W4A16)
     // warp-level MMAs fed from registers; AUTO takes the warp MMAs when the
     // batch leaves fewer than two rows an expert on average (decode)
@@ -181,7 +177,15 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     // rows a tensor-core tile covers: 32 for the warp MMAs, 64 for the W4A16
     // tcgen05 GEMMs, 128 for the W4A4 ones
     p.tile_rows = p.cfg.mode == MOE_W4A4 ? moe::kTileRows : (wm ? 32 : 64);
+    // decode-sized batches: the router's last block also groups the pairs
+    const bool fused_group = moe::router_groups(T);
     {
+        Stage s(plan, MOE_STAGE_ROUTE, st);
+        if (s.done(moe::launch_router(p, x, T, rw, bias, p.ids, p.wts, st, fused_group), moe::router_launches(T)) !=
+            cudaSuccess)
+            return MOE_ERR_CUDA;
+    }
+    if (!fused_group) {
         Stage s(plan, MOE_STAGE_GROUP, st);
         if (s.done(moe::launch_group(p, T, p.ids, nullptr, nullptr, true, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
     }

@@ -510,11 +510,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 // 16 << class and a B stage holds (8 >> class) boxes of 64 K values.
 __device__ __forceinline__ int hrows_class(int valid) { return valid <= 16 ? 0 : (valid <= 32 ? 1 : 2); }
 
-// Item = (tile * nf + f) * ks + kh: the tile's token rows against weight-row
-// group f, part kh of K (down items only are split).  For many tokens the
-// down items run column group first, (kh * nf + f) * n_tiles + tile, so the
-// accumulator slice being added into stays in L2 (see decode_item).  Returns
-// false for a group past the expert's intermediate size or an empty part of K.
+// Item = kh * (n_tiles * nf) + tile * nf + f: the tile's token rows against
+// weight-row group f, part kh of K when the caller splits K (ks parts; the
+// kernels here use ks = 1: a split of the down items measured slower at
+// decode).  For many tokens the down items run column group first,
+// (kh * nf + f) * n_tiles + tile, so the accumulator slice being added into
+// stays in L2 (see decode_item).  Returns false for a group past the expert's
+// intermediate size or an empty part of K.
 __device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi, int ks, Item &it) {
     const int nt = a.scratch->n_tiles;
     int tile, kh = 0;
@@ -524,9 +526,10 @@ __device__ __forceinline__ bool decode_item_h(const HcArgs &a, int item, int epi
         it.f = rest % a.nf;
         kh = rest / a.nf;
     } else {
-        kh = item % ks;
-        tile = (item / ks) / a.nf;
-        it.f = (item / ks) % a.nf;
+        const int per = nt * a.nf;
+        kh = item / per;
+        tile = (item % per) / a.nf;
+        it.f = (item % per) % a.nf;
     }
     const int4 t = a.tiles[tile];
     it.e = t.x;
@@ -863,9 +866,10 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
 constexpr int kRThreads = 32 * (2 + 16);          // TMA producer, token-row gatherer, 16 compute warps
 constexpr int kRXchg = 8 * 4 * 32 * 4 * 4;        // 16 KB: up-operand accumulators handed to the gate warps
 // Ring geometry a launch picks: with at most 16 tokens every tile has at most
-// 16 rows, so token-row slots of 8 KB leave room for a fifth weight stage.
+// 16 rows and token-row slots of 8 KB suffice (a fifth weight stage in the
+// room this frees measured no faster).
 struct RegRings { int cst, bst, bslot; };
-constexpr RegRings kRegSmall{5, 3, 16 * 512}, kRegLarge{4, 3, 32 * 512};
+constexpr RegRings kRegSmall{4, 3, 16 * 512}, kRegLarge{4, 3, 32 * 512};
 constexpr size_t reg_smem(RegRings r) {
     return (size_t)r.cst * kHCodeStage + (size_t)r.bst * r.bslot + kRXchg + 512 + 1024;
 }
@@ -936,7 +940,7 @@ template <int EPI>
 __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
                                             float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
                                             uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
-    const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
+    const int ks = 1;
     const int n_items = a.scratch->n_tiles * a.nf * ks;
     const int cw = warp - 2, rg = cw & 7, op = cw >> 3;
     const int g = lane >> 2, q = lane & 3;
@@ -950,6 +954,24 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
         Item it;
         if (!decode_item_h(a, item, EPI, ks, it)) continue;
         const int nt_n = (it.valid + 7) >> 3;
+        // epilogue inputs, loaded now so their latency hides behind the K loop:
+        // tensor scales, and the (token, weight) of this lane's first two columns
+        const int m = it.sh ? 1 : 0;
+        const int e = it.sh ? 0 : it.e;
+        const float ts0 = a.ts_a0[m][e], ts1 = EPI == kSwiGLU ? a.ts_a1[m][e] : 0.0f;
+        int tk[2] = {0, 0};
+        float wt[2] = {0.0f, 0.0f};
+        if (EPI == kScatter) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int n = 2 * q + c;
+                if (n < it.valid) {
+                    const int pair = a.pad_pair[it.row0 + n];
+                    tk[c] = pair >= a.P ? pair - a.P : pair / a.k;
+                    wt[c] = pair >= a.P ? 1.0f : a.wts[pair];
+                }
+            }
+        }
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -970,8 +992,6 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             bs.next(a.rbst);
         }
         if (!ok) break;
-        const int m = it.sh ? 1 : 0;
-        const int e = it.sh ? 0 : it.e;
         if (EPI == kSwiGLU) {
             float *slot = xchg + (size_t)rg * (4 * 32 * 4);
             if (op == 1) {   // up warp: hand the accumulators to the gate warp of the same rows
@@ -985,7 +1005,7 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
                 if (lane == 0) mbar_arrive(xfull + rg);
             } else {
                 if (!mbar_wait(xfull + rg, xph, a.err)) { ok = false; break; }
-                const float sg = a.ts_a0[m][e] * xunscale, su = a.ts_a1[m][e] * xunscale;
+                const float sg = ts0 * xunscale, su = ts1 * xunscale;
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     if (nt >= nt_n) break;
@@ -1009,7 +1029,7 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             }
             xph ^= 1;
         } else {
-            const float ds = a.ts_a0[m][e];
+            const float ds = ts0;
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 if (nt >= nt_n) break;
@@ -1017,9 +1037,16 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
                 for (int i = 0; i < 4; ++i) {
                     const int n = nt * 8 + 2 * q + (i & 1);
                     if (n < it.valid) {
-                        const int pair = a.pad_pair[it.row0 + n];
-                        const int t = pair >= a.P ? pair - a.P : pair / a.k;
-                        const float wv = (pair >= a.P ? 1.0f : a.wts[pair]) * ds;
+                        int t;
+                        float wv;
+                        if (nt == 0) {
+                            t = tk[i & 1];
+                            wv = wt[i & 1] * ds;
+                        } else {
+                            const int pair = a.pad_pair[it.row0 + n];
+                            t = pair >= a.P ? pair - a.P : pair / a.k;
+                            wv = (pair >= a.P ? 1.0f : a.wts[pair]) * ds;
+                        }
                         const int j = it.f * 256 + op * 128 + rg * 16 + g + (i >> 1) * 8;
                         atomicAdd(a.acc + (size_t)t * a.H + j, acc[nt][i] * wv);
                     }
@@ -1116,7 +1143,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
     uint64_t *xempty = xfull + 8;                // [8] and read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ks = 1;   // K is not split: a split of the down items measured slower (more atomics on the same outputs)
+    const int ks = 1;
     const int n_items = a.scratch->n_tiles * a.nf * ks;
     const bool gather = EPI == kSwiGLU && a.x != nullptr;
     if (threadIdx.x == 0) {

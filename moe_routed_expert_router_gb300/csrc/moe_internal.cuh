@@ -251,8 +251,9 @@ struct ExpertPtrs {
 };
 
 int router_launches(int T);
+bool router_groups(int T);
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias,
-                          int32_t *ids, float *wts, cudaStream_t st);
+                          int32_t *ids, float *wts, cudaStream_t st, bool with_group = false);
 cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out,
                          int32_t *sorted_out, bool build_work, cudaStream_t st);
 cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes, uint8_t *scales,

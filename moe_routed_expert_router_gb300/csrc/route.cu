@@ -252,28 +252,151 @@ __global__ void __launch_bounds__(128) k_router_topk(const float *__restrict__ l
     topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
 }
 
+// Outputs of the grouping step when it runs inside the decode router.
+struct GroupArgs {
+    int active;
+    int32_t *offsets, *poff, *sorted, *inv, *pad_pair;
+    int4 *chunks, *tiles;
+    int rows_cap, tile_rows, has_shared;
+};
+
+__host__ __device__ __forceinline__ size_t group_small_smem(int E, int P) {
+    return sizeof(int) * (5 * (size_t)(E + 2) + (size_t)P);
+}
+
+// Grouping of at most 512 pairs by one block (the decode router's last
+// block): the same outputs as k_group (offsets, padded offsets, the stable
+// order, the padded row map, work lists).  Counts come from the block's own
+// top-k ids; warp 0 places the pairs 32 at a time in increasing order, so
+// the order inside an expert is increasing p.
+__device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids, int P, int E, int T, int *sm,
+                            CallScratch *sc, int *err) {
+    int *s_cnt = sm, *s_off = s_cnt + (E + 2), *s_poff = s_off + (E + 2), *s_cb = s_poff + (E + 2),
+        *s_tb = s_cb + (E + 2), *s_ids = s_tb + (E + 2);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    for (int i = tid; i < E; i += nthr) s_cnt[i] = 0;
+    __syncthreads();
+    for (int q = tid; q < P; q += nthr) {
+        int e = ids[q];
+        if (e < 0 || e >= E) { atomicOr(err, kErrDevice); e = -1; }
+        s_ids[q] = e;
+        if (e >= 0) atomicAdd(&s_cnt[e], 1);
+    }
+    __syncthreads();
+    if (warp == 0) {   // exclusive scans of (count, padded count, chunks, tiles), 32 experts at a time
+        int ra = 0, rb = 0, rd = 0, rf = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = e < E ? s_cnt[e] : 0;
+            const int pc = (c + kTileRows - 1) / kTileRows * kTileRows, nc = (c + kChunkRows - 1) / kChunkRows,
+                      nt = (c + g.tile_rows - 1) / g.tile_rows;
+            int a = c, b = pc, d = nc, f = nt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o),
+                          yd = __shfl_up_sync(0xffffffffu, d, o), yf = __shfl_up_sync(0xffffffffu, f, o);
+                if (lane >= o) { a += ya; b += yb; d += yd; f += yf; }
+            }
+            if (e < E) {
+                s_off[e] = ra + a - c;
+                s_poff[e] = rb + b - pc;
+                s_cb[e] = rd + d - nc;
+                s_tb[e] = rf + f - nt;
+            }
+            ra += __shfl_sync(0xffffffffu, a, 31);
+            rb += __shfl_sync(0xffffffffu, b, 31);
+            rd += __shfl_sync(0xffffffffu, d, 31);
+            rf += __shfl_sync(0xffffffffu, f, 31);
+        }
+        if (lane == 0) {
+            s_off[E] = ra;
+            s_poff[E] = rb;
+            s_poff[E + 1] = rb + (g.has_shared ? (T + kTileRows - 1) / kTileRows * kTileRows : 0);
+            s_cb[E] = rd;
+            s_cb[E + 1] = rd + (g.has_shared ? (T + kChunkRows - 1) / kChunkRows : 0);
+            s_tb[E] = rf;
+            s_tb[E + 1] = rf + (g.has_shared ? (T + g.tile_rows - 1) / g.tile_rows : 0);
+            if (ra != P) atomicOr(err, kErrDevice);
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i <= E; i += nthr) g.offsets[i] = s_off[i];
+    for (int i = tid; i <= E + 1; i += nthr) g.poff[i] = s_poff[i];
+    if (s_poff[E + 1] > g.rows_cap) {   // inconsistent counts: refuse, never write out of range
+        if (tid == 0) atomicOr(err, kErrDevice);
+        return;
+    }
+    for (int i = tid; i < E; i += nthr) s_cnt[i] = s_off[i];   // running position of each expert
+    __syncthreads();
+    if (warp == 0) {
+        for (int base = 0; base < P; base += 32) {
+            const int q = base + lane;
+            int e = q < P ? s_ids[q] : -1;
+            if (e < 0) e = -1 - lane;
+            const unsigned peers = __match_any_sync(0xffffffffu, e);
+            int pos = 0;
+            if (e >= 0) pos = s_cnt[e] + __popc(peers & ((1u << lane) - 1u));
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[e] += __popc(peers);
+            __syncwarp();
+            if (e >= 0) {
+                const int prow = s_poff[e] + (pos - s_off[e]);
+                if (pos >= P || prow >= g.rows_cap) {
+                    atomicOr(err, kErrDevice);
+                } else {
+                    g.sorted[pos] = q;
+                    g.inv[q] = prow;
+                    g.pad_pair[prow] = q;
+                }
+            }
+        }
+    }
+    for (int e = warp; e < E; e += nwarps) {   // padding rows
+        const int cnt = s_off[e + 1] - s_off[e], pend = s_poff[e + 1] - s_poff[e];
+        for (int q = cnt + lane; q < pend; q += 32) g.pad_pair[s_poff[e] + q] = -1;
+    }
+    if (g.has_shared) {
+        const int sh_rows = s_poff[E + 1] - s_poff[E];
+        for (int q = tid; q < sh_rows; q += nthr) g.pad_pair[s_poff[E] + q] = (q < T) ? P + q : -1;
+    }
+    for (int e = warp; e <= E; e += nwarps) {   // work lists, one warp an expert
+        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (g.has_shared ? T : 0);
+        const int cb = s_cb[e], tb = s_tb[e];
+        for (int q = lane; q * kChunkRows < cnt; q += 32)
+            g.chunks[cb + q] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
+        for (int q = lane; q * g.tile_rows < cnt; q += 32)
+            g.tiles[tb + q] = make_int4(e, s_poff[e] + q * g.tile_rows, min(g.tile_rows, cnt - q * g.tile_rows), 0);
+    }
+    if (tid == 0) {
+        sc->n_tiles = s_tb[E + 1];
+        sc->n_chunks = s_cb[E + 1];
+        sc->n_chunks_routed = s_cb[E];
+    }
+}
+
 // Decode-sized batches (T <= 16), router and top-k in one launch: block e
 // computes expert e's logit for every token.  The router row (H fp32) is
 // staged in shared memory once; warp t streams token t's x row through its own
 // 4-deep cp.async ring of 1024-position slabs (512 for T > 8, so two blocks
 // fit an SM; the last slab ragged; 16-byte copies, no block barrier), lane l
-// taking positions 32j + l in increasing j.  Each
-// block also checks a 1/E slice of x (non-finite values, amax).  The last
-// block to finish (a ticket in the per-call scratch) runs the top-k for all
-// tokens, one warp a token.
+// taking positions 32j + l in increasing j.  Each block also checks a 1/E
+// slice of x (non-finite values, amax).  The last block to finish (a ticket in
+// the per-call scratch) runs the top-k for all tokens, one warp a token, and,
+// in moe_forward, groups the pairs (group_small).
 constexpr int kDecodeRouterThreads = 512;
 constexpr int kDSlab = 1024, kDStages = 4;
 
 __host__ __device__ __forceinline__ int decode_slab(int T) { return T <= 8 ? kDSlab : kDSlab / 2; }
 
-size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * decode_slab(T) * 2; }
+__host__ __device__ __forceinline__ size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * decode_slab(T) * 2; }
 
 template <int NPL>
 __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     const uint16_t *__restrict__ x, int T, int H, const float *__restrict__ rw, const float *__restrict__ bias,
     int E, int k, int kind, int renorm, float *__restrict__ logits, int32_t *__restrict__ ids,
-    float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err) {
-    extern __shared__ __align__(16) float wrow[];     // [H], then per-token x rings [T][kDStages][kDSlab] bf16
+    float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err, GroupArgs grp) {
+    extern __shared__ __align__(16) float wrow[];     // [H], per-token x rings [T][kDStages][slab] bf16, grouping
     __shared__ float s_amax[kDecodeRouterThreads / 32];
     __shared__ int s_bad[kDecodeRouterThreads / 32];
     __shared__ int s_last;
@@ -367,6 +490,11 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     __threadfence();
     for (int t = warp; t < T; t += kDecodeRouterThreads / 32)
         topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
+    if (grp.active) {
+        __syncthreads();   // the block's ids are visible to all its threads
+        int *gsm = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(wrow) + decode_router_smem(H, T));
+        group_small(grp, ids, T * k, E, T, gsm, sc, err);
+    }
 }
 
 // Single-block grouping (1024 threads).  Stable counting sort of the pairs
@@ -529,16 +657,21 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
 }  // namespace
 
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias, int32_t *ids,
-                          float *wts, cudaStream_t st) {
+                          float *wts, cudaStream_t st, bool with_group) {
     const int H = p.cfg.hidden, E = p.cfg.num_experts, k = p.cfg.top_k;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     const int npl = (E + 31) / 32;
     if (T <= kDecodeRouterThreads / 32 && H % 256 == 0) {
-        const size_t smem = decode_router_smem(H, T);
+        GroupArgs grp{};
+        if (with_group) {
+            grp = GroupArgs{1, p.offsets, p.poff, p.sorted, p.inv, p.pad_pair, p.chunks, p.tiles,
+                            (int)p.rows_pad_max, p.tile_rows, p.cfg.has_shared};
+        }
+        const size_t smem = decode_router_smem(H, T) + (with_group ? group_small_smem(E, T * k) : 0);
 #define MOE_DEC(N)                                                                                           \
     k_router_decode<N><<<E, kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router,          \
                                                               p.cfg.renormalize, p.logits, ids, wts, p.counts, \
-                                                              p.scratch, p.err)
+                                                              p.scratch, p.err, grp)
         if (npl <= 1) MOE_DEC(1);
         else if (npl <= 2) MOE_DEC(2);
         else if (npl <= 4) MOE_DEC(4);
@@ -568,12 +701,16 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
 // Kernels launch_router issues for T tokens (hidden is always a multiple of 256).
 int router_launches(int T) { return T <= kDecodeRouterThreads / 32 ? 1 : 2; }
 
+// Whether launch_router(..., with_group = true) also groups the pairs.
+bool router_groups(int T) { return T <= kDecodeRouterThreads / 32; }
+
 size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (size_t)E + 8); }
 
 cudaError_t configure_group_kernel(int E) {
     cudaError_t e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
     if (e != cudaSuccess) return e;
-    const int dec = (int)decode_router_smem(8192, kDecodeRouterThreads / 32);
+    const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32) +
+                          group_small_smem(kMaxExperts, kDecodeRouterThreads / 32 * kMaxTopK));
     for (auto f : {k_router_decode<1>, k_router_decode<2>, k_router_decode<4>, k_router_decode<8>,
                    k_router_decode<16>, k_router_decode<32>}) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
