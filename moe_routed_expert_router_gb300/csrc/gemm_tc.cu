@@ -866,10 +866,10 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
 constexpr int kRThreads = 32 * (2 + 16);          // TMA producer, token-row gatherer, 16 compute warps
 constexpr int kRXchg = 8 * 4 * 32 * 4 * 4;        // 16 KB: up-operand accumulators handed to the gate warps
 // Ring geometry a launch picks: with at most 16 tokens every tile has at most
-// 16 rows and token-row slots of 8 KB suffice (a fifth weight stage in the
-// room this frees measured no faster).
+// 16 rows, token-row slots of 8 KB suffice and the token-row ring gets a
+// fourth stage (a fifth weight stage measured no faster).
 struct RegRings { int cst, bst, bslot; };
-constexpr RegRings kRegSmall{4, 3, 16 * 512}, kRegLarge{4, 3, 32 * 512};
+constexpr RegRings kRegSmall{4, 4, 16 * 512}, kRegLarge{4, 3, 32 * 512};
 constexpr size_t reg_smem(RegRings r) {
     return (size_t)r.cst * kHCodeStage + (size_t)r.bst * r.bslot + kRXchg + 512 + 1024;
 }
@@ -891,15 +891,15 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
     const uint4 sv0 = lds128(st + 2 * kHCodeTile + op * 2048 + r0 * 16);
     const uint4 sv1 = lds128(st + 2 * kHCodeTile + op * 2048 + r1 * 16);
     const uint32_t sw0[4] = {sv0.x, sv0.y, sv0.z, sv0.w}, sw1[4] = {sv1.x, sv1.y, sv1.z, sv1.w};
+    const uint32_t ssel = (uint32_t)q | ((uint32_t)(4 + q) << 4);   // byte q of the r0 word, then of the r1 word
 #pragma unroll
     for (int sb = 0; sb < 4; ++sb) {
         const uint32_t ch = (uint32_t)(2 * sb + (q >> 1));
         uint2 c0, c1;
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c0.x), "=r"(c0.y) : "r"(crow0 + ((ch ^ (uint32_t)(r0 & 7)) << 4) + (q & 1) * 8) : "memory");
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c1.x), "=r"(c1.y) : "r"(crow1 + ((ch ^ (uint32_t)(r1 & 7)) << 4) + (q & 1) * 8) : "memory");
-        // scale bytes of block 4 sb + q for rows r0 (low) and r1 (high)
-        const uint32_t s2 = ((sw0[sb] >> (8 * q)) & 0xFFu) | (((sw1[sb] >> (8 * q)) & 0xFFu) << 8);
-        const uint32_t sc = e4m3x2_to_f16x2(s2);
+        // scale bytes of block 4 sb + q for rows r0 (low byte) and r1 (next byte)
+        const uint32_t sc = e4m3x2_to_f16x2(__byte_perm(sw0[sb], sw1[sb], ssel));
         __half2 sc0 = __low2half2(*reinterpret_cast<const __half2 *>(&sc));
         __half2 sc1 = __high2half2(*reinterpret_cast<const __half2 *>(&sc));
         uint32_t h0[8], h1[8];
