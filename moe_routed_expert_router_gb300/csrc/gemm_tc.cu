@@ -159,6 +159,8 @@ __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, 
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
+    pdl_wait();      // routing, permute or gate/up results come from the previous kernel
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
@@ -565,6 +567,8 @@ struct RingPos {
 
 template <int EPI>
 __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant__ HcArgs a) {
+    pdl_wait();      // routing, permute or gate/up results come from the previous kernel
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *code_ring = smem;
@@ -1130,6 +1134,8 @@ __device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b
 
 template <int EPI>
 __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
+    pdl_wait();      // routing, permute or gate/up results come from the previous kernel
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *code_ring = smem;
@@ -1396,10 +1402,12 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         a.ts_a0[1] = sp.gts;
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
+        cudaError_t e0;
         if (warp_mma)
-            k_gemm_reg<kSwiGLU><<<p.num_sms, kRThreads, rsmem, st>>>(a);
+            e0 = launch_pdl(k_gemm_reg<kSwiGLU>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
         else
-            k_gemm_f16<kSwiGLU><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+            e0 = launch_pdl(k_gemm_f16<kSwiGLU>, dim3(p.num_sms), dim3(kHThreads), kHSmemBytes, st, a);
+        if (e0 != cudaSuccess) return e0;
         return cudaGetLastError();
     }
     ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
@@ -1418,10 +1426,12 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.ts_a1[0] = r.dts;
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
+    cudaError_t e0;
     if (warp_mma)
-        k_gemm_reg<kScatter><<<p.num_sms, kRThreads, rsmem, st>>>(a);
+        e0 = launch_pdl(k_gemm_reg<kScatter>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
     else
-        k_gemm_f16<kScatter><<<p.num_sms, kHThreads, kHSmemBytes, st>>>(a);
+        e0 = launch_pdl(k_gemm_f16<kScatter>, dim3(p.num_sms), dim3(kHThreads), kHSmemBytes, st, a);
+    if (e0 != cudaSuccess) return e0;
     return cudaGetLastError();
 }
 
@@ -1479,7 +1489,8 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
         a.ts_a0[1] = sp.gts;
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
-        k_gemm_fp4<kSwiGLU><<<p.num_sms, kThreads, kSmemBytes, st>>>(a);
+        cudaError_t e0 = launch_pdl(k_gemm_fp4<kSwiGLU>, dim3(p.num_sms), dim3(kThreads), kSmemBytes, st, a);
+        if (e0 != cudaSuccess) return e0;
         return cudaGetLastError();
     }
     ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
@@ -1499,7 +1510,8 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
     a.ts_a1[0] = r.dts;
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
-    k_gemm_fp4<kScatter><<<p.num_sms, kThreads, kSmemBytes, st>>>(a);
+    cudaError_t e0 = launch_pdl(k_gemm_fp4<kScatter>, dim3(p.num_sms), dim3(kThreads), kSmemBytes, st, a);
+    if (e0 != cudaSuccess) return e0;
     return cudaGetLastError();
 }
 

@@ -237,6 +237,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *e
     return true;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may start
+// while the previous kernel in the stream is finishing; it calls pdl_wait()
+// before it reads anything that kernel wrote (the wait returns once that
+// kernel has completed and its writes are visible; without the launch
+// attribute it returns at once), then pdl_trigger() so that the next kernel's
+// launch can overlap this one in turn.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void bulk_copy(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -266,5 +275,20 @@ cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtr
 cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st);
 cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st);
 cudaError_t launch_wait_check(int *err, uint64_t limit_ns, cudaStream_t st);
+
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace moe

@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kThreads) k_quant_h(const float *__restrict__ 
 
 // out = bf16_rne(acc); acc = 0 (so the next call starts from zero).
 __global__ void __launch_bounds__(kThreads) k_finalize(float4 *__restrict__ acc, uint2 *__restrict__ out, int64_t n4) {
+    pdl_wait();      // the down GEMM's scatter-adds are complete
+    pdl_trigger();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n4; i += (int64_t)gridDim.x * blockDim.x) {
         float4 v = acc[i];
         __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
@@ -235,9 +237,8 @@ cudaError_t launch_wait_check(int *err, uint64_t limit_ns, cudaStream_t st) {
 
 cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st) {
     const int64_t n4 = (int64_t)T * p.cfg.hidden / 4;
-    k_finalize<<<grid_for(n4, p.num_sms), kThreads, 0, st>>>(reinterpret_cast<float4 *>(p.acc),
-                                                             static_cast<uint2 *>(out), n4);
-    return cudaGetLastError();
+    return launch_pdl(k_finalize, dim3(grid_for(n4, p.num_sms)), dim3(kThreads), 0, st, reinterpret_cast<float4 *>(p.acc),
+                      static_cast<uint2 *>(out), n4);
 }
 
 }  // namespace moe
