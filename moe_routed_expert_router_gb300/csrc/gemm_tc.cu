@@ -38,6 +38,8 @@ constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
 constexpr int kStageBytes = 3 * kTile + 3 * kSf;   // A0, A1, B codes; A0, A1 scales (re-laid in place); B scales
 constexpr int kEpiWarps = 8;                      // two per 32-lane TMEM quadrant
+constexpr uint32_t kSfCol0 = 256;                 // scale-factor TMEM columns: 48 a stage slot after the accumulators
+static_assert(kSfCol0 + kStages * 48 <= 512, "FP4 TMEM plan exceeds 512 columns");
 constexpr int kThreads = 32 * (3 + kEpiWarps);    // producer, MMA, scale re-layout, epilogue
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
@@ -290,22 +292,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                 for (int ks = 0; ks < ks_n; ++ks) {
                     if (!mbar_wait(sf_ready + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
                     tc_fence_after();
+                    // descriptors of the stage's operands: built once, then stepped by
+                    // their 16-byte address units (the smem window is below 256 KB, so
+                    // adding to the start-address field never carries out of it)
                     const uint32_t base = smem_u32(smem + s * kStageBytes);
-                    const uint32_t at0 = base + 3 * kTile, at1 = at0 + kSf, atb = at0 + 2 * kSf;
+                    const uint64_t dA = desc_sw128(base), dS = desc_sf(base + 3 * kTile);
+                    // scale factors of this stage slot: their own 48 TMEM columns
+                    // (A0, A1, B x 4 K chunks), so copying the next stage's scales never
+                    // has to wait for this stage's MMAs to read theirs
+                    const uint32_t sf = tmem + kSfCol0 + s * 48;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        sf_copy(tmem + 256 + 4 * kk, desc_sf(at0 + 512 * kk));
-                        sf_copy(tmem + 272 + 4 * kk, desc_sf(at1 + 512 * kk));
-                        sf_copy(tmem + 288 + 4 * kk, desc_sf(atb + 512 * kk));
+                        sf_copy(sf + 4 * kk, dS + 32 * kk);
+                        sf_copy(sf + 16 + 4 * kk, dS + (kSf >> 4) + 32 * kk);
+                        sf_copy(sf + 32 + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks | kk) ? 1u : 0u;
-                        const uint64_t bd = desc_sw128(base + 2 * kTile + 32 * kk);
-                        mma_fp4(d0, desc_sw128(base + 32 * kk), bd, idesc, tmem + 256 + 4 * kk, tmem + 288 + 4 * kk,
-                                accum);
-                        mma_fp4(d1, desc_sw128(base + kTile + 32 * kk), bd, idesc, tmem + 272 + 4 * kk,
-                                tmem + 288 + 4 * kk, accum);
+                        const uint64_t bd = dA + (2 * kTile >> 4) + 2 * kk;
+                        mma_fp4(d0, dA + 2 * kk, bd, idesc, sf + 4 * kk, sf + 32 + 4 * kk, accum);
+                        mma_fp4(d1, dA + (kTile >> 4) + 2 * kk, bd, idesc, sf + 16 + 4 * kk, sf + 32 + 4 * kk, accum);
                     }
                     mma_commit(empty + s);
                     if (++s == kStages) { s = 0; ph ^= 1; }
