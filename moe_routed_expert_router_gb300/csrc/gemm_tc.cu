@@ -15,11 +15,19 @@
 // rows): gate+up (two 128-row MMAs sharing B, SwiGLU epilogue) or down (two
 // 128-row MMAs, weighted scatter-add epilogue).
 //
-// Warp roles (192 threads, one CTA per SM, persistent over the items):
+// Warp roles (one CTA per SM, persistent over the items):
 //   warp 0   TMA producer (one lane)
-//   warp 1   TMEM owner; re-lays the weight scale tiles into the tensor-core
-//            scale-factor layout, then one lane issues tcgen05.cp + tcgen05.mma
-//   warps 2-5 epilogue (tcgen05.ld of their 32-lane quadrant of the accumulators)
+//   warp 1   TMEM owner; one lane issues tcgen05.mma
+//   scale warps, which put the stage's E4M3 scale factors into tensor memory:
+//     gate/up: warps 2-5, each writing its own 32-lane quadrant with tcgen05.st,
+//              so the tensor pipe spends no time on scales (448 threads);
+//     down:    warp 2, which re-lays the weight scale tiles in shared memory into
+//              512-byte atoms that the MMA lane copies with tcgen05.cp (352
+//              threads). The down epilogue keeps 128 accumulator values a thread
+//              in registers and needs the 168 registers a thread that an 11-warp
+//              block allows; at 14 warps it would spill.
+//   the last 8 warps: epilogue (tcgen05.ld of their 32-lane quadrant of the
+//              accumulators)
 // Every mbarrier wait is bounded (about one second); on expiry the kernel sets
 // the plan's timeout bit and every role leaves its loop.
 #include <cuda.h>
@@ -36,13 +44,17 @@ constexpr int kBK = 256;                  // K values per pipeline stage
 constexpr int kRowBytes = kBK / 2;        // 128 code bytes per row per stage
 constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
-constexpr int kStageBytes = 3 * kTile + 3 * kSf;   // A0, A1, B codes; A0, A1 scales (re-laid in place); B scales
+constexpr int kStageBytes = 3 * kTile + 3 * kSf;   // A0, A1, B codes; A0, A1 scales (plain rows); B scales (atoms)
 constexpr int kEpiWarps = 8;                      // two per 32-lane TMEM quadrant
 constexpr uint32_t kSfCol0 = 256;                 // scale-factor TMEM columns: 48 a stage slot after the accumulators
 static_assert(kSfCol0 + kStages * 48 <= 512, "FP4 TMEM plan exceeds 512 columns");
-constexpr int kThreads = 32 * (3 + kEpiWarps);    // producer, MMA, scale re-layout, epilogue
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
+
+// Scale warps: four tcgen05.st writers (gate/up) or one shared-memory re-layout warp (down).
+__host__ __device__ constexpr int scale_warps(int epi) { return epi == kSwiGLU ? 4 : 1; }
+__host__ __device__ constexpr int epi_warp0(int epi) { return 2 + scale_warps(epi); }
+__host__ __device__ constexpr int fp4_threads(int epi) { return 32 * (epi_warp0(epi) + kEpiWarps); }
 
 struct TcArgs {
     CUtensorMap a0[2];      // [routed, shared]: gate codes (G1) / down codes (G2)
@@ -120,6 +132,15 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// 32 lanes x 16 columns from v[0..15] (each thread: its lane).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 // 32 lanes x 16 columns of fp32 into v[0..15] (each thread: its lane); the
 // caller waits with tcgen05.wait::ld before reading v.
 __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float *v) {
@@ -160,7 +181,8 @@ __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, 
 }
 
 template <int EPI>
-__global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
+__global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
+    constexpr int kScaleWarps = scale_warps(EPI), kEpiWarp0 = epi_warp0(EPI);
     pdl_wait();      // routing, permute or gate/up results come from the previous kernel
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
@@ -179,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(sf_ready + s, 1);
+            mbar_init(sf_ready + s, kScaleWarps);
             mbar_init(empty + s, 1);
         }
         mbar_init(acc_full, 1);
@@ -239,41 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             for (int t = 0; t < kStages; ++t)
                 if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------ weight scale re-layout
-        // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each: the 4
-        // scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
-        int s = 0;
-        uint32_t ph = 0;
-        for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-            Item it;
-            if (!decode_item(a, item, EPI, it)) continue;
-            const int ks_n = it.K / kBK;
-            bool ok = true;
-            for (int ks = 0; ks < ks_n; ++ks) {
-                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
-                uint8_t *st = smem + s * kStageBytes;
-#pragma unroll
-                for (int op = 0; op < 2; ++op) {
-                    // in place: every lane reads its 4 rows, then (after the warp
-                    // has read everything) writes its 4 atom words
-                    const uint32_t tile = smem_u32(st + 3 * kTile + op * kSf);
-                    uint4 v[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) v[q] = lds128(tile + 16 * (lane + 32 * q));
-                    __syncwarp();
-                    sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
-                    sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
-                    sts128(tile + 16 * (2 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
-                    sts128(tile + 16 * (3 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sf_ready + s);
-                if (++s == kStages) { s = 0; ph ^= 1; }
-            }
-            if (!ok) break;
-        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issue (one lane)
         if (lane == 0) {
@@ -296,16 +283,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
                     // their 16-byte address units (the smem window is below 256 KB, so
                     // adding to the start-address field never carries out of it)
                     const uint32_t base = smem_u32(smem + s * kStageBytes);
-                    const uint64_t dA = desc_sw128(base), dS = desc_sf(base + 3 * kTile);
-                    // scale factors of this stage slot: their own 48 TMEM columns
-                    // (A0, A1, B x 4 K chunks), so copying the next stage's scales never
-                    // has to wait for this stage's MMAs to read theirs
+                    const uint64_t dA = desc_sw128(base);
+                    // scale factors of this stage slot: A0, A1, B at columns +0, +16,
+                    // +32, four per 64-value K chunk (gate/up: written by the scale
+                    // warps; down: copied here from the re-laid atoms)
                     const uint32_t sf = tmem + kSfCol0 + s * 48;
+                    if (EPI == kScatter) {
+                        const uint64_t dS = desc_sf(base + 3 * kTile);
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        sf_copy(sf + 4 * kk, dS + 32 * kk);
-                        sf_copy(sf + 16 + 4 * kk, dS + (kSf >> 4) + 32 * kk);
-                        sf_copy(sf + 32 + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            sf_copy(sf + 4 * kk, dS + 32 * kk);
+                            sf_copy(sf + 16 + 4 * kk, dS + (kSf >> 4) + 32 * kk);
+                            sf_copy(sf + 32 + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
+                        }
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
@@ -324,6 +314,101 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
             mma_commit(drain);
             mbar_wait(drain, 0, a.err);
         }
+    } else if (warp >= 2 && warp < kEpiWarp0 && EPI == kScatter) {
+        // ------------------------------------------------ weight scale re-layout (down)
+        // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each, in place:
+        // the 4 scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item(a, item, EPI, it)) continue;
+            const int ks_n = it.K / kBK;
+            for (int ks = 0; ks < ks_n; ++ks) {
+                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                uint8_t *st = smem + s * kStageBytes;
+#pragma unroll
+                for (int op = 0; op < 2; ++op) {
+                    // every lane reads its 4 rows, then (after the warp has read
+                    // everything) writes its 4 atom words
+                    const uint32_t tile = smem_u32(st + 3 * kTile + op * kSf);
+                    uint4 v[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) v[q] = lds128(tile + 16 * (lane + 32 * q));
+                    __syncwarp();
+                    sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
+                    sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
+                    sts128(tile + 16 * (2 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
+                    sts128(tile + 16 * (3 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sf_ready + s);
+                if (++s == kStages) { s = 0; ph ^= 1; }
+            }
+        }
+        mbar_wait(drain, 0, a.err);
+    } else if (warp >= 2 && warp < kEpiWarp0) {
+        // ------------------------------------------------ scale factors -> TMEM
+        // The MMA (scale_vec::4X, M = N = 128) finds the 4 scale bytes of row r
+        // for K chunk kk (64 values) in column 4 * kk + r / 32 of lane r % 32 of
+        // every 32-lane quadrant: the layout a 32x128b.warpx4 copy of a 512-byte
+        // atom gives. Each scale warp writes that layout into its own quadrant:
+        // lane l, column 16 * op + 4 * kk + j <- operand op's row l + 32 * j,
+        // chunk kk. A0 and A1 arrive as plain [128 rows][16 B] tiles (the word
+        // kk of row l + 32 j); B arrives as four atoms (word j of atom kk, row l).
+        // Stage slot s owns columns kSfCol0 + 48 s ..: they are free again once
+        // the slot's next TMA load has landed, because the producer reloads a
+        // slot only after the MMAs that read it have completed.
+        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol0;
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+            Item it;
+            if (!decode_item(a, item, EPI, it)) continue;
+            const int ks_n = it.K / kBK;
+            for (int ks = 0; ks < ks_n; ++ks) {
+                if (!mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sfb = smem_u32(smem + s * kStageBytes + 3 * kTile);
+                uint32_t o[16];
+#pragma unroll
+                for (int op = 0; op < 2; ++op) {
+                    uint4 v[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = lds128(sfb + op * kSf + 16 * (lane + 32 * j));
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        o[j] = v[j].x;
+                        o[4 + j] = v[j].y;
+                        o[8 + j] = v[j].z;
+                        o[12 + j] = v[j].w;
+                    }
+                    tmem_st16(t_lane + s * 48 + 16 * op, o);
+                }
+                {
+                    uint4 v[4];
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) v[kk] = lds128(sfb + 2 * kSf + 512 * kk + 16 * lane);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        o[4 * kk] = v[kk].x;
+                        o[4 * kk + 1] = v[kk].y;
+                        o[4 * kk + 2] = v[kk].z;
+                        o[4 * kk + 3] = v[kk].w;
+                    }
+                    tmem_st16(t_lane + s * 48 + 32, o);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sf_ready + s);
+                if (++s == kStages) { s = 0; ph ^= 1; }
+            }
+        }
+        mbar_wait(drain, 0, a.err);
     } else {
         // ------------------------------------------------ epilogue (8 warps)
         // Each warp copies its 32 lanes x 64 columns of both accumulators into
@@ -331,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_fp4(const __grid_constant_
         // does the arithmetic and the global writes, so the next item's MMAs
         // overlap them.
         const int quad = warp & 3;                 // TMEM lanes this warp may read
-        const int col0 = ((warp - 3) >> 2) * 64;   // its half of the token columns
+        const int col0 = ((warp - kEpiWarp0) >> 2) * 64;   // its half of the token columns
         uint32_t aph = 0;
         float lmax = 0.0f, lmax_s = 0.0f;
         for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
@@ -503,15 +588,6 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// 32 lanes x 16 columns from v[0..15] (each thread: its lane).
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-        ::"r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
-          "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
 }
 
@@ -1496,7 +1572,7 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
         a.ts_a0[1] = sp.gts;
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
-        cudaError_t e0 = launch_pdl(k_gemm_fp4<kSwiGLU>, dim3(p.num_sms), dim3(kThreads), kSmemBytes, st, a);
+        cudaError_t e0 = launch_pdl(k_gemm_fp4<kSwiGLU>, dim3(p.num_sms), dim3(fp4_threads(kSwiGLU)), kSmemBytes, st, a);
         if (e0 != cudaSuccess) return e0;
         return cudaGetLastError();
     }
@@ -1517,7 +1593,7 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
     a.ts_a1[0] = r.dts;
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e0 = launch_pdl(k_gemm_fp4<kScatter>, dim3(p.num_sms), dim3(kThreads), kSmemBytes, st, a);
+    cudaError_t e0 = launch_pdl(k_gemm_fp4<kScatter>, dim3(p.num_sms), dim3(fp4_threads(kScatter)), kSmemBytes, st, a);
     if (e0 != cudaSuccess) return e0;
     return cudaGetLastError();
 }
