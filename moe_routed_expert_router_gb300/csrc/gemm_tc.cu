@@ -351,17 +351,22 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
         mbar_wait(drain, 0, a.err);
     } else if (warp >= 2 && warp < kEpiWarp0) {
         // ------------------------------------------------ scale factors -> TMEM
-        // The MMA (scale_vec::4X, M = N = 128) finds the 4 scale bytes of row r
-        // for K chunk kk (64 values) in column 4 * kk + r / 32 of lane r % 32 of
-        // every 32-lane quadrant: the layout a 32x128b.warpx4 copy of a 512-byte
-        // atom gives. Each scale warp writes that layout into its own quadrant:
-        // lane l, column 16 * op + 4 * kk + j <- operand op's row l + 32 * j,
-        // chunk kk. A0 and A1 arrive as plain [128 rows][16 B] tiles (the word
-        // kk of row l + 32 j); B arrives as four atoms (word j of atom kk, row l).
+        // Scale-factor layout (scale_vec::4X, M = N = 128), 4 columns per K chunk
+        // kk of 64 values, as a 32x128b.warpx4 copy of a 512-byte atom lays it
+        // out: lane l of each 32-lane quadrant, column 4 * kk + j holds the 4
+        // scale bytes of row l + 32 * j.
+        //   A (weight rows): the MMA reads row r's scales only from its own lane
+        //     r (column 4 * kk + r / 32), so the warp of quadrant q loads just
+        //     rows 32 q + l (one 16-byte row: its 4 chunk words) and writes each
+        //     word to all four columns of its chunk.
+        //   B (token rows): every quadrant reads all 128 rows, so each warp
+        //     writes the full atoms (word j of atom kk, row l).
+        // A0 and A1 arrive as plain [128 rows][16 B] tiles, B as four atoms.
         // Stage slot s owns columns kSfCol0 + 48 s ..: they are free again once
         // the slot's next TMA load has landed, because the producer reloads a
         // slot only after the MMAs that read it have completed.
-        const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16) + kSfCol0;
+        const int quad = warp & 3;
+        const uint32_t t_lane = tmem + ((uint32_t)(quad * 32) << 16) + kSfCol0;
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -376,15 +381,13 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                 uint32_t o[16];
 #pragma unroll
                 for (int op = 0; op < 2; ++op) {
-                    uint4 v[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = lds128(sfb + op * kSf + 16 * (lane + 32 * j));
+                    const uint4 v = lds128(sfb + op * kSf + 16 * (lane + 32 * quad));
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        o[j] = v[j].x;
-                        o[4 + j] = v[j].y;
-                        o[8 + j] = v[j].z;
-                        o[12 + j] = v[j].w;
+                        o[j] = v.x;
+                        o[4 + j] = v.y;
+                        o[8 + j] = v.z;
+                        o[12 + j] = v.w;
                     }
                     tmem_st16(t_lane + s * 48 + 16 * op, o);
                 }
