@@ -90,6 +90,12 @@ struct Carver {
     }
 };
 
+// Per-call scratch, cleared at the start of every call: the call's counters,
+// the per-expert counts, and the arrival tickets of split gate/up items.
+size_t scratch_bytes(const Plan &p) {
+    return sizeof(moe::CallScratch) + sizeof(int32_t) * ((size_t)p.cfg.num_experts + 8 * (size_t)p.num_sms);
+}
+
 void carve(Plan &p, Carver &c) {
     const moe_config &k = p.cfg;
     const int64_t T = k.max_tokens, H = k.hidden, E = k.num_experts;
@@ -97,8 +103,9 @@ void carve(Plan &p, Carver &c) {
     p.logits = c.take<float>(sizeof(float) * T * E);
     p.ids = c.take<int32_t>(sizeof(int32_t) * p.pairs_max);
     p.wts = c.take<float>(sizeof(float) * p.pairs_max);
-    p.scratch = c.take<moe::CallScratch>(sizeof(moe::CallScratch) + sizeof(int32_t) * E);
+    p.scratch = c.take<moe::CallScratch>(scratch_bytes(p));
     p.counts = p.scratch ? reinterpret_cast<int32_t *>(p.scratch + 1) : nullptr;
+    p.tail_tickets = p.counts ? p.counts + E : nullptr;
     p.offsets = c.take<int32_t>(sizeof(int32_t) * (E + 2));
     p.poff = c.take<int32_t>(sizeof(int32_t) * (E + 2));
     p.sorted = c.take<int32_t>(sizeof(int32_t) * p.pairs_max);
@@ -112,6 +119,7 @@ void carve(Plan &p, Carver &c) {
         p.hq_atoms = c.take<uint8_t>(p.rows_pad_max * Imax / 16);
     } else {
         p.xp16 = c.take<__half>(p.rows_pad_max * H * 2);
+        p.tail_part = c.take<float>(sizeof(float) * (size_t)p.num_sms * moe::kTailPartFloats);
     }
     p.xts = c.take<float>(64);
     p.xq = c.take<uint8_t>(T * H / 2);
@@ -126,7 +134,6 @@ void carve(Plan &p, Carver &c) {
     p.out_stage = c.take<void>(2 * T * H);
 }
 
-size_t scratch_bytes(const Plan &p) { return sizeof(moe::CallScratch) + sizeof(int32_t) * p.cfg.num_experts; }
 
 moe_status check_call(moe_plan plan, const void *x, int32_t T, const float *rw, const float *bias) {
     if (!plan || T < 0 || T > plan->p.cfg.max_tokens) return MOE_ERR_INVALID_ARG;

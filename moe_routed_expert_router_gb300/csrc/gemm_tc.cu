@@ -155,6 +155,7 @@ __device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, float *v) {
 struct Item {
     int e, row0, valid, f, sh, K;
     int kc0, kc1;   // code stages [kc0, kc1) of K this item covers (split-K down items)
+    int part = 0, parts = 1, slot = -1;   // K piece of a split item (warp-MMA engine), its index among split items
 };
 
 // Items run tile by tile (one tile's token rows against every weight group).
@@ -573,6 +574,10 @@ struct HcArgs {
     // the gate/up launch gathers its token rows from (no separate permute)
     int rcst, rbst, rbslot;
     const uint16_t *x;
+    // split last round (warp-MMA engine): arrival tickets and partial sums
+    int tail_split;
+    int *tickets;
+    float *tail_part;
 };
 
 // f16 scale exponent s of the activations: x * 2^-s keeps amax below 2^15.
@@ -640,6 +645,53 @@ __device__ __forceinline__ void h_rows(const HcArgs &a, const Item &it, int epi,
         r0 = (it.sh ? 0 : it.e * a.H) + it.f * 256;
         r1 = r0 + 128;
     }
+}
+
+// Item order of the warp-MMA engine. The grid (one CTA an SM) takes items in
+// rounds; when the last round would leave most SMs idle, each of its items is
+// split along K into `parts` pieces (2 to kMaxTailParts, as many as the grid
+// holds), so the round runs parts x as many shorter pieces. Down pieces add
+// into the fp32 accumulator like whole items; gate/up pieces leave partial
+// sums, and the last piece of each to finish adds them in piece order and
+// applies SwiGLU.
+struct RegSplit {
+    int n_whole;   // items before the split round
+    int parts;     // pieces a split item is cut into (1: no split)
+    int n_items;   // flat items, pieces counted one by one
+};
+
+__device__ __forceinline__ RegSplit reg_split(const HcArgs &a) {
+    const int n_full = a.scratch->n_tiles * a.nf;
+    const int W = gridDim.x, r = n_full % W;
+    RegSplit s;
+    s.parts = (a.tail_split && r > 0 && 2 * r <= W) ? min(kMaxTailParts, W / r) : 1;
+    s.n_whole = s.parts > 1 ? n_full - r : n_full;
+    s.n_items = s.n_whole + (n_full - s.n_whole) * s.parts;
+    return s;
+}
+
+__device__ __forceinline__ bool decode_item_r(const HcArgs &a, const RegSplit &rs, int item, int epi, Item &it) {
+    int base = item, part = 0, parts = 1, slot = -1;
+    if (item >= rs.n_whole) {
+        const int j = item - rs.n_whole;
+        slot = j / rs.parts;
+        base = rs.n_whole + slot;
+        part = j % rs.parts;
+        parts = rs.parts;
+    }
+    if (!decode_item_h(a, base, epi, 1, it)) return false;
+    if (parts > 1) {
+        // pieces of `per` stages; as many pieces as that takes (never an empty one)
+        const int stages = it.kc1 - it.kc0, per = (stages + parts - 1) / parts;
+        parts = (stages + per - 1) / per;
+        if (part >= parts) return false;
+        it.kc1 = min(it.kc1, it.kc0 + (part + 1) * per);
+        it.kc0 += part * per;
+        it.part = part;
+        it.parts = parts;
+        it.slot = slot;
+    }
+    return true;
 }
 
 // One ring position: index in the ring and the parity of its current use.
@@ -1030,8 +1082,8 @@ template <int EPI>
 __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
                                             float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
                                             uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
-    const int ks = 1;
-    const int n_items = a.scratch->n_tiles * a.nf * ks;
+    const RegSplit rs = reg_split(a);
+    const int n_items = rs.n_items;
     const int cw = warp - 2, rg = cw & 7, op = cw >> 3;
     const int g = lane >> 2, q = lane & 3;
     const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
@@ -1042,7 +1094,7 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
     bool ok = true, range_bad = false;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item it;
-        if (!decode_item_h(a, item, EPI, ks, it)) continue;
+        if (!decode_item_r(a, rs, item, EPI, it)) continue;
         const int nt_n = (it.valid + 7) >> 3;
         // epilogue inputs, loaded now so their latency hides behind the K loop:
         // tensor scales, and the (token, weight) of this lane's first two columns
@@ -1095,27 +1147,78 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
                 if (lane == 0) mbar_arrive(xfull + rg);
             } else {
                 if (!mbar_wait(xfull + rg, xph, a.err)) { ok = false; break; }
-                const float sg = ts0 * xunscale, su = ts1 * xunscale;
+                float up[4][4];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
-                    if (nt >= nt_n) break;
-                    const float4 u4 = *reinterpret_cast<const float4 *>(slot + (nt * 32 + lane) * 4);
-                    const float u[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int n = nt * 8 + 2 * q + (i & 1);
-                        const int feat = it.f * 128 + rg * 16 + g + (i >> 1) * 8;
-                        if (n < it.valid) {
-                            const float gv = acc[nt][i] * sg, uv = u[i] * su;
-                            // SwiGLU output rounded to bf16 (W4A16), held as f16 for the down product
-                            const float hb = __bfloat162float(__float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv));
-                            range_bad |= fabsf(hb) > 65504.0f;
-                            a.hout[(size_t)(it.row0 + n) * a.hstride + feat] = __float2half_rn(hb);
-                        }
-                    }
+                    float4 u4 = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (nt < nt_n) u4 = *reinterpret_cast<const float4 *>(slot + (nt * 32 + lane) * 4);
+                    up[nt][0] = u4.x;
+                    up[nt][1] = u4.y;
+                    up[nt][2] = u4.z;
+                    up[nt][3] = u4.w;
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(xempty + rg);
+                bool last = true;
+                if (it.parts > 1) {
+                    // a K piece: leave this piece's partial sums, then take the
+                    // (item, row group) ticket; the last piece to arrive adds all
+                    // pieces in piece order (the same sum whichever finishes last)
+                    // and goes on to SwiGLU
+                    const size_t stride = 4 * 32 * 8;
+                    float *mine = a.tail_part + ((size_t)(it.slot * rs.parts + it.part) * 8 + rg) * stride;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        if (nt >= nt_n) break;
+                        float4 *dst = reinterpret_cast<float4 *>(mine + (nt * 32 + lane) * 8);
+                        __stcg(dst, make_float4(acc[nt][0], acc[nt][1], acc[nt][2], acc[nt][3]));
+                        __stcg(dst + 1, make_float4(up[nt][0], up[nt][1], up[nt][2], up[nt][3]));
+                    }
+                    __threadfence();
+                    __syncwarp();
+                    int arrived = 0;
+                    if (lane == 0) arrived = atomicAdd(a.tickets + it.slot * 8 + rg, 1);
+                    last = __shfl_sync(0xffffffffu, arrived, 0) == it.parts - 1;
+                    if (last) {
+                        __threadfence();
+#pragma unroll
+                        for (int nt = 0; nt < 4; ++nt) {
+                            if (nt >= nt_n) break;
+                            float gs[4] = {0.0f, 0.0f, 0.0f, 0.0f}, us[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            for (int pc = 0; pc < it.parts; ++pc) {
+                                const float4 *src = reinterpret_cast<const float4 *>(
+                                    a.tail_part + ((size_t)(it.slot * rs.parts + pc) * 8 + rg) * stride + (nt * 32 + lane) * 8);
+                                const float4 g4 = __ldcg(src), u4 = __ldcg(src + 1);
+                                gs[0] += g4.x; gs[1] += g4.y; gs[2] += g4.z; gs[3] += g4.w;
+                                us[0] += u4.x; us[1] += u4.y; us[2] += u4.z; us[3] += u4.w;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                acc[nt][i] = gs[i];
+                                up[nt][i] = us[i];
+                            }
+                        }
+                    }
+                }
+                if (last) {
+                    const float sg = ts0 * xunscale, su = ts1 * xunscale;
+#pragma unroll
+                    for (int nt = 0; nt < 4; ++nt) {
+                        if (nt >= nt_n) break;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int n = nt * 8 + 2 * q + (i & 1);
+                            const int feat = it.f * 128 + rg * 16 + g + (i >> 1) * 8;
+                            if (n < it.valid) {
+                                const float gv = acc[nt][i] * sg, uv = up[nt][i] * su;
+                                // SwiGLU output rounded to bf16 (W4A16), held as f16 for the down product
+                                const float hb = __bfloat162float(__float2bfloat16_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv));
+                                range_bad |= fabsf(hb) > 65504.0f;
+                                a.hout[(size_t)(it.row0 + n) * a.hstride + feat] = __float2half_rn(hb);
+                            }
+                        }
+                    }
+                }
             }
             xph ^= 1;
         } else {
@@ -1152,13 +1255,14 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
 // exact), in the 128-byte-swizzled box layout the compute warps read.
 template <int EPI>
 __device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b_ring, uint64_t *bfull,
-                                           uint64_t *bempty, int n_items, int ks) {
+                                           uint64_t *bempty, const RegSplit &rs) {
+    const int n_items = rs.n_items;
     const float scale = __uint_as_float((uint32_t)(127 - f16_shift(a.scratch->x_amax)) << 23);   // 2^-s
     RingPos b;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         Item it;
-        if (!decode_item_h(a, item, EPI, ks, it)) continue;
+        if (!decode_item_r(a, rs, item, EPI, it)) continue;
         const int rows = it.valid <= 16 ? 16 : 32;
         int tok = 0;   // lane n < valid: token of row n
         if (lane < it.valid) {
@@ -1235,8 +1339,8 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
     uint64_t *xempty = xfull + 8;                // [8] and read
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ks = 1;
-    const int n_items = a.scratch->n_tiles * a.nf * ks;
+    const RegSplit rs = reg_split(a);
+    const int n_items = rs.n_items;
     const bool gather = EPI == kSwiGLU && a.x != nullptr;
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.rcst; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
@@ -1254,7 +1358,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, ks, it)) continue;
+                if (!decode_item_r(a, rs, item, EPI, it)) continue;
                 const int m = it.sh ? 1 : 0;
                 int r0, r1;
                 h_rows(a, it, EPI, r0, r1);
@@ -1282,7 +1386,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             uint32_t used = 0, last_ph = 0;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
-                if (!decode_item_h(a, item, EPI, ks, it)) continue;
+                if (!decode_item_r(a, rs, item, EPI, it)) continue;
                 const int rc = it.valid <= 16 ? 0 : 1;
                 const int rows = 16 << rc;
                 for (int kc = it.kc0; kc < it.kc1; ++kc) {
@@ -1300,7 +1404,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                 if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
         }
     } else if (warp == 1) {
-        if (gather) reg_gather<EPI>(a, lane, b_ring, bfull, bempty, n_items, ks);
+        if (gather) reg_gather<EPI>(a, lane, b_ring, bfull, bempty, rs);
     } else {
         reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty);
     }
@@ -1457,6 +1561,9 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.k = c.top_k;
     a.acc = p.acc;
     a.err = p.err;
+    a.tail_split = (p.tail_part && p.tail_tickets) ? 1 : 0;
+    a.tickets = p.tail_tickets;
+    a.tail_part = p.tail_part;
     const RegRings rr = T <= 16 ? kRegSmall : kRegLarge;   // T <= 16: every tile has at most 16 rows
     a.rcst = rr.cst;
     a.rbst = rr.bst;

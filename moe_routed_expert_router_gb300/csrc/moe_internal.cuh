@@ -16,6 +16,11 @@ namespace moe {
 constexpr int kTileRows = 128;
 // Tokens of one expert handled together by the CUDA-core (decode-shaped) kernels.
 constexpr int kChunkRows = 4;
+// The warp-MMA engine may split the items of its grid's last, partial round
+// along K (at most kMaxTailParts pieces); a gate/up piece leaves its partial
+// sums for 8 row groups x 4 token tiles x 32 lanes x (4 gate + 4 up) values.
+constexpr int kMaxTailParts = 4;
+constexpr int kTailPartFloats = 8 * 4 * 32 * 8;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
 
@@ -73,6 +78,8 @@ struct Plan {
     uint8_t *hsc = nullptr;         // [rows_pad][Imax/16]
     float *hts = nullptr;           // [2] h tensor scales (routed, shared)
     float *acc = nullptr;           // [Tmax][H] fp32 combine accumulator, kept zero between calls
+    int32_t *tail_tickets = nullptr;   // [8 * num_sms] arrivals per split gate/up item and row group (per-call scratch)
+    float *tail_part = nullptr;        // [num_sms][8192] partial gate/up sums of split items (W4A16 warp MMAs)
     int *err = nullptr;             // device error word
     void *x_stage = nullptr;        // [Tmax][H] bf16 (moe_forward_host)
     void *out_stage = nullptr;      // [Tmax][H] bf16
