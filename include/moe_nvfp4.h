@@ -175,7 +175,8 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream);
 
 /* Device address and size of a plan workspace buffer, for tests that check a
  * step in isolation.  name: "h_codes", "h_scales", "h_ts", "x_ts", "acc",
- * "counts", "padded_offsets".  Returns MOE_ERR_INVALID_ARG for an unknown name. */
+ * "counts", "padded_offsets", "offsets", "sorted", "pad_pair", "tiles", "h".
+ * Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 
 /* Expert-FFN implementation moe_forward uses.  CUDA_CORE: weight-streaming

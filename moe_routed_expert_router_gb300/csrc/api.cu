@@ -445,6 +445,9 @@ moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, si
         {"acc", p.acc, sizeof(float) * (size_t)p.cfg.max_tokens * p.cfg.hidden},
         {"counts", p.counts, sizeof(int32_t) * (size_t)p.cfg.num_experts},
         {"padded_offsets", p.poff, sizeof(int32_t) * (size_t)(p.cfg.num_experts + 2)},
+        {"offsets", p.offsets, sizeof(int32_t) * (size_t)(p.cfg.num_experts + 1)},
+        {"sorted", p.sorted, sizeof(int32_t) * (size_t)p.pairs_max},
+        {"tiles", p.tiles, sizeof(int4) * (size_t)p.tiles_max},
         {"pad_pair", p.pad_pair, sizeof(int32_t) * (size_t)p.rows_pad_max},
         {"h", p.hbuf, sizeof(float) * (size_t)(p.rows_pad_max * Imax)},
     };

@@ -261,63 +261,101 @@ struct GroupArgs {
 };
 
 __host__ __device__ __forceinline__ size_t group_small_smem(int E, int P) {
-    return sizeof(int) * (5 * (size_t)(E + 2) + (size_t)P);
+    return sizeof(int) * (5 * (size_t)(E + 2) + (size_t)P + 4 * 32);
 }
 
-// Grouping of at most 512 pairs by one block (the decode router's last
-// block): the same outputs as k_group (offsets, padded offsets, the stable
-// order, the padded row map, work lists).  Counts come from the block's own
-// top-k ids; warp 0 places the pairs 32 at a time in increasing order, so
-// the order inside an expert is increasing p.
-__device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids, int P, int E, int T, int *sm,
-                            CallScratch *sc, int *err) {
-    int *s_cnt = sm, *s_off = s_cnt + (E + 2), *s_poff = s_off + (E + 2), *s_cb = s_poff + (E + 2),
-        *s_tb = s_cb + (E + 2), *s_ids = s_tb + (E + 2);
+// Grouping of the pairs of at most 32 tokens by one block (the decode
+// router's last block), with the outputs of k_group: offsets, padded
+// offsets, the stable order, the padded row map and the work lists. A token's
+// top-k experts are distinct, so each expert gets a bit mask of its tokens:
+// its population is the expert's count and the bits below token t give the
+// rank of t's pair inside the expert (the stable order, increasing p). Every
+// step is then one thread a pair or an expert. The padding rows of the map
+// were set to -1 by every block of the launch before this one started.
+__device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids, int P, int E, int T, int k,
+                            int *sm, CallScratch *sc, int *err) {
+    unsigned *s_mask = reinterpret_cast<unsigned *>(sm);
+    int *s_off = sm + (E + 2), *s_poff = s_off + (E + 2), *s_cb = s_poff + (E + 2), *s_tb = s_cb + (E + 2),
+        *s_ids = s_tb + (E + 2), *s_warp = s_ids + P;   // s_warp: [32][4] scan of the warp totals
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nthr = blockDim.x, nwarps = nthr >> 5;
-    for (int i = tid; i < E; i += nthr) s_cnt[i] = 0;
+    if (T > 32) {   // masks hold 32 tokens; the decode router never groups more
+        if (tid == 0) atomicOr(err, kErrDevice);
+        return;
+    }
+    for (int i = tid; i < E; i += nthr) s_mask[i] = 0u;
     __syncthreads();
     for (int q = tid; q < P; q += nthr) {
         int e = ids[q];
         if (e < 0 || e >= E) { atomicOr(err, kErrDevice); e = -1; }
         s_ids[q] = e;
-        if (e >= 0) atomicAdd(&s_cnt[e], 1);
+        if (e >= 0) atomicOr(&s_mask[e], 1u << (q / k));
     }
     __syncthreads();
-    if (warp == 0) {   // exclusive scans of (count, padded count, chunks, tiles), 32 experts at a time
-        int ra = 0, rb = 0, rd = 0, rf = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int c = e < E ? s_cnt[e] : 0;
-            const int pc = (c + kTileRows - 1) / kTileRows * kTileRows, nc = (c + kChunkRows - 1) / kChunkRows,
-                      nt = (c + g.tile_rows - 1) / g.tile_rows;
-            int a = c, b = pc, d = nc, f = nt;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o),
-                          yd = __shfl_up_sync(0xffffffffu, d, o), yf = __shfl_up_sync(0xffffffffu, f, o);
-                if (lane >= o) { a += ya; b += yb; d += yd; f += yf; }
-            }
-            if (e < E) {
-                s_off[e] = ra + a - c;
-                s_poff[e] = rb + b - pc;
-                s_cb[e] = rd + d - nc;
-                s_tb[e] = rf + f - nt;
-            }
-            ra += __shfl_sync(0xffffffffu, a, 31);
-            rb += __shfl_sync(0xffffffffu, b, 31);
-            rd += __shfl_sync(0xffffffffu, d, 31);
-            rf += __shfl_sync(0xffffffffu, f, 31);
+    // exclusive scans over experts of (count, padded count, chunks, tiles):
+    // thread tid sums experts [tid * per, tid * per + per), then warp and block scans
+    const int per = (E + nthr - 1) / nthr, e0 = tid * per;
+    int va = 0, vb = 0, vd = 0, vf = 0;
+    for (int j = 0; j < per; ++j) {
+        const int e = e0 + j;
+        if (e < E) {
+            const int c = __popc(s_mask[e]);
+            va += c;
+            vb += (c + kTileRows - 1) / kTileRows * kTileRows;
+            vd += (c + kChunkRows - 1) / kChunkRows;
+            vf += (c + g.tile_rows - 1) / g.tile_rows;
         }
-        if (lane == 0) {
-            s_off[E] = ra;
-            s_poff[E] = rb;
-            s_poff[E + 1] = rb + (g.has_shared ? (T + kTileRows - 1) / kTileRows * kTileRows : 0);
-            s_cb[E] = rd;
-            s_cb[E + 1] = rd + (g.has_shared ? (T + kChunkRows - 1) / kChunkRows : 0);
-            s_tb[E] = rf;
-            s_tb[E + 1] = rf + (g.has_shared ? (T + g.tile_rows - 1) / g.tile_rows : 0);
-            if (ra != P) atomicOr(err, kErrDevice);
+    }
+    int a = va, b = vb, d = vd, f = vf;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o),
+                  yd = __shfl_up_sync(0xffffffffu, d, o), yf = __shfl_up_sync(0xffffffffu, f, o);
+        if (lane >= o) { a += ya; b += yb; d += yd; f += yf; }
+    }
+    if (lane == 31) { s_warp[4 * warp] = a; s_warp[4 * warp + 1] = b; s_warp[4 * warp + 2] = d; s_warp[4 * warp + 3] = f; }
+    __syncthreads();
+    if (warp == 0) {
+        int wa = lane < nwarps ? s_warp[4 * lane] : 0, wb = lane < nwarps ? s_warp[4 * lane + 1] : 0,
+            wd = lane < nwarps ? s_warp[4 * lane + 2] : 0, wf = lane < nwarps ? s_warp[4 * lane + 3] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ya = __shfl_up_sync(0xffffffffu, wa, o), yb = __shfl_up_sync(0xffffffffu, wb, o),
+                      yd = __shfl_up_sync(0xffffffffu, wd, o), yf = __shfl_up_sync(0xffffffffu, wf, o);
+            if (lane >= o) { wa += ya; wb += yb; wd += yd; wf += yf; }
+        }
+        __syncwarp();
+        if (lane < nwarps) { s_warp[4 * lane] = wa; s_warp[4 * lane + 1] = wb; s_warp[4 * lane + 2] = wd; s_warp[4 * lane + 3] = wf; }
+    }
+    __syncthreads();
+    {
+        int ra = (warp ? s_warp[4 * (warp - 1)] : 0) + a - va, rb = (warp ? s_warp[4 * (warp - 1) + 1] : 0) + b - vb,
+            rd = (warp ? s_warp[4 * (warp - 1) + 2] : 0) + d - vd, rf = (warp ? s_warp[4 * (warp - 1) + 3] : 0) + f - vf;
+        for (int j = 0; j < per; ++j) {
+            const int e = e0 + j;
+            if (e < E) {
+                const int c = __popc(s_mask[e]);
+                s_off[e] = ra;
+                s_poff[e] = rb;
+                s_cb[e] = rd;
+                s_tb[e] = rf;
+                ra += c;
+                rb += (c + kTileRows - 1) / kTileRows * kTileRows;
+                rd += (c + kChunkRows - 1) / kChunkRows;
+                rf += (c + g.tile_rows - 1) / g.tile_rows;
+            }
+        }
+        if (tid == 0) {
+            const int ta = s_warp[4 * (nwarps - 1)], tb = s_warp[4 * (nwarps - 1) + 1],
+                      td = s_warp[4 * (nwarps - 1) + 2], tf = s_warp[4 * (nwarps - 1) + 3];
+            s_off[E] = ta;
+            s_poff[E] = tb;
+            s_poff[E + 1] = tb + (g.has_shared ? (T + kTileRows - 1) / kTileRows * kTileRows : 0);
+            s_cb[E] = td;
+            s_cb[E + 1] = td + (g.has_shared ? (T + kChunkRows - 1) / kChunkRows : 0);
+            s_tb[E] = tf;
+            s_tb[E + 1] = tf + (g.has_shared ? (T + g.tile_rows - 1) / g.tile_rows : 0);
+            if (ta != P) atomicOr(err, kErrDevice);
         }
     }
     __syncthreads();
@@ -327,45 +365,27 @@ __device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids,
         if (tid == 0) atomicOr(err, kErrDevice);
         return;
     }
-    for (int i = tid; i < E; i += nthr) s_cnt[i] = s_off[i];   // running position of each expert
-    __syncthreads();
-    if (warp == 0) {
-        for (int base = 0; base < P; base += 32) {
-            const int q = base + lane;
-            int e = q < P ? s_ids[q] : -1;
-            if (e < 0) e = -1 - lane;
-            const unsigned peers = __match_any_sync(0xffffffffu, e);
-            int pos = 0;
-            if (e >= 0) pos = s_cnt[e] + __popc(peers & ((1u << lane) - 1u));
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(peers) - 1) s_cnt[e] += __popc(peers);
-            __syncwarp();
-            if (e >= 0) {
-                const int prow = s_poff[e] + (pos - s_off[e]);
-                if (pos >= P || prow >= g.rows_cap) {
-                    atomicOr(err, kErrDevice);
-                } else {
-                    g.sorted[pos] = q;
-                    g.inv[q] = prow;
-                    g.pad_pair[prow] = q;
-                }
-            }
+    for (int q = tid; q < P; q += nthr) {   // placement: rank of the pair's token among the expert's tokens
+        const int e = s_ids[q];
+        if (e < 0) continue;
+        const int r = __popc(s_mask[e] & ((1u << (q / k)) - 1u));
+        const int pos = s_off[e] + r, prow = s_poff[e] + r;
+        if (pos >= P || prow >= g.rows_cap) {
+            atomicOr(err, kErrDevice);
+        } else {
+            g.sorted[pos] = q;
+            g.inv[q] = prow;
+            g.pad_pair[prow] = q;
         }
     }
-    for (int e = warp; e < E; e += nwarps) {   // padding rows
-        const int cnt = s_off[e + 1] - s_off[e], pend = s_poff[e + 1] - s_poff[e];
-        for (int q = cnt + lane; q < pend; q += 32) g.pad_pair[s_poff[e] + q] = -1;
-    }
-    if (g.has_shared) {
-        const int sh_rows = s_poff[E + 1] - s_poff[E];
-        for (int q = tid; q < sh_rows; q += nthr) g.pad_pair[s_poff[E] + q] = (q < T) ? P + q : -1;
-    }
-    for (int e = warp; e <= E; e += nwarps) {   // work lists, one warp an expert
-        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (g.has_shared ? T : 0);
+    if (g.has_shared)
+        for (int q = tid; q < T; q += nthr) g.pad_pair[s_poff[E] + q] = P + q;
+    for (int e = tid; e <= E; e += nthr) {   // work lists, one thread an expert (at most 32 rows each)
+        const int cnt = (e < E) ? __popc(s_mask[e]) : (g.has_shared ? T : 0);
         const int cb = s_cb[e], tb = s_tb[e];
-        for (int q = lane; q * kChunkRows < cnt; q += 32)
+        for (int q = 0; q * kChunkRows < cnt; ++q)
             g.chunks[cb + q] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
-        for (int q = lane; q * g.tile_rows < cnt; q += 32)
+        for (int q = 0; q * g.tile_rows < cnt; ++q)
             g.tiles[tb + q] = make_int4(e, s_poff[e] + q * g.tile_rows, min(g.tile_rows, cnt - q * g.tile_rows), 0);
     }
     if (tid == 0) {
@@ -482,6 +502,11 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
         if (lane == 0) logits[(size_t)warp * E + e] = bias ? acc + bias[e] : acc;
     }
+    if (grp.active) {   // every row of the padded map starts as padding; the last block fills in the pairs
+        const int per = (grp.rows_cap + (int)gridDim.x - 1) / (int)gridDim.x;
+        const int r0 = (int)blockIdx.x * per, r1 = min(grp.rows_cap, r0 + per);
+        for (int r = r0 + tid; r < r1; r += kDecodeRouterThreads) grp.pad_pair[r] = -1;
+    }
     __threadfence();
     __syncthreads();
     if (tid == 0) s_last = (atomicAdd(&sc->route_done, 1) == (int)gridDim.x - 1);
@@ -493,7 +518,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     if (grp.active) {
         __syncthreads();   // the block's ids are visible to all its threads
         int *gsm = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(wrow) + decode_router_smem(H, T));
-        group_small(grp, ids, T * k, E, T, gsm, sc, err);
+        group_small(grp, ids, T * k, E, T, k, gsm, sc, err);
     }
 }
 

@@ -92,3 +92,55 @@ def test_bounded_wait_reports_timeout_and_context_survives():
         r = plan.route(x, synth.router_weight(w, 0, "cuda"))
         assert plan.sync_status() == moe.OK
         assert int(r["expert_offsets"][-1]) == w.tokens * w.top_k
+
+
+def _padded_layout(offsets, rows, E, T, P, shared, tile_rows, pad=128):
+    """The padded row layout moe_forward builds from the grouping, derived from
+    the oracle's offsets and stable order: each expert's segment padded to a
+    multiple of 128 rows (-1 marks a padding row), the shared expert's T token
+    rows last (P + t), and the tiles of `tile_rows` rows over every segment."""
+    counts = np.diff(offsets)
+    seg = [-(-int(c) // pad) * pad for c in counts] + [(-(-T // pad) * pad) if shared else 0]
+    poff = np.concatenate([[0], np.cumsum(seg)]).astype(np.int32)
+    pad_pair = np.full(int(poff[-1]), -1, np.int32)
+    tiles = []
+    for e in range(E + 1):
+        c = int(counts[e]) if e < E else (T if shared else 0)
+        if e < E:
+            pad_pair[poff[e]:poff[e] + c] = rows[offsets[e]:offsets[e] + c]
+        else:
+            pad_pair[poff[e]:poff[e] + c] = P + np.arange(c)
+        for q in range(-(-c // tile_rows)):
+            tiles.append((e, int(poff[e]) + q * tile_rows, min(tile_rows, c - q * tile_rows), 0))
+    return poff, pad_pair, np.array(tiles, np.int32).reshape(-1, 4)
+
+
+@pytest.mark.parametrize("mode,T,path,tile_rows", [("w4a16", 1, "warp_mma", 32), ("w4a16", 16, "warp_mma", 32),
+                                                   ("w4a16", 16, "tensor_core", 64), ("w4a4", 16, "tensor_core", 128),
+                                                   ("w4a4", 3, "cuda_core", 128), ("w4a4", 20, "tensor_core", 128)])
+def test_forward_grouping_matches_oracle(mode, T, path, tile_rows):
+    """The grouping moe_forward runs (inside the decode router's last block for
+    T <= 16, k_group above) against the oracle's grouping, bit for bit: expert
+    offsets, the stable order, the padded offsets, the padded row map and the
+    tile work list."""
+    from helpers import Case
+    base = synth.WORKLOADS["decode4_w4a16"] if mode == "w4a16" else synth.WORKLOADS["verify16_w4a4"]
+    w = synth.scaled(base, tokens=T, hidden=512, experts=48, inter=256, shared_inter=256)
+    case = Case(w, 3)
+    paths = {"cuda_core": moe.PATH_CUDA_CORE, "tensor_core": moe.PATH_TENSOR_CORE, "warp_mma": moe.PATH_WARP_MMA}
+    with plan_for(w) as plan:
+        plan.set_path(paths[path])
+        for _ in range(2):   # the second call must not depend on what the first one left behind
+            _, st, _ = case.gpu_forward(plan)
+            assert st == moe.OK
+        bufs = {n: moe.device_view(*plan.debug_buffer(n)).view(torch.int32).cpu().numpy()
+                for n in ("offsets", "sorted", "padded_offsets", "pad_pair", "tiles")}
+    ref = oracle.route(case.x_host(), case.rw_host(), case.bias_host(), w.top_k,
+                       oracle.ROUTER_SIGMOID if w.router == "sigmoid" else oracle.ROUTER_SOFTMAX, w.renormalize)
+    E, P = w.experts, T * w.top_k
+    poff, pad_pair, tiles = _padded_layout(ref["offsets"], ref["sorted_rows"], E, T, P, True, tile_rows)
+    np.testing.assert_array_equal(bufs["offsets"][:E + 1], ref["offsets"])
+    np.testing.assert_array_equal(bufs["sorted"][:P], ref["sorted_rows"])
+    np.testing.assert_array_equal(bufs["padded_offsets"][:E + 2], poff)
+    np.testing.assert_array_equal(bufs["pad_pair"][:poff[-1]], pad_pair)
+    np.testing.assert_array_equal(bufs["tiles"].reshape(-1, 4)[:len(tiles)], tiles)
