@@ -165,6 +165,11 @@ __device__ __forceinline__ uint32_t logit_key(float v) {
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// The logit a non-zero key came from (logit_key is a bijection off NaN).
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // Top-k of token t by logit (ties -> lower id), then the weights; one warp,
 // NPL logits per lane (expert lane + 32*i).  Each round every lane offers its
 // best remaining (key, id); redux.sync takes the warp's largest key, then the
@@ -184,7 +189,9 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int
         v[i] = (e < E) ? __ldcg(logits + (size_t)t * E + e) : NEG;
         key[i] = (e < E) ? logit_key(v[i]) : 0u;
     }
-    float mine = 0.0f;  // lane j keeps the logit of slot j
+    float mine = 0.0f;  // lane j keeps the logit and the expert of slot j
+    int mine_id = 0;
+    bool nan_left = false;
     for (int j = 0; j < k; ++j) {
         uint32_t bk = 0u;
         int bi = 0x7fffffff;
@@ -195,27 +202,23 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int
         int wi = (int)__reduce_min_sync(0xffffffffu, (bk == wk && wk != 0u) ? (uint32_t)bi : 0x7fffffffu);
         float wv;
         if (wk == 0u || wi >= E) {  // only NaN logits left
-            if (lane == 0) atomicOr(err, kErrDevice);
+            nan_left = true;
             wi = 0;
             wv = 0.0f;
         } else {
-            wv = __shfl_sync(0xffffffffu, v[0], wi & 31);
-#pragma unroll
-            for (int i = 1; i < NPL; ++i) {
-                const float o = __shfl_sync(0xffffffffu, v[i], wi & 31);
-                if ((wi >> 5) == i) wv = o;
-            }
+            wv = key_logit(wk);   // the winner's logit, exactly
             if ((wi & 31) == lane) {
 #pragma unroll
                 for (int i = 0; i < NPL; ++i)
                     if ((wi >> 5) == i) key[i] = 0u;
             }
         }
-        if (lane == j) mine = wv;
-        if (lane == 0) {
-            ids[(size_t)t * k + j] = wi;
-            if (counts) atomicAdd(counts + wi, 1);
-        }
+        if (lane == j) { mine = wv; mine_id = wi; }
+    }
+    if (nan_left && lane == 0) atomicOr(err, kErrDevice);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = mine_id;
+        if (counts) atomicAdd(counts + mine_id, 1);
     }
     float num = 0.0f, den;
     if (kind == MOE_ROUTER_SOFTMAX) {
@@ -416,6 +419,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     const uint16_t *__restrict__ x, int T, int H, const float *__restrict__ rw, const float *__restrict__ bias,
     int E, int k, int kind, int renorm, float *__restrict__ logits, int32_t *__restrict__ ids,
     float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err, GroupArgs grp) {
+    pdl_trigger();   // the next kernel may be scheduled on free SMs (it waits for this one to finish)
     extern __shared__ __align__(16) float wrow[];     // [H], per-token x rings [T][kDStages][slab] bf16, grouping
     __shared__ float s_amax[kDecodeRouterThreads / 32];
     __shared__ int s_bad[kDecodeRouterThreads / 32];
