@@ -17,15 +17,25 @@
 //
 // Warp roles (one CTA per SM, persistent over the items):
 //   warp 0   TMA producer (one lane)
-//   warp 1   TMEM owner; one lane issues tcgen05.mma
+//   MMA warps: one lane each issues tcgen05.mma. A thread issuing tcgen05.mma
+//            stalls about as long as the MMA runs, so whatever else it does
+//            between MMAs (barrier waits, fences, descriptors, copies, commits)
+//            idles the tensor pipe.
+//     gate/up: warp 1 drives both accumulators; its stages wait on data
+//              (weights and token rows from L2) more than on issue;
+//     down:    warps 1 and 2, one accumulator each (the first and second 128
+//              weight rows), so one lane's bookkeeping runs under the other's
+//              MMAs.
+//            Warp 1 owns the TMEM allocation.
 //   scale warps, which put the stage's E4M3 scale factors into tensor memory:
 //     gate/up: warps 2-5, each writing its own 32-lane quadrant with tcgen05.st,
 //              so the tensor pipe spends no time on scales (448 threads);
-//     down:    warp 2, which re-lays the weight scale tiles in shared memory into
-//              512-byte atoms that the MMA lane copies with tcgen05.cp (352
-//              threads). The down epilogue keeps 128 accumulator values a thread
-//              in registers and needs the 168 registers a thread that an 11-warp
-//              block allows; at 14 warps it would spill.
+//     down:    warp 3, which re-lays the weight scale tiles in shared memory into
+//              512-byte atoms that each MMA lane copies with tcgen05.cp (the
+//              atoms its MMAs read; 384 threads). The down epilogue keeps 128
+//              accumulator values a thread in registers and needs the 168
+//              registers a thread that a 12-warp block allows; at 14 warps it
+//              would spill.
 //   the last 8 warps: epilogue (tcgen05.ld of their 32-lane quadrant of the
 //              accumulators)
 // Every mbarrier wait is bounded (about one second); on expiry the kernel sets
@@ -46,14 +56,20 @@ constexpr int kTile = 128 * kRowBytes;    // 16 KB operand tile
 constexpr int kSf = 128 * 16;             // 2 KB: 128 rows x 16 scale bytes
 constexpr int kStageBytes = 3 * kTile + 3 * kSf;   // A0, A1, B codes; A0, A1 scales (plain rows); B scales (atoms)
 constexpr int kEpiWarps = 8;                      // two per 32-lane TMEM quadrant
-constexpr uint32_t kSfCol0 = 256;                 // scale-factor TMEM columns: 48 a stage slot after the accumulators
-static_assert(kSfCol0 + kStages * 48 <= 512, "FP4 TMEM plan exceeds 512 columns");
+constexpr uint32_t kSfCol0 = 256;                 // scale-factor TMEM columns, after the two 128-column accumulators
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
 
 // Scale warps: four tcgen05.st writers (gate/up) or one shared-memory re-layout warp (down).
+__host__ __device__ constexpr int mma_warps(int epi) { return epi == kSwiGLU ? 1 : 2; }
 __host__ __device__ constexpr int scale_warps(int epi) { return epi == kSwiGLU ? 4 : 1; }
-__host__ __device__ constexpr int epi_warp0(int epi) { return 2 + scale_warps(epi); }
+__host__ __device__ constexpr int epi_warp0(int epi) { return 1 + mma_warps(epi) + scale_warps(epi); }
+// TMEM scale columns a stage slot owns: A0, A1, B (gate/up, written by the
+// scale warps and read by both MMA lanes); A0, A1, B for MMA lane 0, B for MMA
+// lane 1 (down: each lane copies the atoms its own MMAs read, since copies and
+// MMAs issued by different threads are not ordered)
+__host__ __device__ constexpr int sf_stride(int epi) { return epi == kSwiGLU ? 48 : 64; }
+static_assert(kSfCol0 + kStages * 64 <= 512, "FP4 TMEM plan exceeds 512 columns");
 __host__ __device__ constexpr int fp4_threads(int epi) { return 32 * (epi_warp0(epi) + kEpiWarps); }
 
 struct TcArgs {
@@ -183,7 +199,7 @@ __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, 
 
 template <int EPI>
 __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
-    constexpr int kScaleWarps = scale_warps(EPI), kEpiWarp0 = epi_warp0(EPI);
+    constexpr int kMmaWarps = mma_warps(EPI), kScaleWarps = scale_warps(EPI), kEpiWarp0 = epi_warp0(EPI);
     pdl_wait();      // routing, permute or gate/up results come from the previous kernel
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
@@ -203,11 +219,11 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full + s, 1);
             mbar_init(sf_ready + s, kScaleWarps);
-            mbar_init(empty + s, 1);
+            mbar_init(empty + s, kMmaWarps);   // every MMA lane commits every stage
         }
-        mbar_init(acc_full, 1);
+        mbar_init(acc_full, kMmaWarps);
         mbar_init(acc_empty, kEpiWarps);
-        mbar_init(drain, 1);
+        mbar_init(drain, kMmaWarps);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -262,13 +278,15 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
             for (int t = 0; t < kStages; ++t)
                 if (used & (1u << t)) mbar_wait(full + t, (last_ph >> t) & 1u, a.err);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issue (one lane)
+    } else if (warp >= 1 && warp <= kMmaWarps) {
+        // ------------------------------------------------ MMA issue (one lane a warp)
         if (lane == 0) {
+            // accumulators this lane drives: h0 .. h0 + nh - 1 (0: weight rows 0-127,
+            // i.e. gate / first down half; 1: rows 128-255)
+            const int h0 = warp - 1, nh = kMmaWarps == 1 ? 2 : 1;
             int s = 0;
             uint32_t ph = 0, aph = 0;
             bool ok = true;
-            const uint32_t d0 = tmem, d1 = tmem + 128;
             for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
                 Item it;
                 if (!decode_item(a, item, EPI, it)) continue;
@@ -284,26 +302,31 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                     // their 16-byte address units (the smem window is below 256 KB, so
                     // adding to the start-address field never carries out of it)
                     const uint32_t base = smem_u32(smem + s * kStageBytes);
-                    const uint64_t dA = desc_sw128(base);
-                    // scale factors of this stage slot: A0, A1, B at columns +0, +16,
-                    // +32, four per 64-value K chunk (gate/up: written by the scale
-                    // warps; down: copied here from the re-laid atoms)
-                    const uint32_t sf = tmem + kSfCol0 + s * 48;
+                    const uint64_t dA = desc_sw128(base), dB = desc_sw128(base + 2 * kTile);
+                    // scale factors of this stage slot: accumulator h's A at +16 h, its
+                    // B at +32 (gate/up) or +32 + 16 h (down), four columns a K chunk
+                    const uint32_t sf = tmem + kSfCol0 + s * sf_stride(EPI);
                     if (EPI == kScatter) {
                         const uint64_t dS = desc_sf(base + 3 * kTile);
+                        for (int h = h0; h < h0 + nh; ++h) {
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            sf_copy(sf + 4 * kk, dS + 32 * kk);
-                            sf_copy(sf + 16 + 4 * kk, dS + (kSf >> 4) + 32 * kk);
-                            sf_copy(sf + 32 + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
+                            for (int kk = 0; kk < 4; ++kk) {
+                                sf_copy(sf + 16 * h + 4 * kk, dS + h * (kSf >> 4) + 32 * kk);
+                                sf_copy(sf + 32 + 16 * h + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
+                            }
                         }
                     }
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks | kk) ? 1u : 0u;
-                        const uint64_t bd = dA + (2 * kTile >> 4) + 2 * kk;
-                        mma_fp4(d0, dA + 2 * kk, bd, idesc, sf + 4 * kk, sf + 32 + 4 * kk, accum);
-                        mma_fp4(d1, dA + (kTile >> 4) + 2 * kk, bd, idesc, sf + 16 + 4 * kk, sf + 32 + 4 * kk, accum);
+                        if (kMmaWarps == 1) {
+                            mma_fp4(tmem, dA + 2 * kk, dB + 2 * kk, idesc, sf + 4 * kk, sf + 32 + 4 * kk, accum);
+                            mma_fp4(tmem + 128, dA + (kTile >> 4) + 2 * kk, dB + 2 * kk, idesc, sf + 16 + 4 * kk,
+                                    sf + 32 + 4 * kk, accum);
+                        } else {
+                            mma_fp4(tmem + 128 * h0, dA + h0 * (kTile >> 4) + 2 * kk, dB + 2 * kk, idesc,
+                                    sf + 16 * h0 + 4 * kk, sf + 32 + 16 * h0 + 4 * kk, accum);
+                        }
                     }
                     mma_commit(empty + s);
                     if (++s == kStages) { s = 0; ph ^= 1; }
@@ -315,7 +338,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
             mma_commit(drain);
             mbar_wait(drain, 0, a.err);
         }
-    } else if (warp >= 2 && warp < kEpiWarp0 && EPI == kScatter) {
+    } else if (warp > kMmaWarps && warp < kEpiWarp0 && EPI == kScatter) {
         // ------------------------------------------------ weight scale re-layout (down)
         // plain [128 rows][16 B] scale tiles -> four 512-byte atoms each, in place:
         // the 4 scale bytes of row r for K chunk c go to word (r % 32) * 4 + r / 32
@@ -350,7 +373,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
             }
         }
         mbar_wait(drain, 0, a.err);
-    } else if (warp >= 2 && warp < kEpiWarp0) {
+    } else if (warp > kMmaWarps && warp < kEpiWarp0) {
         // ------------------------------------------------ scale factors -> TMEM
         // Scale-factor layout (scale_vec::4X, M = N = 128), 4 columns per K chunk
         // kk of 64 values, as a 32x128b.warpx4 copy of a 512-byte atom lays it
@@ -390,7 +413,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                         o[8 + j] = v.z;
                         o[12 + j] = v.w;
                     }
-                    tmem_st16(t_lane + s * 48 + 16 * op, o);
+                    tmem_st16(t_lane + s * sf_stride(EPI) + 16 * op, o);
                 }
                 {
                     uint4 v[4];
@@ -403,7 +426,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                         o[4 * kk + 2] = v[kk].z;
                         o[4 * kk + 3] = v[kk].w;
                     }
-                    tmem_st16(t_lane + s * 48 + 32, o);
+                    tmem_st16(t_lane + s * sf_stride(EPI) + 32, o);
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
                 tc_fence_before();
