@@ -571,7 +571,12 @@ constexpr int kConvWarps = 8 * kConvSplit;
 constexpr int kConvCols = 32 / kConvSplit;       // TMEM columns (2 K values each) a converter fills per A stage
 static_assert(kConvSplit == 2, "the converter loop below is written for two K halves");
 constexpr int kHEpiWarps = 4;
-constexpr int kHThreads = 32 * (2 + kConvWarps + kHEpiWarps);
+// the second MMA lane's warp, after the epilogue warps (warp 1 drives the
+// first accumulator half, this one the second: a thread issuing tcgen05.mma
+// stalls about as long as the MMA runs, so one issuer idles the pipe during
+// its own barrier waits and commits)
+constexpr int kHMma2 = 2 + kConvWarps + kHEpiWarps;
+constexpr int kHThreads = 32 * (kHMma2 + 1);
 constexpr size_t kHRingBytes = (size_t)kHCStages * kHCodeStage + (size_t)kHBStages * kHBTile;
 constexpr size_t kHSmemBytes = kHRingBytes + 512 + 1024;
 static_assert(kHSmemBytes <= 227 * 1024, "W4A16 pipeline exceeds shared memory");
@@ -750,10 +755,10 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
     const int n_items = a.scratch->n_tiles * a.nf;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kHCStages; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, kConvWarps); }
-        for (int i = 0; i < kHBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 1); }
-        for (int i = 0; i < kHAStages; ++i) { mbar_init(afull + i, kConvWarps); mbar_init(aempty + i, 1); }
-        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 1); mbar_init(acc_empty + i, kHEpiWarps); }
-        mbar_init(drain, 1);
+        for (int i = 0; i < kHBStages; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 2); }
+        for (int i = 0; i < kHAStages; ++i) { mbar_init(afull + i, kConvWarps); mbar_init(aempty + i, 2); }
+        for (int i = 0; i < 2; ++i) { mbar_init(acc_full + i, 2); mbar_init(acc_empty + i, kHEpiWarps); }
+        mbar_init(drain, 2);                // both MMA lanes commit
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -879,9 +884,10 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 }
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------ MMA issue (one lane)
+    } else if (warp == 1 || warp == kHMma2) {
+        // ------------------------------------------------ MMA issue: one lane an accumulator half
         if (lane == 0) {
+            const int hs = warp == 1 ? 0 : 1;   // columns +64 hs of the accumulator, A columns +32 hs
             RingPos as, bs;
             int buf = 0;
             uint32_t aph = 0;   // bit b: parity of accumulator buffer b
@@ -892,7 +898,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 if (!mbar_wait(acc_empty + buf, ((aph >> buf) & 1u) ^ 1u, a.err)) break;
                 aph ^= 1u << buf;
                 tc_fence_after();
-                const uint32_t d0 = tmem + buf * 128, d1 = d0 + 64;
+                const uint32_t d = tmem + buf * 128 + 64 * hs;
                 const int rc = hrows_class(it.valid);
                 const int rows = 16 << rc, boxes = 8 >> rc, nq = it.K / kHBK;
                 const uint32_t idesc = idesc_f16((uint32_t)rows);
@@ -909,8 +915,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (qq | kk) ? 1u : 0u;
                         const uint64_t bd = desc_sw128(bt + 32 * kk);
-                        mma_f16_ts(d0, at + 8 * kk, bd, idesc, accum);
-                        mma_f16_ts(d1, at + 32 + 8 * kk, bd, idesc, accum);
+                        mma_f16_ts(d, at + 32 * hs + 8 * kk, bd, idesc, accum);
                     }
                     mma_commit(aempty + as.s);
                     as.next(kHAStages);
