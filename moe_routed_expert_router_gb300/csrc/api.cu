@@ -113,6 +113,7 @@ void carve(Plan &p, Carver &c) {
     p.pad_pair = c.take<int32_t>(sizeof(int32_t) * p.rows_pad_max);
     p.chunks = c.take<int4>(sizeof(int4) * p.chunks_max);
     p.tiles = c.take<int4>(sizeof(int4) * p.tiles_max);
+    p.group_blk = c.take<int32_t>(sizeof(int32_t) * (size_t)((p.pairs_max + moe::kGroupSeg - 1) / moe::kGroupSeg) * E);
     if (k.mode == MOE_W4A4) {
         p.xp = c.take<uint8_t>(p.rows_pad_max * H / 2);
         p.xp_atoms = c.take<uint8_t>(p.rows_pad_max * H / 16);
@@ -194,7 +195,8 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *
     }
     if (!fused_group) {
         Stage s(plan, MOE_STAGE_GROUP, st);
-        if (s.done(moe::launch_group(p, T, p.ids, nullptr, nullptr, true, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
+        if (s.done(moe::launch_group(p, T, p.ids, nullptr, nullptr, true, st), moe::group_launches(p, T)) != cudaSuccess)
+            return MOE_ERR_CUDA;
     }
     if (p.cfg.mode == MOE_W4A4) {
         Stage s(plan, MOE_STAGE_QUANT_X, st);

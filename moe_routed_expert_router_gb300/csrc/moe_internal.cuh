@@ -20,6 +20,8 @@ constexpr int kChunkRows = 4;
 // along K (at most kMaxTailParts pieces); a gate/up piece leaves its partial
 // sums for 8 row groups x 4 token tiles x 32 lanes x (4 gate + 4 up) values.
 constexpr int kMaxTailParts = 4;
+// Pairs a block of the multi-block grouping takes.
+constexpr int kGroupSeg = 1024;
 constexpr int kTailPartFloats = 8 * 4 * 32 * 8;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
@@ -78,6 +80,7 @@ struct Plan {
     uint8_t *hsc = nullptr;         // [rows_pad][Imax/16]
     float *hts = nullptr;           // [2] h tensor scales (routed, shared)
     float *acc = nullptr;           // [Tmax][H] fp32 combine accumulator, kept zero between calls
+    int32_t *group_blk = nullptr;      // [ceil(pairs_max / kGroupSeg)][E] per-block expert counts / first slots
     int32_t *tail_tickets = nullptr;   // [8 * num_sms] arrivals per split gate/up item and row group (per-call scratch)
     float *tail_part = nullptr;        // [num_sms][8192] partial gate/up sums of split items (W4A16 warp MMAs)
     int *err = nullptr;             // device error word
@@ -270,6 +273,7 @@ int router_launches(int T);
 bool router_groups(int T);
 cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias,
                           int32_t *ids, float *wts, cudaStream_t st, bool with_group = false);
+int group_launches(const Plan &p, int T);
 cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out,
                          int32_t *sorted_out, bool build_work, cudaStream_t st);
 cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes, uint8_t *scales,

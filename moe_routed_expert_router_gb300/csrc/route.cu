@@ -526,39 +526,16 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     }
 }
 
-// Single-block grouping (1024 threads).  Stable counting sort of the pairs
-// p = t*k + j by expert: each of the 32 warps owns a contiguous segment of
-// pairs, counts it per expert, the per-(warp, expert) bases are scanned, and a
-// second walk places every pair (ranks within a warp come from match_any, so
-// the order inside an expert is increasing p).  Also writes the padded row
-// layout used by the expert kernels and their work lists.
-__global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids, int P, int E, int T, int k,
-                                                int has_shared, const int32_t *__restrict__ counts,
-                                                int32_t *__restrict__ offsets, int32_t *__restrict__ poff,
-                                                int32_t *__restrict__ sorted, int32_t *__restrict__ inv,
-                                                int32_t *__restrict__ pad_pair, int4 *__restrict__ chunks,
-                                                int4 *__restrict__ tiles,
-                                                CallScratch *scratch, int32_t *__restrict__ offsets_out,
-                                                int32_t *__restrict__ sorted_out, int build_work, int rows_cap,
-                                                int tile_rows, int *err) {
-    extern __shared__ int smem[];
-    int *wc = smem;                        // [32][E]
-    int *s_off = smem + 32 * E;            // [E+1]
-    int *s_poff = s_off + (E + 1);         // [E+2]
-    int *s_cb = s_poff + (E + 2);          // [E+2] chunk bases
-    int *s_tb = s_cb + (E + 2);            // [E+2] tile bases
-    __shared__ int s_warp[32][4];
+// Per-expert layout of a grouping, computed by one 1024-thread block from the
+// expert counts (thread e < E holds count c of expert e): exclusive scans over
+// experts of (count, count padded to kTileRows, CUDA-core chunks, tensor-core
+// tiles) into s_off, s_poff, s_cb, s_tb, with the totals (and the shared
+// expert's segment) at E and E + 1.
+__device__ void group_scan_experts(int c, int E, int T, int P, int has_shared, int tile_rows, int *s_off,
+                                   int *s_poff, int *s_cb, int *s_tb, int (*s_warp)[4], int *err) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-
-    for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
-    // exclusive scans over experts of (count, padded count, chunks, tiles)
-    int c = 0, pc = 0, nc = 0, nt = 0;
-    if (tid < E) {
-        c = counts[tid];
-        pc = (c + kTileRows - 1) / kTileRows * kTileRows;
-        nc = (c + kChunkRows - 1) / kChunkRows;
-        nt = (c + tile_rows - 1) / tile_rows;
-    }
+    const int pc = (c + kTileRows - 1) / kTileRows * kTileRows, nc = (c + kChunkRows - 1) / kChunkRows,
+              nt = (c + tile_rows - 1) / tile_rows;
     int a = c, b = pc, d = nc, f = nt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -599,26 +576,92 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         if (tot_a != P) atomicOr(err, kErrDevice);
     }
     __syncthreads();
-    for (int i = tid; i <= E; i += 1024) {
-        offsets[i] = s_off[i];
-        if (offsets_out) offsets_out[i] = s_off[i];
-    }
-    for (int i = tid; i <= E + 1; i += 1024) poff[i] = s_poff[i];
+}
 
-    // pass 1: per-warp segment counts
-    const int seg = ((P + 31) / 32 + 31) / 32 * 32;
-    const int p_beg = warp * seg, p_end = min(P, p_beg + seg);
-    for (int base = p_beg; base < p_end; base += 32) {
-        int p = base + lane;
-        int e = (p < p_end) ? ids[p] : -1 - lane;
-        if (p < p_end && (e < 0 || e >= E)) { atomicOr(err, kErrDevice); e = -1 - lane; }
-        unsigned peers = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && lane == __ffs(peers) - 1) wc[warp * E + e] += __popc(peers);
+// The expert (0..E, E = shared) whose entries [base[e], base[e + 1]) hold entry
+// i: the largest e with base[e] <= i (experts without entries are skipped).
+__device__ __forceinline__ int group_owner(const int *base, int E, int i) {
+    int lo = 0, hi = E;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (base[mid] <= i) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// The padded row map's padding rows and the shared expert's rows, the
+// CUDA-core work chunks (up to kChunkRows rows of one expert) and the
+// tensor-core tiles (tile_rows padded rows of one expert, inside its
+// 128-row-aligned segment), from a block's s_off / s_poff / s_cb / s_tb.
+// Padding: one warp an expert, its lanes writing consecutive rows (fewer than
+// kTileRows each); chunks and tiles: one thread an entry, its expert found by
+// binary search, so a heavily routed expert's thousands of entries spread over
+// the block (both keep the stores coalesced).
+__device__ void group_build_work(int E, int T, int P, int has_shared, int tile_rows, const int *s_off,
+                                 const int *s_poff, const int *s_cb, const int *s_tb, int32_t *__restrict__ pad_pair,
+                                 int4 *__restrict__ chunks, int4 *__restrict__ tiles, CallScratch *scratch) {
+    const int tid = threadIdx.x, nthr = blockDim.x, lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
+    for (int e = warp; e < E; e += nwarps) {
+        const int cnt = s_off[e + 1] - s_off[e], pend = s_poff[e + 1] - s_poff[e];
+        for (int q = cnt + lane; q < pend; q += 32) pad_pair[s_poff[e] + q] = -1;
+    }
+    if (has_shared) {
+        int sh_rows = s_poff[E + 1] - s_poff[E];
+        for (int q = tid; q < sh_rows; q += nthr) pad_pair[s_poff[E] + q] = (q < T) ? P + q : -1;
+    }
+    for (int i = tid; i < s_cb[E + 1]; i += nthr) {
+        const int e = group_owner(s_cb, E, i), q = i - s_cb[e];
+        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : T;
+        chunks[i] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
+    }
+    for (int i = tid; i < s_tb[E + 1]; i += nthr) {
+        const int e = group_owner(s_tb, E, i), q = i - s_tb[e];
+        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : T;
+        tiles[i] = make_int4(e, s_poff[e] + q * tile_rows, min(tile_rows, cnt - q * tile_rows), 0);
+    }
+    if (tid == 0) {
+        scratch->n_tiles = s_tb[E + 1];
+        scratch->n_chunks = s_cb[E + 1];
+        scratch->n_chunks_routed = s_cb[E];
+    }
+}
+
+// Stable placement of the pairs [p_beg, p_end) of one block, split among its
+// 32 warps in order: each warp counts its segment per expert (shared atomics),
+// the per-(warp, expert) starts are scanned from base[e] (the block's first
+// slot of expert e), and a second walk places every pair (ranks within a warp
+// from match_any, so the order inside an expert is increasing p). match_any
+// has a low throughput an SM, so rounds past the warp's segment are skipped.
+// wc: [32][E] shared words.
+__device__ void group_place(const int32_t *__restrict__ ids, int p_beg, int p_end, int P, int E, int *wc,
+                            const int *base, const int *s_off, const int *s_poff, int32_t *__restrict__ sorted,
+                            int32_t *__restrict__ sorted_out, int32_t *__restrict__ inv,
+                            int32_t *__restrict__ pad_pair, int rows_cap, int *err) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kPre = 8;   // rounds whose ids are loaded together (one L2 round trip for kPre rounds)
+    const int n = p_end - p_beg, seg = ((n + 31) / 32 + 31) / 32 * 32;
+    const int w_beg = p_beg + warp * seg, w_end = min(p_end, w_beg + seg);
+    for (int base0 = w_beg; base0 < w_end; base0 += 32 * kPre) {
+        int ev[kPre];
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            const int p = base0 + 32 * u + lane;
+            ev[u] = (p < w_end) ? __ldg(ids + p) : -1 - lane;
+        }
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            const int p = base0 + 32 * u + lane;
+            const int e = ev[u];
+            if (p < w_end) {
+                if (e < 0 || e >= E) atomicOr(err, kErrDevice);
+                else atomicAdd(&wc[warp * E + e], 1);
+            }
+        }
     }
     __syncthreads();
-    // per-expert scan over warps
-    for (int e = tid; e < E; e += 1024) {
-        int run = s_off[e];
+    for (int e = tid; e < E; e += blockDim.x) {   // per-expert scan over warps
+        int run = base[e];
         for (int w = 0; w < 32; ++w) {
             int t = wc[w * E + e];
             wc[w * E + e] = run;
@@ -626,61 +669,167 @@ __global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids,
         }
     }
     __syncthreads();
-    // pass 2: place
-    for (int base = p_beg; base < p_end; base += 32) {
-        int p = base + lane;
-        int e = (p < p_end) ? ids[p] : -1 - lane;
-        if (e >= E) e = -1 - lane;
-        unsigned peers = __match_any_sync(0xffffffffu, e);
-        int pos = 0;
-        if (e >= 0) pos = wc[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
-        __syncwarp();
-        if (e >= 0 && lane == __ffs(peers) - 1) wc[warp * E + e] += __popc(peers);
-        __syncwarp();
-        if (e >= 0) {
-            int prow = s_poff[e] + (pos - s_off[e]);
-            if (pos >= P || prow >= rows_cap) {  // inconsistent counts: refuse, never write out of range
-                atomicOr(err, kErrDevice);
-                continue;
+    for (int base0 = w_beg; base0 < w_end; base0 += 32 * kPre) {
+        int ev[kPre];
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            const int p = base0 + 32 * u + lane;
+            ev[u] = (p < w_end) ? __ldg(ids + p) : -1 - lane;
+        }
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            if (base0 + 32 * u >= w_end) break;   // warp-uniform
+            const int p = base0 + 32 * u + lane;
+            int e = ev[u];
+            if (e >= E) e = -1 - lane;
+            unsigned peers = __match_any_sync(0xffffffffu, e);
+            int pos = 0;
+            if (e >= 0) pos = wc[warp * E + e] + __popc(peers & ((1u << lane) - 1u));
+            __syncwarp();
+            if (e >= 0 && lane == __ffs(peers) - 1) wc[warp * E + e] += __popc(peers);
+            __syncwarp();
+            if (e >= 0) {
+                const int prow = s_poff[e] + (pos - s_off[e]);
+                if (pos >= P || prow >= rows_cap) {  // inconsistent counts: refuse, never write out of range
+                    atomicOr(err, kErrDevice);
+                } else {
+                    sorted[pos] = p;
+                    if (sorted_out) sorted_out[pos] = p;
+                    inv[p] = prow;
+                    pad_pair[prow] = p;
+                }
             }
-            sorted[pos] = p;
-            if (sorted_out) sorted_out[pos] = p;
-            inv[p] = prow;
-            pad_pair[prow] = p;
         }
     }
+}
+
+// Single-block grouping (1024 threads), for small batches and callers without
+// the per-block count buffer: stable counting sort of the pairs p = t*k + j by
+// expert (group_place over all pairs), plus the padded row layout used by the
+// expert kernels and their work lists.
+__global__ void __launch_bounds__(1024) k_group(const int32_t *__restrict__ ids, int P, int E, int T, int k,
+                                                int has_shared, const int32_t *__restrict__ counts,
+                                                int32_t *__restrict__ offsets, int32_t *__restrict__ poff,
+                                                int32_t *__restrict__ sorted, int32_t *__restrict__ inv,
+                                                int32_t *__restrict__ pad_pair, int4 *__restrict__ chunks,
+                                                int4 *__restrict__ tiles,
+                                                CallScratch *scratch, int32_t *__restrict__ offsets_out,
+                                                int32_t *__restrict__ sorted_out, int build_work, int rows_cap,
+                                                int tile_rows, int *err) {
+    extern __shared__ int smem[];
+    int *wc = smem;                        // [32][E]
+    int *s_off = smem + 32 * E;            // [E+1]
+    int *s_poff = s_off + (E + 1);         // [E+2]
+    int *s_cb = s_poff + (E + 2);          // [E+2] chunk bases
+    int *s_tb = s_cb + (E + 2);            // [E+2] tile bases
+    __shared__ int s_warp[32][4];
+    const int tid = threadIdx.x;
+    for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+    group_scan_experts(tid < E ? counts[tid] : 0, E, T, P, has_shared, tile_rows, s_off, s_poff, s_cb, s_tb,
+                       s_warp, err);
+    for (int i = tid; i <= E; i += 1024) {
+        offsets[i] = s_off[i];
+        if (offsets_out) offsets_out[i] = s_off[i];
+    }
+    for (int i = tid; i <= E + 1; i += 1024) poff[i] = s_poff[i];
+    group_place(ids, 0, P, P, E, wc, s_off, s_off, s_poff, sorted, sorted_out, inv, pad_pair, rows_cap, err);
     if (!build_work) return;
     if (s_poff[E + 1] > rows_cap) {
         if (tid == 0) atomicOr(err, kErrDevice);
         return;
     }
-    // padding rows and the shared expert's rows
-    for (int e = warp; e < E; e += 32) {
-        int cnt = s_off[e + 1] - s_off[e];
-        int pend = s_poff[e + 1] - s_poff[e];
-        for (int q = cnt + lane; q < pend; q += 32) pad_pair[s_poff[e] + q] = -1;
+    group_build_work(E, T, P, has_shared, tile_rows, s_off, s_poff, s_cb, s_tb, pad_pair, chunks, tiles, scratch);
+}
+
+// Multi-block grouping of large batches, three launches over blocks of
+// kGroupSeg pairs: per-block expert counts; one block scanning them into the
+// per-expert layout (and each block's first slot of every expert) and building
+// the work lists; per-block placement. The order is the single-block one.
+__global__ void __launch_bounds__(1024) k_group_count(const int32_t *__restrict__ ids, int P, int E,
+                                                      int32_t *__restrict__ blk, int *err) {
+    pdl_trigger();   // the scan launch may be scheduled now (it waits for this one)
+    extern __shared__ int hist[];   // [E]
+    for (int i = threadIdx.x; i < E; i += 1024) hist[i] = 0;
+    __syncthreads();
+    const int p = blockIdx.x * kGroupSeg + threadIdx.x;
+    if (p < P) {
+        const int e = ids[p];
+        if (e < 0 || e >= E) atomicOr(err, kErrDevice);
+        else atomicAdd(&hist[e], 1);
     }
-    if (has_shared) {
-        int sh_rows = s_poff[E + 1] - s_poff[E];
-        for (int q = tid; q < sh_rows; q += 1024) pad_pair[s_poff[E] + q] = (q < T) ? P + q : -1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < E; i += 1024) blk[(size_t)blockIdx.x * E + i] = hist[i];
+}
+
+// blk[b][e] (counts in, each block's first slot of expert e out)
+__global__ void __launch_bounds__(1024) k_group_scan(int nb, int P, int E, int T, int has_shared,
+                                                     int32_t *__restrict__ blk, int32_t *__restrict__ offsets,
+                                                     int32_t *__restrict__ poff, int4 *__restrict__ chunks,
+                                                     int4 *__restrict__ tiles, CallScratch *scratch,
+                                                     int32_t *__restrict__ offsets_out, int32_t *__restrict__ pad_pair,
+                                                     int build_work, int rows_cap, int tile_rows, int *err) {
+    pdl_wait();      // the per-block counts are complete
+    pdl_trigger();
+    extern __shared__ int smem[];
+    int *s_off = smem, *s_poff = s_off + (E + 1), *s_cb = s_poff + (E + 2), *s_tb = s_cb + (E + 2);
+    __shared__ int s_warp[32][4];
+    const int tid = threadIdx.x;
+    int c = 0;
+    if (tid < E) {   // the expert's count over all blocks (loads issued eight at a time)
+        for (int b0 = 0; b0 < nb; b0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = b0 + u < nb ? blk[(size_t)(b0 + u) * E + tid] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) c += v[u];
+        }
     }
-    // CUDA-core work chunks (up to kChunkRows rows of one expert) and
-    // tensor-core tiles (tile_rows padded rows of one expert, inside its
-    // 128-row-aligned segment): one warp an expert, its lanes writing
-    // consecutive entries
-    for (int e = warp; e <= E; e += 32) {
-        const int cnt = (e < E) ? s_off[e + 1] - s_off[e] : (has_shared ? T : 0);
-        const int cb = s_cb[e], tb = s_tb[e];
-        for (int q = lane; q * kChunkRows < cnt; q += 32)
-            chunks[cb + q] = make_int4(e, s_poff[e] + q * kChunkRows, min(kChunkRows, cnt - q * kChunkRows), 0);
-        for (int q = lane; q * tile_rows < cnt; q += 32)
-            tiles[tb + q] = make_int4(e, s_poff[e] + q * tile_rows, min(tile_rows, cnt - q * tile_rows), 0);
+    group_scan_experts(c, E, T, P, has_shared, tile_rows, s_off, s_poff, s_cb, s_tb, s_warp, err);
+    if (tid < E) {   // each block's first slot of this expert (counts loaded eight at a time, then stored)
+        int run = s_off[tid];
+        for (int b0 = 0; b0 < nb; b0 += 8) {
+            int v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = b0 + u < nb ? blk[(size_t)(b0 + u) * E + tid] : 0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (b0 + u < nb) blk[(size_t)(b0 + u) * E + tid] = run;
+                run += v[u];
+            }
+        }
     }
-    if (tid == 0) {
-        scratch->n_tiles = s_tb[E + 1];
-        scratch->n_chunks = s_cb[E + 1];
-        scratch->n_chunks_routed = s_cb[E];
+    for (int i = tid; i <= E; i += 1024) {
+        offsets[i] = s_off[i];
+        if (offsets_out) offsets_out[i] = s_off[i];
     }
+    for (int i = tid; i <= E + 1; i += 1024) poff[i] = s_poff[i];
+    if (!build_work) return;
+    if (s_poff[E + 1] > rows_cap) {
+        if (tid == 0) atomicOr(err, kErrDevice);
+        return;
+    }
+    group_build_work(E, T, P, has_shared, tile_rows, s_off, s_poff, s_cb, s_tb, pad_pair, chunks, tiles, scratch);
+}
+
+__global__ void __launch_bounds__(1024) k_group_place(const int32_t *__restrict__ ids, int P, int E,
+                                                      const int32_t *__restrict__ blk,
+                                                      const int32_t *__restrict__ offsets,
+                                                      const int32_t *__restrict__ poff, int32_t *__restrict__ sorted,
+                                                      int32_t *__restrict__ sorted_out, int32_t *__restrict__ inv,
+                                                      int32_t *__restrict__ pad_pair, int rows_cap, int *err) {
+    pdl_wait();      // the layout and the per-block first slots are complete
+    pdl_trigger();
+    extern __shared__ int smem[];
+    int *wc = smem, *s_base = wc + 32 * E, *s_off = s_base + E, *s_poff = s_off + E;
+    for (int i = threadIdx.x; i < 32 * E; i += 1024) wc[i] = 0;
+    for (int i = threadIdx.x; i < E; i += 1024) {
+        s_base[i] = blk[(size_t)blockIdx.x * E + i];
+        s_off[i] = offsets[i];
+        s_poff[i] = poff[i];
+    }
+    __syncthreads();
+    const int p_beg = blockIdx.x * kGroupSeg, p_end = min(P, p_beg + kGroupSeg);
+    group_place(ids, p_beg, p_end, P, E, wc, s_base, s_off, s_poff, sorted, sorted_out, inv, pad_pair, rows_cap, err);
 }
 
 }  // namespace
@@ -745,14 +894,36 @@ cudaError_t configure_group_kernel(int E) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
         if (e != cudaSuccess) return e;
     }
+    e = cudaFuncSetAttribute(k_group_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(sizeof(int) * 35 * (size_t)E));
+    if (e != cudaSuccess) return e;
     return cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(E));
+}
+
+// Launches of launch_group: three (count, scan, place) for batches larger than
+// two segments when the plan holds the per-block count buffer, else one.
+int group_launches(const Plan &p, int T) {
+    return (p.group_blk && (int64_t)T * p.cfg.top_k > 2 * kGroupSeg) ? 3 : 1;
 }
 
 cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out, int32_t *sorted_out,
                          bool build_work, cudaStream_t st) {
-    const int E = p.cfg.num_experts, k = p.cfg.top_k;
+    const int E = p.cfg.num_experts, k = p.cfg.top_k, P = T * k;
+    if (group_launches(p, T) == 3) {
+        const int nb = (P + kGroupSeg - 1) / kGroupSeg;
+        k_group_count<<<nb, 1024, sizeof(int) * E, st>>>(ids, P, E, p.group_blk, p.err);
+        cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess)
+            e = launch_pdl(k_group_scan, dim3(1), dim3(1024), sizeof(int) * (4 * (size_t)E + 8), st, nb, P, E, T,
+                           (int)p.cfg.has_shared, p.group_blk, p.offsets, p.poff, p.chunks, p.tiles, p.scratch,
+                           offsets_out, p.pad_pair, build_work ? 1 : 0, (int)p.rows_pad_max, p.tile_rows, p.err);
+        if (e == cudaSuccess)
+            e = launch_pdl(k_group_place, dim3(nb), dim3(1024), sizeof(int) * 35 * (size_t)E, st, (const int32_t *)ids,
+                           P, E, (const int32_t *)p.group_blk, (const int32_t *)p.offsets, (const int32_t *)p.poff,
+                           p.sorted, sorted_out, p.inv, p.pad_pair, (int)p.rows_pad_max, p.err);
+        return e;
+    }
     size_t smem = group_smem_bytes(E);
-    k_group<<<1, 1024, smem, st>>>(ids, T * k, E, T, k, p.cfg.has_shared, p.counts, p.offsets, p.poff, p.sorted,
+    k_group<<<1, 1024, smem, st>>>(ids, P, E, T, k, p.cfg.has_shared, p.counts, p.offsets, p.poff, p.sorted,
                                    p.inv, p.pad_pair, p.chunks, p.tiles, p.scratch, offsets_out, sorted_out,
                                    build_work ? 1 : 0, (int)p.rows_pad_max, p.tile_rows, p.err);
     return cudaGetLastError();
