@@ -123,28 +123,34 @@ __global__ void __launch_bounds__(kThreads) k_quant_h(const float *__restrict__ 
     const int shared_row0 = poff[E];
     const int rows = poff[E + 1];
     const int bpr = stride / 16;
-    const int64_t total = (int64_t)rows * bpr;
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
-        const int row = (int)(i / bpr), blk = (int)(i % bpr);
+    // one warp an item of 32 consecutive 16-value blocks of a row (a lane a
+    // block); an item of a padding row is skipped whole
+    const int lane = threadIdx.x & 31;
+    const int warps = (int)(gridDim.x * blockDim.x) >> 5;
+    const int nch = (bpr + 31) / 32;
+    for (int item = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); item < rows * nch; item += warps) {
+        const int row = item / nch, blk = (item - row * nch) * 32 + lane;
+        if (pad_pair[row] < 0) continue;   // warp-uniform
         const bool sh = row >= shared_row0;
-        if (blk * 16 >= (sh ? Is : I) || pad_pair[row] < 0) continue;
-        const float4 *p = reinterpret_cast<const float4 *>(h + (int64_t)row * stride + blk * 16);
-        float v[16];
+        if (blk < (sh ? Is : I) / 16) {
+            const float4 *p = reinterpret_cast<const float4 *>(h + (int64_t)row * stride + blk * 16);
+            float v[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            float4 q = p[j];
-            v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
-        }
-        uint2 c;
-        uint32_t s;
-        quant_block16(v, sh ? ts_s : ts_r, c, s);
-        codes[(int64_t)row * (stride / 16) + blk] = c;
-        if (atoms) {  // tensor-core scale layout: 512-byte atoms of 128 rows x 4 scales
-            const int rr = row & 127;
-            atoms[((int64_t)(row >> 7) * (stride / 64) + (blk >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (blk & 3)] =
-                (uint8_t)s;
-        } else {
-            scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+            for (int j = 0; j < 4; ++j) {
+                float4 q = p[j];
+                v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+            }
+            uint2 c;
+            uint32_t s;
+            quant_block16(v, sh ? ts_s : ts_r, c, s);
+            codes[(int64_t)row * (stride / 16) + blk] = c;
+            if (atoms) {  // tensor-core scale layout: 512-byte atoms of 128 rows x 4 scales
+                const int rr = row & 127;
+                atoms[((int64_t)(row >> 7) * (stride / 64) + (blk >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 + (blk & 3)] =
+                    (uint8_t)s;
+            } else {
+                scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+            }
         }
     }
 }
