@@ -156,6 +156,21 @@ def ncu_traffic(key: str, workload: str):
     return None
 
 
+def compute_dtype(w, path):
+    """The arithmetic the expert products run in: the CUDA-core engine multiplies
+    dequantised weights in fp32; the tensor-core and warp-MMA engines take f16
+    operands (W4A16: weights exact in f16, x scaled into range) or FP4 codes with
+    E4M3 block scales (W4A4), accumulating in fp32. For AUTO this follows the
+    library's rule: the tensor paths need H, I (and the shared expert's I) to be
+    multiples of 256, and W4A4 takes them from 64 (token, slot) pairs on."""
+    tc_ok = w.hidden % 256 == 0 and w.inter % 256 == 0 and w.shared_inter % 256 == 0
+    if path == "auto":
+        path = "tensor_core" if tc_ok and (w.mode == "w4a16" or w.tokens * w.top_k >= 64) else "cuda_core"
+    if path == "cuda_core":
+        return "fp32"
+    return "f16xf16->fp32" if w.mode == "w4a16" else "fp4xfp4->fp32"
+
+
 def algorithmic(w, ids_list):
     """Per-step algorithmic bytes of the gate/up and down kernels and flops,
     averaged over the instances (distinct experts touched come from routing)."""
@@ -377,7 +392,7 @@ def run_ours(args, w, world, rank, local):
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "fp32" if w.mode == "w4a16" else "fp4xfp4->fp32",
+        "scaling": "weak", "vs_baseline": None, "dtype": compute_dtype(w, args.path),
         "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to NVFP4 on device)",
         "config": {"workload": w.name, "description": w.description, "tokens": w.tokens, "hidden": w.hidden,
                    "experts": w.experts, "inter": w.inter, "top_k": w.top_k, "shared_inter": w.shared_inter,
