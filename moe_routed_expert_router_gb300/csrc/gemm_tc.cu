@@ -1352,7 +1352,11 @@ __device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b
 
 template <int EPI>
 __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
-    pdl_wait();      // routing, permute or gate/up results come from the previous kernel
+    // gate/up: the routing results come from the previous kernel. down: only
+    // its token rows (h) do, so only their producer waits (below); the weights,
+    // the work list and the routing weights were complete before the gate/up
+    // kernel passed its own wait, and the weight stream starts at once.
+    if (EPI != kScatter) pdl_wait();
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1409,6 +1413,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                 if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
         } else if (lane == 1 && !gather) {
             // ---------------------------------------- TMA producer of the token-row ring
+            pdl_wait();   // the token rows are the previous kernel's output
             RingPos b;
             bool ok = true;
             uint32_t used = 0, last_ph = 0;
