@@ -117,12 +117,13 @@ def _padded_layout(offsets, rows, E, T, P, shared, tile_rows, pad=128):
 
 @pytest.mark.parametrize("mode,T,path,tile_rows", [("w4a16", 1, "warp_mma", 32), ("w4a16", 16, "warp_mma", 32),
                                                    ("w4a16", 16, "tensor_core", 64), ("w4a4", 16, "tensor_core", 128),
-                                                   ("w4a4", 3, "cuda_core", 128), ("w4a4", 20, "tensor_core", 128)])
+                                                   ("w4a4", 3, "cuda_core", 128), ("w4a4", 20, "tensor_core", 128),
+                                                   ("w4a4", 300, "tensor_core", 128), ("w4a16", 300, "tensor_core", 64)])
 def test_forward_grouping_matches_oracle(mode, T, path, tile_rows):
     """The grouping moe_forward runs (inside the decode router's last block for
-    T <= 16, k_group above) against the oracle's grouping, bit for bit: expert
-    offsets, the stable order, the padded offsets, the padded row map and the
-    tile work list."""
+    T <= 16, k_group up to 2048 pairs, the multi-block grouping above) against
+    the oracle's grouping, bit for bit: expert offsets, the stable order, the
+    padded offsets, the padded row map and the tile work list."""
     from helpers import Case
     base = synth.WORKLOADS["decode4_w4a16"] if mode == "w4a16" else synth.WORKLOADS["verify16_w4a4"]
     w = synth.scaled(base, tokens=T, hidden=512, experts=48, inter=256, shared_inter=256)
@@ -144,3 +145,13 @@ def test_forward_grouping_matches_oracle(mode, T, path, tile_rows):
     np.testing.assert_array_equal(bufs["padded_offsets"][:E + 2], poff)
     np.testing.assert_array_equal(bufs["pad_pair"][:poff[-1]], pad_pair)
     np.testing.assert_array_equal(bufs["tiles"].reshape(-1, 4)[:len(tiles)], tiles)
+
+
+@pytest.mark.parametrize("T,E", [(256, 64), (257, 64), (300, 1024)])
+def test_route_grouping_around_the_multi_block_switch(T, E):
+    """Batches of up to 2048 (token, slot) pairs group in one block, larger ones
+    over blocks of 1024 pairs (per-block counts, scan, placement): both sides of
+    the switch, and the largest expert count (the placement's biggest shared
+    memory), against the oracle bit for bit."""
+    w = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=T, hidden=512, experts=E, top_k=8)
+    _check(w, synth.activations(w, 11, device="cuda"), synth.router_weight(w, 11, "cuda"), synth.router_bias(w, 11, "cuda"))
