@@ -398,13 +398,15 @@ __device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids,
     }
 }
 
-// Decode-sized batches (T <= 16), router and top-k in one launch: block e
-// computes expert e's logit for every token.  The router row (H fp32) is
-// staged in shared memory once; warp t streams token t's x row through its own
-// 4-deep cp.async ring of 1024-position slabs (512 for T > 8, so two blocks
-// fit an SM; the last slab ragged; 16-byte copies, no block barrier), lane l
-// taking positions 32j + l in increasing j.  Each block also checks a 1/E
-// slice of x (non-finite values, amax).  The last block to finish (a ticket in
+// Decode-sized batches (T <= 16), router and top-k in one launch: a block
+// computes the logits of one expert (two for T > 8 and an even E, so the x
+// rows streamed through the block serve two experts and half as many blocks
+// read them) for every token.  The router rows (H fp32 each) are staged in
+// shared memory once; warp t streams token t's x row through its own 4-deep
+// cp.async ring of 1024-position slabs (512 for T > 8; the last slab ragged;
+// 16-byte copies, no block barrier), lane l taking positions 32j + l in
+// increasing j, one fma chain an expert.  Each block also checks a slice of x
+// (non-finite values, amax).  The last block to finish (a ticket in
 // the per-call scratch) runs the top-k for all tokens, one warp a token, and,
 // in moe_forward, groups the pairs (group_small).
 constexpr int kDecodeRouterThreads = 512;
@@ -412,7 +414,12 @@ constexpr int kDSlab = 1024, kDStages = 4;
 
 __host__ __device__ __forceinline__ int decode_slab(int T) { return T <= 8 ? kDSlab : kDSlab / 2; }
 
-__host__ __device__ __forceinline__ size_t decode_router_smem(int H, int T) { return sizeof(float) * (size_t)H + (size_t)kDStages * T * decode_slab(T) * 2; }
+// Experts a block of the decode router takes.
+__host__ __device__ __forceinline__ int decode_epb(int T, int E) { return (T > 8 && E % 2 == 0) ? 2 : 1; }
+
+__host__ __device__ __forceinline__ size_t decode_router_smem(int H, int T, int E) {
+    return sizeof(float) * (size_t)H * decode_epb(T, E) + (size_t)kDStages * T * decode_slab(T) * 2;
+}
 
 template <int NPL>
 __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
@@ -425,12 +432,13 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     __shared__ int s_bad[kDecodeRouterThreads / 32];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int e = blockIdx.x;
+    const int epb = decode_epb(T, E), e = blockIdx.x * epb;   // this block's experts: e .. e + epb - 1
     const int slab = decode_slab(T);
     const int slabs = (H + slab - 1) / slab;
-    for (int c = tid; c < H / 4; c += kDecodeRouterThreads) cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
+    for (int c = tid; c < epb * H / 4; c += kDecodeRouterThreads)
+        cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
     asm volatile("cp.async.commit_group;" ::: "memory");
-    uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + H) + (size_t)warp * kDStages * slab;
+    uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + (size_t)epb * H) + (size_t)warp * kDStages * slab;
     const uint16_t *xr = x + (size_t)warp * H;
     auto load_x = [&](int sl) {   // warp-private: lane l copies 16-byte chunks lane + 32i of the slab
         if (sl < slabs) {
@@ -479,32 +487,57 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         }
     }
     if (warp < T) {
-        float acc = 0.0f;
+        float acc = 0.0f, acc1 = 0.0f;   // experts e and e + 1 (the second when epb == 2)
         for (int sl = 0; sl < slabs; ++sl) {
             load_x(sl + kDStages - 1);
             asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
             __syncwarp();
             const uint16_t *xs = ring + (sl % kDStages) * slab;
-            const float *wr = wrow + sl * slab;
+            const float *wr = wrow + sl * slab, *wr1 = wr + H;
             const int len = min(slab, H - sl * slab);   // a multiple of 256
-#pragma unroll 4
-            for (int j0 = 0; j0 < len / 32; j0 += 8) {   // loads of the group issue ahead of its FMA chain
-                uint32_t xv[8];
-                float wv[8];
+            if (epb == 2) {
+#pragma unroll 2
+                for (int j0 = 0; j0 < len / 32; j0 += 8) {   // loads of the group issue ahead of its FMA chains
+                    uint32_t xv[8];
+                    float wv[8], wv1[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    xv[j] = xs[32 * (j0 + j) + lane];
-                    wv[j] = wr[32 * (j0 + j) + lane];
+                    for (int j = 0; j < 8; ++j) {
+                        xv[j] = xs[32 * (j0 + j) + lane];
+                        wv[j] = wr[32 * (j0 + j) + lane];
+                        wv1[j] = wr1[32 * (j0 + j) + lane];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        acc = fmaf(__uint_as_float(xv[j] << 16), wv[j], acc);
+                        acc1 = fmaf(__uint_as_float(xv[j] << 16), wv1[j], acc1);
+                    }
                 }
+            } else {
+#pragma unroll 4
+                for (int j0 = 0; j0 < len / 32; j0 += 8) {   // loads of the group issue ahead of its FMA chain
+                    uint32_t xv[8];
+                    float wv[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc = fmaf(__uint_as_float(xv[j] << 16), wv[j], acc);
+                    for (int j = 0; j < 8; ++j) {
+                        xv[j] = xs[32 * (j0 + j) + lane];
+                        wv[j] = wr[32 * (j0 + j) + lane];
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc = fmaf(__uint_as_float(xv[j] << 16), wv[j], acc);
+                }
             }
             __syncwarp();   // every lane is done with the slot before it is refilled
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) logits[(size_t)warp * E + e] = bias ? acc + bias[e] : acc;
+        for (int o = 16; o >= 1; o >>= 1) {
+            acc = acc + __shfl_xor_sync(0xffffffffu, acc, o);
+            acc1 = acc1 + __shfl_xor_sync(0xffffffffu, acc1, o);
+        }
+        if (lane == 0) {
+            logits[(size_t)warp * E + e] = bias ? acc + bias[e] : acc;
+            if (epb == 2) logits[(size_t)warp * E + e + 1] = bias ? acc1 + bias[e + 1] : acc1;
+        }
     }
     if (grp.active) {   // every row of the padded map starts as padding; the last block fills in the pairs
         const int per = (grp.rows_cap + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -521,7 +554,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
     if (grp.active) {
         __syncthreads();   // the block's ids are visible to all its threads
-        int *gsm = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(wrow) + decode_router_smem(H, T));
+        int *gsm = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(wrow) + decode_router_smem(H, T, E));
         group_small(grp, ids, T * k, E, T, k, gsm, sc, err);
     }
 }
@@ -845,9 +878,9 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
             grp = GroupArgs{1, p.offsets, p.poff, p.sorted, p.inv, p.pad_pair, p.chunks, p.tiles,
                             (int)p.rows_pad_max, p.tile_rows, p.cfg.has_shared};
         }
-        const size_t smem = decode_router_smem(H, T) + (with_group ? group_small_smem(E, T * k) : 0);
+        const size_t smem = decode_router_smem(H, T, E) + (with_group ? group_small_smem(E, T * k) : 0);
 #define MOE_DEC(N)                                                                                           \
-    k_router_decode<N><<<E, kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router,          \
+    k_router_decode<N><<<E / decode_epb(T, E), kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router,          \
                                                               p.cfg.renormalize, p.logits, ids, wts, p.counts, \
                                                               p.scratch, p.err, grp)
         if (npl <= 1) MOE_DEC(1);
@@ -887,7 +920,7 @@ size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (siz
 cudaError_t configure_group_kernel(int E) {
     cudaError_t e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
     if (e != cudaSuccess) return e;
-    const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32) +
+    const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32, 2) +
                           group_small_smem(kMaxExperts, kDecodeRouterThreads / 32 * kMaxTopK));
     for (auto f : {k_router_decode<1>, k_router_decode<2>, k_router_decode<4>, k_router_decode<8>,
                    k_router_decode<16>, k_router_decode<32>}) {
