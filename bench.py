@@ -110,11 +110,11 @@ class ClockSampler:
 class Instance:
     """One seeded problem: device activations, router, NVFP4 weights."""
 
-    def __init__(self, moe, w, seed, batch=0):
+    def __init__(self, moe, w, seed, batch=0, device="cuda"):
         self.seed, self.batch = seed, batch
-        self.x = synth.activations(w, seed, batch, device="cuda")
-        self.rw = synth.router_weight(w, seed, device="cuda")
-        self.bias = synth.router_bias(w, seed, device="cuda")
+        self.x = synth.activations(w, seed, batch, device=device)
+        self.rw = synth.router_weight(w, seed, device=device)
+        self.bias = synth.router_bias(w, seed, device=device)
 
 
 def build_weights(moe, w, seed):
@@ -192,6 +192,12 @@ def algorithmic(w, ids_list):
 
 # ---------------------------------------------------------------- oracle (CPU)
 
+def _draw_device():
+    """Where the oracle's inputs are drawn: the GPU when there is one (the same
+    bytes the GPU run uses), else the host (the reference arm needs no GPU)."""
+    return "cuda" if torch.cuda.is_available() else "cpu"
+
+
 class OraclePrep:
     """Host copies of one instance and the oracle's own quantisation of every
     expert it touches (untimed preparation)."""
@@ -206,12 +212,12 @@ class OraclePrep:
         self.mode = oracle.MODE_W4A4 if w.mode == "w4a4" else oracle.MODE_W4A16
         self.route = oracle.route(self.xb, self.rw, self.bias, w.top_k, self.kind, w.renormalize)
         need = sorted(set(int(e) for e in np.unique(self.route["ids"])))
-        self.packed = {e: tuple(oracle.quantize(synth.expert_weight(w, inst.seed, e, p, device="cuda").cpu().numpy())
+        self.packed = {e: tuple(oracle.quantize(synth.expert_weight(w, inst.seed, e, p, device=_draw_device()).cpu().numpy())
                                 for p in PROJ) for e in need}
         self.shared = None
         if w.shared_inter:
             self.shared = tuple(oracle.quantize(
-                synth.expert_weight(w, inst.seed, "shared", p, device="cuda").cpu().numpy()) for p in PROJ)
+                synth.expert_weight(w, inst.seed, "shared", p, device=_draw_device()).cpu().numpy()) for p in PROJ)
         self.threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
     def full(self):
@@ -323,14 +329,16 @@ def run_ours(args, w, world, rank, local):
     # per-stage CUDA events inside the timed region, on every PROFILE_EVERY-th
     # step only: a timed event between two kernels makes the second wait for
     # the first to drain, which at decode sizes costs ~15% of the step
+    # (at most 400 profiled steps: the plan's event pool holds 4096 stage records)
+    every = max(PROFILE_EVERY, -(-args.steps // 400))
     profiled = 0
     barrier(world)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        on = i % PROFILE_EVERY == 0
-        if on or i % PROFILE_EVERY == 1:
+        on = i % every == 0
+        if on or i % every == 1:
             plan.set_profiling(on)
         profiled += on
         step(i)
@@ -426,7 +434,7 @@ def run_reference(args, w, world, rank):
     tokens/s = steps / pairs-per-token / time."""
     if rank != 0:
         return None
-    inst = Instance(None, w, w.seeds[0])
+    inst = Instance(None, w, w.seeds[0], device=_draw_device())
     prep = OraclePrep(w, inst)
     pairs = prep.pairs()
     for i in range(args.warmup):
@@ -451,7 +459,8 @@ def run_reference(args, w, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default 2000; 200 for --impl reference, whose steps are oracle calls)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="decode4_w4a16", choices=list(synth.WORKLOADS))
@@ -470,6 +479,8 @@ def main():
     if args.override:
         kv = dict(item.split("=") for item in args.override.split(","))
         w = synth.scaled(w, **{k: int(v) for k, v in kv.items()})
+    if args.steps is None:
+        args.steps = 200 if args.impl == "reference" else 2000
     if args.impl == "reference":
         world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
         if rank == 0:
