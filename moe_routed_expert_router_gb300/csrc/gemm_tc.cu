@@ -60,12 +60,14 @@ constexpr uint32_t kSfCol0 = 256;                 // scale-factor TMEM columns, 
 
 enum Epi { kSwiGLU = 0, kScatter = 1 };
 
-// Scale warps: four tcgen05.st writers (gate/up) or one shared-memory re-layout warp (down).
+// Warps by role: MMA issuers (gate/up one, down two) and scale warps (gate/up
+// four tcgen05.st writers, down one shared-memory re-layout warp), after the
+// producer warp; the 8 epilogue warps follow them.
 __host__ __device__ constexpr int mma_warps(int epi) { return epi == kSwiGLU ? 1 : 2; }
 __host__ __device__ constexpr int scale_warps(int epi) { return epi == kSwiGLU ? 4 : 1; }
 __host__ __device__ constexpr int epi_warp0(int epi) { return 1 + mma_warps(epi) + scale_warps(epi); }
 // TMEM scale columns a stage slot owns: A0, A1, B (gate/up, written by the
-// scale warps and read by both MMA lanes); A0, A1, B for MMA lane 0, B for MMA
+// scale warps and read by the MMA lane); A0, A1, B for MMA lane 0, B for MMA
 // lane 1 (down: each lane copies the atoms its own MMAs read, since copies and
 // MMAs issued by different threads are not ordered)
 __host__ __device__ constexpr int sf_stride(int epi) { return epi == kSwiGLU ? 48 : 64; }
