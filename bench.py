@@ -138,7 +138,6 @@ def build_weights(moe, w, seed):
     return routed, shared
 
 
-PROFILE_EVERY = 8
 
 
 def ncu_traffic(key: str, workload: str):
@@ -258,6 +257,99 @@ def oracle_baseline(w, inst, budget_s=15.0):
     return n * w.tokens / el, desc, prep.threads
 
 
+# ---------------------------------------------------------------- stage profile, roofline
+
+def profile_stages(plan, step, n_steps):
+    """Per-stage CUDA-event times (ms a launch) and kernel launches a step, from
+    a separate untimed pass of n_steps steps: events recorded between two
+    kernels make the second wait for the first, which would distort the timed
+    region, so they are never recorded there."""
+    plan.set_profiling(True)
+    plan.read_profile()
+    for i in range(n_steps):
+        step(i)
+    prof = plan.read_profile()
+    plan.set_profiling(False)
+    stage_ms = {k: v[0] / v[2] for k, v in prof.items() if v[2] > 0}
+    launches = sum(v[1] for v in prof.values()) / n_steps
+    return stage_ms, launches, n_steps
+
+
+def roofline(w, stage_ms, gu_bytes, dn_bytes, flops, pk, path):
+    """Roofline of the dominant stage: algorithmic bytes a launch / its mean
+    event time against the measured HBM copy bandwidth; for W4A4 also its FP4
+    flops against the dense NVFP4 peak (measured bf16 burst x 6, the nominal
+    ratio) and the ceiling the weight bytes put on that fraction."""
+    dom = max(stage_ms, key=stage_ms.get)
+    alg = {"gate_up": gu_bytes, "down": dn_bytes}
+    if dom not in alg:
+        return None
+    t = stage_ms[dom] / 1e3
+    ach = alg[dom] / t / 1e9
+    roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / pk["hbm_gbs"], 4), "traffic": ncu_traffic(f"{dom}:{path}", w.name),
+            "peak_source": pk["source"], "algorithmic_bytes_per_launch": round(alg[dom]),
+            "avg_launch_us": round(stage_ms[dom] * 1e3, 2)}
+    if w.mode == "w4a4":
+        fl = flops * (2.0 / 3.0 if dom == "gate_up" else 1.0 / 3.0)
+        peak = pk["bf16_tflops"] * 6 * 1e12
+        roof["fp4_tflops"] = round(fl / t / 1e12, 1)
+        roof["fp4_peak_tflops"] = round(peak / 1e12, 1)
+        roof["fp4_peak_source"] = "derived: measured bf16 burst x 6"
+        roof["fp4_frac"] = round(fl / t / peak, 4)
+        # weights alone take alg / BW: the best FP4 fraction that allows
+        roof["fp4_frac_weight_bound_ceiling"] = round(min(1.0, (fl / peak) / (alg[dom] / (pk["hbm_gbs"] * 1e9))), 4)
+    return roof
+
+
+def run_prefill(moe, pk, args, world, local):
+    """The 4096-token W4A4 prompt (H 7168, 256 experts, I 2048, top-8, sigmoid,
+    Zipf bias) timed in the same run: one seeded instance, W warm-up steps,
+    args.prefill_steps timed steps (each reads ~4 GB of expert weights, far more
+    than L2), then an untimed per-stage pass."""
+    w = synth.WORKLOADS["prompt4096_w4a4"]
+    routed, shared = build_weights(moe, w, 0)
+    inst = Instance(moe, w, 0)
+    plan = moe.Plan(w.hidden, w.inter, w.experts, w.top_k, w.tokens, router=moe.ROUTER_SIGMOID,
+                    renormalize=w.renormalize, mode=moe.W4A4, has_shared=False)
+    ids = plan.route(inst.x, inst.rw, inst.bias)["topk_ids"].cpu().numpy()
+    gu_bytes, dn_bytes, flops, distinct = algorithmic(w, [ids])
+    out = torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        plan.forward(inst.x, inst.rw, inst.bias, routed, shared, out=out)
+
+    clk = ClockSampler(local)
+    for i in range(max(3, args.warmup // 2)):
+        step(i)
+    if plan.sync_status() != moe.OK:
+        raise SystemExit("prefill moe_forward failed")
+    barrier(world)
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.prefill_steps):
+        step(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(t0.elapsed_time(t1), world) / args.prefill_steps
+    clocks = clk.stop()
+    if plan.sync_status() != moe.OK:
+        raise SystemExit("prefill moe_forward failed")
+    stage_ms, lps, n = profile_stages(plan, step, 3)
+    roof = roofline(w, {k: v for k, v in stage_ms.items() if k == "gate_up"}, gu_bytes, dn_bytes, flops, pk, "auto")
+    plan.close()
+    return {"workload": w.name, "description": w.description, "steps": args.prefill_steps,
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(world * w.tokens / (ms / 1e3), 1),
+            "step_fp4_tflops": round(flops / (ms / 1e3) / 1e12, 1),
+            "distinct_experts": distinct, "gate_up": roof,
+            "stages_us_per_step": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+            "gpu_launches_per_step": lps, "clocks": clocks,
+            "l2": "inputs larger than L2: each step streams the touched experts' weights (GBs)"}
+
+
 # ---------------------------------------------------------------- main arms
 
 def dist_init():
@@ -310,6 +402,7 @@ def run_ours(args, w, world, rank, local):
     plan.set_path({"auto": moe.PATH_AUTO, "cuda_core": moe.PATH_CUDA_CORE,
                    "tensor_core": moe.PATH_TENSOR_CORE, "warp_mma": moe.PATH_WARP_MMA}[args.path])
     ids_list = [plan.route(i.x, i.rw, i.bias)["topk_ids"].cpu().numpy() for i in insts]
+    first_inst = insts[0]
     gu_bytes, dn_bytes, flops, distinct = algorithmic(w, ids_list)
     outs = [torch.empty(w.tokens, w.hidden, dtype=torch.bfloat16, device="cuda") for _ in insts]
     stream = torch.cuda.current_stream()
@@ -325,33 +418,22 @@ def run_ours(args, w, world, rank, local):
     st = plan.sync_status()
     if st != moe.OK:
         raise SystemExit(f"moe_forward failed: {moe.STATUS[st]}")
-    plan.read_profile()
-    # per-stage CUDA events inside the timed region, on every PROFILE_EVERY-th
-    # step only: a timed event between two kernels makes the second wait for
-    # the first to drain, which at decode sizes costs ~15% of the step
-    # (at most 400 profiled steps: the plan's event pool holds 4096 stage records)
-    every = max(PROFILE_EVERY, -(-args.steps // 400))
-    profiled = 0
+    # the timed region: K plain moe_forward calls, nothing else on the stream
     barrier(world)
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        on = i % every == 0
-        if on or i % every == 1:
-            plan.set_profiling(on)
-        profiled += on
         step(i)
     t1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     ms = t0.elapsed_time(t1)
-    prof = plan.read_profile()
-    plan.set_profiling(False)
     st = plan.sync_status()
     if st != moe.OK:
         raise SystemExit(f"moe_forward failed: {moe.STATUS[st]}")
     ms = max_over_ranks(ms, world)
+    stage_ms, launches_per_step, profiled = profile_stages(plan, step, args.profile_steps)
 
     # end to end through the host-buffer entry point: H2D of x + D2H of out each step
     xh = [i.x.cpu().pin_memory() for i in insts]
@@ -378,27 +460,8 @@ def run_ours(args, w, world, rank, local):
 
     tokens = world * args.steps * w.tokens
     value = tokens / (ms / 1e3)
-    # dominant kernel by measured stage time
-    # mean event time of each stage over the profiled steps (each stage runs once a step)
-    stage_ms = {k: v[0] / profiled for k, v in prof.items() if v[2] > 0}
-    dom = max(stage_ms, key=stage_ms.get)
-    per_launch = dict(stage_ms)
-    alg = {"gate_up": gu_bytes, "down": dn_bytes}
-    roof = None
-    if dom in alg:
-        ach = alg[dom] / (per_launch[dom] / 1e3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": round(ach / pk["hbm_gbs"], 4), "traffic": ncu_traffic(f"{dom}:{args.path}", w.name),
-                "peak_source": pk["source"], "algorithmic_bytes_per_launch": round(alg[dom]),
-                "avg_launch_us": round(per_launch[dom] * 1e3, 2)}
-        if w.mode == "w4a4":
-            # the FP4 tensor roof beside the HBM one: dense NVFP4 peak = measured bf16 x 6 (nominal ratio)
-            fl = flops * (2.0 / 3.0 if dom == "gate_up" else 1.0 / 3.0)
-            tf = fl / (per_launch[dom] / 1e3) / 1e12
-            roof["fp4_tflops"] = round(tf, 1)
-            roof["fp4_peak_tflops"] = round(pk["bf16_tflops"] * 6, 1)
-            roof["fp4_frac"] = round(tf / (pk["bf16_tflops"] * 6), 4)
-    launches = sum(v[1] for v in prof.values())
+    roof = roofline(w, stage_ms, gu_bytes, dn_bytes, flops, pk, args.path)
+    launches = round(launches_per_step * args.steps)
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 5), "higher_is_better": True,
@@ -416,14 +479,18 @@ def run_ours(args, w, world, rank, local):
         "roofline": roof,
         "stages_us_per_step": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
         "stages_profiled_steps": profiled,
+        "stages_note": "per-stage CUDA events from a separate untimed pass after the timed region",
         "hbm_gbs_whole_step": round((gu_bytes + dn_bytes) / (ms / args.steps / 1e3) / 1e9, 1),
         "clocks": clocks,
     }
+    plan.close()
+    del weights, insts, outs
+    if args.prefill and w.name != "prompt4096_w4a4":
+        res["prefill"] = run_prefill(moe, pk, args, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, desc, thr = oracle_baseline(w, insts[0], args.cpu_budget)
+        v, desc, thr = oracle_baseline(w, first_inst, args.cpu_budget)
         res["cpu_baseline"] = {"value": round(v, 3), "unit": "tokens/s", "cores": thr, "kind": "oracle",
                                "sample": desc}
-    plan.close()
     return res
 
 
@@ -456,6 +523,18 @@ def run_reference(args, w, world, rank):
             "e2e": {"value": round(v, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def relaunch(n):
+    """--gpus N outside a launcher: run this same command as N replica
+    processes, one a GPU, under torch.distributed.run on 127.0.0.1."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + sys.argv[1:]
+    raise SystemExit(subprocess.call(cmd))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -472,6 +551,12 @@ def main():
                     help="comma-separated workload fields for a scaled-down profiling run, e.g. tokens=1024,experts=64")
     ap.add_argument("--instances", type=int, default=0,
                     help="use only the first N seeded instances / batches (0 = all; for small profiling runs)")
+    ap.add_argument("--profile-steps", type=int, default=32,
+                    help="steps of the untimed per-stage pass after the timed region")
+    ap.add_argument("--prefill-steps", type=int, default=10,
+                    help="timed steps of the 4096-token W4A4 prompt sub-record")
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false",
+                    help="skip the 4096-token W4A4 prompt sub-record")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -488,6 +573,10 @@ def main():
             res = run_reference(args, w, world, rank)
             print(json.dumps(res), flush=True)
         return
+    if args.gpus > 1 and int(os.environ.get("WORLD_SIZE", "1")) == 1:
+        relaunch(args.gpus)
+    if args.gpus != int(os.environ.get("WORLD_SIZE", "1")):
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={os.environ.get('WORLD_SIZE')}")
     world, rank, local = dist_init()
     res = run_ours(args, w, world, rank, local)
     if rank == 0:

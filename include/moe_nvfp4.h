@@ -127,7 +127,7 @@ moe_status moe_plan_destroy(moe_plan plan);
  *   sorted_rows    [T*k] int32, pair indices t*k+j grouped by expert, each
  *                  expert's pairs in increasing t*k+j
  * Logits are fp32 with a fixed order: position h of the H dimension belongs to
- * lane (h/8) mod 32, each lane sums fmaf in increasing h from +0, the 32 lane
+ * lane h mod 32, each lane sums fmaf in increasing h from +0, the 32 lane
  * sums are combined by an xor butterfly over offsets 16, 8, 4, 2, 1, and the
  * bias is added last.  Indices and offsets are therefore reproducible bit for
  * bit. */
@@ -169,13 +169,26 @@ moe_status moe_quantize_act(moe_plan plan, const void *x_bf16, int32_t T, uint8_
 moe_status moe_quantize_nvfp4(const float *w, int32_t batch, int32_t rows, int32_t cols,
                               uint8_t *codes, uint8_t *scales, float *tensor_scale, void *stream);
 
+/* Test hook: the device's fp32 -> E4M3 and fp32 -> E2M1 conversions, exactly
+ * as the quantisers above apply them (round to nearest even, saturating to the
+ * largest finite value; the sign is kept).  For every i < n, dst[i] =
+ *   format MOE_FMT_E4M3: the E4M3 byte of src[i];
+ *   format MOE_FMT_E2M1: the 4-bit E2M1 code of src[i] in bits 0..3.
+ * src [n] fp32 and dst [n] uint8 are device memory (src 16-byte aligned).
+ * Needs no plan.  MOE_ERR_INVALID_ARG for an unknown format or n < 0. */
+typedef enum { MOE_FMT_E4M3 = 0, MOE_FMT_E2M1 = 1 } moe_format;
+moe_status moe_convert_f32(const float *src, int64_t n, int32_t format, uint8_t *dst, void *stream);
+
 /* Synchronise `stream`, then return and clear the plan's device error word
  * (MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE). */
 moe_status moe_plan_sync_status(moe_plan plan, void *stream);
 
 /* Device address and size of a plan workspace buffer, for tests that check a
- * step in isolation.  name: "h_codes", "h_scales", "h_ts", "x_ts", "acc",
- * "counts", "padded_offsets", "offsets", "sorted", "pad_pair", "tiles", "h".
+ * step in isolation.  name: "h_codes", "h_scales", "h_scale_atoms" (W4A4 on
+ * the tensor cores: the SwiGLU scales in 512-byte atoms of 128 rows x 4
+ * blocks, byte (r % 32) * 16 + (r % 128 / 32) * 4 + b % 4 of atom
+ * (r / 128, b / 4)), "h_ts", "x_ts", "acc", "counts", "padded_offsets",
+ * "offsets", "sorted", "pad_pair", "tiles", "h".
  * Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 

@@ -28,7 +28,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_NONFINITE, ERR_T
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_route", "moe_forward", "moe_forward_host",
            "moe_quantize_act", "moe_quantize_nvfp4", "moe_plan_sync_status", "moe_plan_debug_buffer",
            "moe_plan_set_profiling", "moe_plan_read_profile", "moe_plan_set_path", "moe_plan_check_timeout",
-           "moe_route_static", "moe_status_string", "moe_version"]
+           "moe_route_static", "moe_convert_f32", "moe_status_string", "moe_version"]
+FMT_E4M3, FMT_E2M1 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_WARP_MMA = 0, 1, 2, 3
 STAGES = ["route", "group", "quant_x", "permute", "gate_up", "quant_h", "down", "finalize"]
 
@@ -78,6 +79,7 @@ def lib():
         L.moe_plan_check_timeout.argtypes = [P, ctypes.c_int64, P]
         L.moe_route_static.argtypes = [P, I32, I32, P, P, I32, I32, I32, I32, P, P, P, P, P]
         L.moe_plan_read_profile.argtypes = [P, P, P, P]
+        L.moe_convert_f32.argtypes = [P, ctypes.c_int64, I32, P, P]
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_version.restype = ctypes.c_char_p
@@ -137,6 +139,15 @@ def quantize_nvfp4(w: torch.Tensor, out: NvfpTensor | None = None, stream=None) 
                          torch.empty(b, dtype=torch.float32, device=w.device))
     _check(lib().moe_quantize_nvfp4(_ptr(w), b, r, c, _ptr(out.codes), _ptr(out.scales), _ptr(out.ts),
                                     _stream(stream)), "moe_quantize_nvfp4")
+    return out
+
+
+def convert_f32(src: torch.Tensor, fmt: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The device's fp32 -> E4M3 byte (FMT_E4M3) or E2M1 code (FMT_E2M1) conversion, element-wise."""
+    assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.uint8, device=src.device)
+    _check(lib().moe_convert_f32(_ptr(src), src.numel(), fmt, _ptr(out), _stream(stream)), "moe_convert_f32")
     return out
 
 

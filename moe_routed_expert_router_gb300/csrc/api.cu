@@ -11,7 +11,7 @@
 
 namespace moe {
 size_t group_smem_bytes(int E);
-cudaError_t configure_group_kernel(int E);
+cudaError_t configure_group_kernel();
 cudaError_t configure_tc(const Plan &p);
 cudaError_t configure_simt();
 bool tc_supported(const Plan &p);
@@ -279,7 +279,7 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
     real.base = static_cast<char *>(p.ws);
     carve(p, real);
     cudaError_t e = cudaMemset(p.ws, 0, p.ws_bytes);
-    if (e == cudaSuccess) e = moe::configure_group_kernel(cfg->num_experts);
+    if (e == cudaSuccess) e = moe::configure_group_kernel();
     if (e == cudaSuccess) e = moe::configure_simt();
     if (e == cudaSuccess && moe::tc_supported(p)) e = moe::configure_tc(p);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -417,6 +417,14 @@ moe_status moe_quantize_nvfp4(const float *w, int32_t batch, int32_t rows, int32
                                                static_cast<cudaStream_t>(stream)));
 }
 
+moe_status moe_convert_f32(const float *src, int64_t n, int32_t format, uint8_t *dst, void *stream) {
+    if (n < 0 || (format != MOE_FMT_E4M3 && format != MOE_FMT_E2M1)) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    if (!src || !dst) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(src)) return MOE_ERR_MISALIGNED;
+    return cuda_status(moe::launch_convert(src, n, format, dst, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status moe_plan_sync_status(moe_plan plan, void *stream) {
     if (!plan) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -442,6 +450,7 @@ moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, si
     struct Item { const char *n; void *p; size_t b; } items[] = {
         {"h_codes", p.hq, (size_t)(p.rows_pad_max * Imax / 2)},
         {"h_scales", p.hsc, (size_t)(p.rows_pad_max * Imax / 16)},
+        {"h_scale_atoms", p.hq_atoms, p.hq_atoms ? (size_t)(p.rows_pad_max * Imax / 16) : 0},
         {"h_ts", p.hts, 2 * sizeof(float)},
         {"x_ts", p.xts, sizeof(float)},
         {"acc", p.acc, sizeof(float) * (size_t)p.cfg.max_tokens * p.cfg.hidden},

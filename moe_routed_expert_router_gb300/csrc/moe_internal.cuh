@@ -25,6 +25,8 @@ constexpr int kGroupSeg = 1024;
 constexpr int kTailPartFloats = 8 * 4 * 32 * 8;
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopK = 32;
+// Devices a process may use (per-device one-time set-up tables).
+constexpr int kMaxDevices = 64;
 
 // Device error bits (plan error word).
 constexpr int kErrNonFinite = 1;
@@ -127,7 +129,7 @@ __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t h2) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h2));
 }
 
-// fp32 >= 0 -> E4M3 byte, round to nearest even, saturating at 448.
+// fp32 -> E4M3 byte (sign kept), round to nearest even, saturating at +-448.
 __device__ __forceinline__ uint32_t f32_to_e4m3_sat(float v) {
     uint32_t out;
     asm("{\n\t.reg .b16 h;\n\tcvt.rn.satfinite.e4m3x2.f32 h, %2, %1;\n\tcvt.u32.u16 %0, h;\n\t}"
@@ -284,6 +286,7 @@ cudaError_t launch_quant_nvfp4(const float *w, int batch, int rows, int cols, ui
 cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtrs &routed,
                             const ExpertPtrs *shared, int part, cudaStream_t st);
 cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st);
+cudaError_t launch_convert(const float *src, int64_t n, int format, uint8_t *dst, cudaStream_t st);
 cudaError_t launch_finalize(const Plan &p, int T, void *out, cudaStream_t st);
 cudaError_t launch_wait_check(int *err, uint64_t limit_ns, cudaStream_t st);
 

@@ -7,7 +7,7 @@
 #include "moe_internal.cuh"
 
 namespace moe {
-cudaError_t configure_group_kernel(int E);
+cudaError_t configure_group_kernel();
 }
 
 namespace {
@@ -32,21 +32,20 @@ struct StaticScratch {
 // One copy per device that loads the library, kept until the process exits.
 static __device__ __align__(256) StaticScratch g_route_scratch;
 
-constexpr int kMaxDevices = 64;
-StaticScratch *g_addr[kMaxDevices] = {};
-int g_sms[kMaxDevices] = {};
+StaticScratch *g_addr[moe::kMaxDevices] = {};
+int g_sms[moe::kMaxDevices] = {};
 std::mutex g_mu;
 
 // Device address of the array on the current device (looked up once per
 // device; host code must not use the symbol itself as an address).
 moe_status static_scratch(StaticScratch **out, int *sms) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= moe::kMaxDevices) return MOE_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_addr[dev]) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_route_scratch) != cudaSuccess) return MOE_ERR_CUDA;
-        if (moe::configure_group_kernel(kStaticMaxExperts) != cudaSuccess) return MOE_ERR_CUDA;
+        if (moe::configure_group_kernel() != cudaSuccess) return MOE_ERR_CUDA;
         int n = 0;
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
         g_sms[dev] = n;

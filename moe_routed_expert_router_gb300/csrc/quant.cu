@@ -155,6 +155,16 @@ __global__ void __launch_bounds__(kThreads) k_quant_h(const float *__restrict__ 
     }
 }
 
+// The element conversions of quant_block16 on their own (moe_convert_f32):
+// format 0 E4M3 byte, format 1 E2M1 code (low nibble).
+__global__ void __launch_bounds__(kThreads) k_convert(const float *__restrict__ src, int64_t n, int format,
+                                                     uint8_t *__restrict__ dst) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = src[i];
+        dst[i] = (uint8_t)(format == 0 ? f32_to_e4m3_sat(v) : (f32x2_to_e2m1x2(v, 0.0f) & 0xFu));
+    }
+}
+
 // out = bf16_rne(acc); acc = 0 (so the next call starts from zero).
 __global__ void __launch_bounds__(kThreads) k_finalize(float4 *__restrict__ acc, uint2 *__restrict__ out, int64_t n4) {
     pdl_wait();      // the down GEMM's scatter-adds are complete
@@ -216,6 +226,11 @@ cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st) {
                                                   p.cfg.shared_inter, p.pad_pair, p.scratch,
                                                   reinterpret_cast<uint2 *>(p.hq), p.hsc,
                                                   tc_layout ? p.hq_atoms : nullptr, p.hts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_convert(const float *src, int64_t n, int format, uint8_t *dst, cudaStream_t st) {
+    k_convert<<<grid_for(n, device_sms()), kThreads, 0, st>>>(src, n, format, dst);
     return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 // From our contributors: normalisation policy as a named value, #772).
 // Grouping (same page and section, #740: a whole batch is routed in one run so
 // each routed expert's weights are read once).
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -917,8 +919,21 @@ bool router_groups(int T) { return T <= kDecodeRouterThreads / 32; }
 
 size_t group_smem_bytes(int E) { return sizeof(int) * (32 * (size_t)E + 4 * (size_t)E + 8); }
 
-cudaError_t configure_group_kernel(int E) {
-    cudaError_t e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
+// The routing kernels' dynamic shared-memory limits are per-function, per-device
+// attributes shared by every plan and by moe_route_static.  They are set once
+// a device, for the largest sizes any call may ask for (kMaxExperts experts,
+// the decode router at H = 8192), so a later call can never lower a limit that
+// an earlier plan or a static call still relies on.
+cudaError_t configure_group_kernel() {
+    static std::mutex mu;
+    static bool done[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return cudaSuccess;
+    e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
     if (e != cudaSuccess) return e;
     const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32, 2) +
                           group_small_smem(kMaxExperts, kDecodeRouterThreads / 32 * kMaxTopK));
@@ -927,9 +942,12 @@ cudaError_t configure_group_kernel(int E) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
         if (e != cudaSuccess) return e;
     }
-    e = cudaFuncSetAttribute(k_group_place, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(sizeof(int) * 35 * (size_t)E));
+    e = cudaFuncSetAttribute(k_group_place, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(int) * 35 * (size_t)kMaxExperts));
     if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(E));
+    e = cudaFuncSetAttribute(k_group, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)group_smem_bytes(kMaxExperts));
+    if (e == cudaSuccess) done[dev] = true;
+    return e;
 }
 
 // Launches of launch_group: three (count, scan, place) for batches larger than

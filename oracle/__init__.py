@@ -303,13 +303,40 @@ def quantize_activations(x_bf16: np.ndarray):
     return quantize(xf)
 
 
+def swiglu_tensor_scale(h_list) -> float:
+    """W4A4 tensor scale of a set of SwiGLU output matrices: the amax over all
+    of them (each rounded to fp32 first), divided by 6 * 448 in fp32.  The
+    routed rows of a batch form one set, the shared expert's rows another."""
+    amax = np.float32(0.0)
+    for h in h_list:
+        if np.asarray(h).size:
+            amax = max(amax, np.float32(np.max(np.abs(np.asarray(h, np.float32)))))
+    return float(np.float32(np.float32(amax) / np.float32(2688.0)))
+
+
+def swiglu_quantize(h_list):
+    """W4A4: NVFP4 quantisation of one set of SwiGLU output matrices with their
+    shared tensor scale.  Returns ([(codes, scales)], ts)."""
+    ts = swiglu_tensor_scale(h_list)
+    out = []
+    for h in h_list:
+        c, sc, _ = quantize(np.asarray(h, np.float32), ts)
+        out.append((c, sc))
+    return out, ts
+
+
 def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormalize=True,
-            mode=MODE_W4A16, shared=None, keep=False):
+            mode=MODE_W4A16, shared=None, keep=False, h_in=None):
     """The whole MoE FFN in FP64.
 
     expert(e) -> ((gc, gs, gts), (uc, us, uts), (dc, ds, dts)): expert e's packed
     NVFP4 gate [I][H], up [I][H] and down [H][I] (the oracle's own quantisation).
     shared: None or the same triple for the shared expert (weight 1, every token).
+    h_in: None, or given SwiGLU outputs to run the rest of the path on (a
+    stage-isolated check): {e: [rows of expert e in grouped order][I]} for every
+    routed expert the batch touches, plus "shared": [T][Is] when a shared expert
+    is given.  The oracle then skips the gate/up products and rounds or
+    quantises these h values by the mode's rule, then runs down and combine.
     Returns a dict with the route, the FP64 output and its bf16 bit patterns.
     """
     x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
@@ -348,8 +375,7 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax.
         Also returns, per matrix, the flip band of its near-boundary decisions."""
         h32 = [h.astype(np.float32) for h in h_all]
-        amax = max((float(np.max(np.abs(h))) for h in h32 if h.size), default=0.0)
-        ts = float(np.float32(np.float32(amax) / np.float32(2688.0)))
+        ts = swiglu_tensor_scale(h32)
         qs = [quant_decisions(h, ts) for h in h32]
         return [q[0] for q in qs], ts, [q[1] for q in qs], sum(q[2] for q in qs)
 
@@ -357,7 +383,11 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
     hs = {}
     for e in active:
         pr = rows[offsets[e]:offsets[e + 1]]
-        hs[e] = up_part(expert(e), xin[pr // k])
+        if h_in is not None:
+            hs[e] = np.asarray(h_in[e], np.float64 if mode == MODE_W4A16 else np.float32)
+            assert hs[e].shape[0] == pr.size
+        else:
+            hs[e] = up_part(expert(e), xin[pr // k])
     band = np.zeros((T, H), np.float64)    # W4A4: what near-boundary h decisions could move
     flips = {}
     n_flip = 0
@@ -379,7 +409,7 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
             np.add.at(band, pr // k, np.abs(wflat[pr])[:, None] * (flips[e] @ np.abs(dequantize(dc, ds, dts)).T))
 
     if shared is not None:
-        hsh = up_part(shared, xin)
+        hsh = np.asarray(h_in["shared"]) if h_in is not None else up_part(shared, xin)
         if mode == MODE_W4A4:
             (hsh,), ts_s, (fs,), ns = quant_h([hsh])
             n_flip += ns

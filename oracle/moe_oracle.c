@@ -221,8 +221,8 @@ void oracle_nvfp4_quantize(const float *x, int64_t rows, int64_t cols, float ts,
 
 /* Router logits l[t][e] = x[t] . Wr[e] (+ bias[e]) in fp32, in a fixed order
  * that a warp can reproduce exactly:
- *   - the H positions are dealt to 32 lanes in chunks of 8: position h
- *     belongs to lane (h / 8) mod 32;
+ *   - the H positions are dealt to 32 lanes one at a time: position h
+ *     belongs to lane h mod 32;
  *   - each lane sums fmaf(x[h], w[h], acc) over its positions in increasing h,
  *     starting from +0;
  *   - the 32 partial sums are combined by a butterfly: for offset 16, 8, 4,

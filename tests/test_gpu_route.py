@@ -155,3 +155,29 @@ def test_route_grouping_around_the_multi_block_switch(T, E):
     memory), against the oracle bit for bit."""
     w = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=T, hidden=512, experts=E, top_k=8)
     _check(w, synth.activations(w, 11, device="cuda"), synth.router_weight(w, 11, "cuda"), synth.router_bias(w, 11, "cuda"))
+
+
+def test_coexisting_plans_with_different_expert_counts():
+    """Two live plans, 256 and 8 experts: the one created first still groups
+    (one-block grouping, whose shared memory grows with the expert count) after
+    the second exists, and both match the oracle."""
+    big = synth.scaled(synth.WORKLOADS["prompt4096_w4a4"], tokens=200, hidden=512)
+    small = synth.scaled(synth.WORKLOADS["tiny_w4a16"], tokens=40)
+    xb, rb, bb = synth.activations(big, 5, device="cuda"), synth.router_weight(big, 5, "cuda"), \
+        synth.router_bias(big, 5, "cuda")
+    xs, rs = synth.activations(small, 5, device="cuda"), synth.router_weight(small, 5, "cuda")
+    with plan_for(big) as p_big, plan_for(small) as p_small:
+        for _ in range(2):
+            got_b = p_big.route(xb, rb, bb)
+            assert p_big.sync_status() == moe.OK
+            got_s = p_small.route(xs, rs)
+            assert p_small.sync_status() == moe.OK
+        for w, x, rw, bias, got in ((big, xb, rb, bb, got_b), (small, xs, rs, None, got_s)):
+            ref = oracle.route(x.cpu().view(torch.int16).numpy().view(np.uint16), rw.cpu().numpy(),
+                               None if bias is None else bias.cpu().numpy(), w.top_k,
+                               oracle.ROUTER_SIGMOID if w.router == "sigmoid" else oracle.ROUTER_SOFTMAX,
+                               w.renormalize)
+            np.testing.assert_array_equal(got["topk_ids"].cpu().numpy(), ref["ids"])
+            np.testing.assert_array_equal(got["expert_offsets"].cpu().numpy(), ref["offsets"])
+            np.testing.assert_array_equal(got["sorted_rows"].cpu().numpy()[:ref["sorted_rows"].size],
+                                          ref["sorted_rows"])

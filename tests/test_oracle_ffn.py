@@ -125,3 +125,46 @@ def test_w4a4_quantises_x_and_h_with_batch_tensor_scales():
     # 4-bit activations move the output by quantisation noise only
     rel = np.linalg.norm(r4["out"] - r16["out"]) / np.linalg.norm(r16["out"])
     assert 1e-4 < rel < 0.3
+
+
+def test_w4a4_hand_worked_swiglu_tensor_scales():
+    """W4A4 by hand, 2 tokens, 2 routed experts (top-1) and a shared expert,
+    with every value on the NVFP4 grid so each step is exact.  Pins the SwiGLU
+    quantiser's tensor scale: the amax over ALL routed rows / 2688 for the
+    routed experts (3528 / 2688 = 1.3125), the shared expert's own rows for its
+    own scale (10584 / 2688 = 3.9375).  A per-expert amax, a routed amax that
+    took in the shared rows, or another divisor each change the output."""
+    H = I = 16
+    x = np.zeros((2, H), np.uint16)
+    x[0, 0] = x[1, 1] = int(oracle.f64_to_bf16(np.array([2688.0]))[0])   # amax 2688: x tensor scale 1
+    wr = np.zeros((2, H), np.float32)
+    wr[0, 0] = wr[1, 1] = 1.0                         # token 0 -> expert 0, token 1 -> expert 1
+    ts_gu, ts_d = 2.0 ** -6, 2.0 ** -10
+    experts = {
+        # g = 2688 * 1 / 64 = 42 (silu(42) = 42 in FP64), u = 2688 * 2 / 64 = 84: h[0] = 3528
+        0: (_packed(I, H, {(0, 0): 2}, ts=ts_gu), _packed(I, H, {(0, 0): 4}, ts=ts_gu),
+            _packed(H, I, {(0, 0): 2, (1, 0): 9}, ts=ts_d)),          # Wd[0][0] = 1, Wd[1][0] = -0.5
+        # g = 42, u = 2688 * 1.5 / 64 = 63: h[3] = 2646
+        1: (_packed(I, H, {(3, 1): 2}, ts=ts_gu), _packed(I, H, {(3, 1): 3}, ts=ts_gu),
+            _packed(H, I, {(2, 3): 4}, ts=ts_d)),                     # Wd[2][3] = 2
+    }
+    # shared: token 0 g = 63, u = 168 (h[5] = 10584); token 1 g = 42, u = 42 (h[5] = 1764)
+    shared = (_packed(I, H, {(5, 0): 3, (5, 1): 2}, ts=ts_gu), _packed(I, H, {(5, 0): 6, (5, 1): 2}, ts=ts_gu),
+              _packed(H, I, {(4, 5): 2}, ts=ts_d))                    # Wd[4][5] = 1
+    r = oracle.forward(x, wr, None, lambda e: experts[e], k=1, router_kind=oracle.ROUTER_SOFTMAX,
+                       mode=oracle.MODE_W4A4, shared=shared, keep=True)
+    assert r["ids"].tolist() == [[0], [1]] and r["weights"].tolist() == [[1.0], [1.0]]
+    assert r["x_ts"] == 1.0
+    assert r["h_ts"] == 1.3125 and r["shared_h_ts"] == 3.9375
+    # routed h, quantised with ts 1.3125:
+    #   3528: s = E4M3((3528/6)/1.3125 = 448) = 448, den = 588, code 6 -> 3528
+    #   2646: (2646/6)/1.3125 = 336, a tie between 320 and 352 -> 320 (even), den = 420,
+    #         2646/420 = 6.3 saturates to 6 -> 6 * 320 * 1.3125 = 2520
+    # shared h, ts 3.9375: 10584 -> 10584; 1764: (1764/6)/3.9375 = 74.67 -> 72, den = 283.5,
+    #         1764/283.5 = 6.22 -> 6 -> 6 * 72 * 3.9375 = 1701
+    assert r["h"][0][0, 0] == 3528.0 and r["h"][1][0, 3] == 2520.0
+    want = np.zeros((2, H))
+    want[0, 0], want[0, 1] = 3528.0 / 1024, -0.5 * 3528.0 / 1024
+    want[1, 2] = 2 * 2520.0 / 1024
+    want[0, 4], want[1, 4] = 10584.0 / 1024, 1701.0 / 1024
+    np.testing.assert_array_equal(r["out"], want)

@@ -35,20 +35,50 @@ def _static_route(w, x, rw, bias):
     return out
 
 
+def _same(got, ref):
+    # the same router and grouping kernels on the same inputs: every output,
+    # the routing weights included, bit for bit
+    for key in ("topk_ids", "topk_w", "expert_offsets", "sorted_rows"):
+        assert torch.equal(got[key], ref[key]), key
+
+
+@pytest.mark.parametrize("static_first", [False, True])
 @pytest.mark.parametrize("name", ["decode4_w4a16", "prompt4096_w4a4"])
-def test_static_route_matches_plan_route_twice(name):
+def test_static_route_matches_plan_route_twice(name, static_first):
     w = synth.WORKLOADS[name]
     with plan_for(w) as plan:
         for seed in (0, 1):   # two calls in a row through the shared array
             x = synth.activations(w, seed, device="cuda")
             rw = synth.router_weight(w, seed, "cuda")
             bias = synth.router_bias(w, seed, "cuda")
+            if static_first:   # nothing the static array holds carries over into a later call
+                got = _static_route(w, x, rw, bias)
             ref = plan.route(x, rw, bias)
             assert plan.sync_status() == moe.OK
-            got = _static_route(w, x, rw, bias)
-            for key in ("topk_ids", "expert_offsets", "sorted_rows"):
-                assert torch.equal(got[key], ref[key]), key
-            np.testing.assert_allclose(got["topk_w"].cpu().numpy(), ref["topk_w"].cpu().numpy(), rtol=2e-6, atol=1e-7)
+            if not static_first:
+                got = _static_route(w, x, rw, bias)
+            _same(got, ref)
+
+
+def test_static_route_after_a_plan_with_fewer_experts():
+    """The routing kernels' shared-memory limits are device-wide: a plan created
+    for 8 experts between two static calls for 256 experts must not lower them."""
+    w = synth.WORKLOADS["prompt4096_w4a4"]
+    x = synth.activations(w, 2, device="cuda")
+    rw = synth.router_weight(w, 2, "cuda")
+    bias = synth.router_bias(w, 2, "cuda")
+    first = _static_route(w, x, rw, bias)
+    small = synth.scaled(synth.WORKLOADS["tiny_w4a16"], tokens=4)
+    with plan_for(small) as tiny:
+        xs = synth.activations(small, 0, device="cuda")
+        tiny.route(xs, synth.router_weight(small, 0, "cuda"))
+        assert tiny.sync_status() == moe.OK
+        again = _static_route(w, x, rw, bias)
+    _same(again, first)
+    with plan_for(w) as plan:
+        ref = plan.route(x, rw, bias)
+        assert plan.sync_status() == moe.OK
+    _same(first, ref)
 
 
 def test_static_route_rejects_sizes_beyond_its_array():
