@@ -69,6 +69,13 @@ typedef enum {
 
 typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router_kind;
 
+/* Word type of the router weight: fp32, or the checkpoint's bf16 words read
+ * as they are stored ("NVIDIA FP4-Local checkpoints on DGX Spark ... #565",
+ * section 4 Round 1: the router kept in its BF16 words, #732).  A bf16 word
+ * widens to fp32 exactly, so the logits keep the fixed fp32 order below; the
+ * router reads half the bytes. */
+typedef enum { MOE_ROUTER_F32 = 0, MOE_ROUTER_BF16 = 1 } moe_router_dtype;
+
 /* W4A16: activations stay bf16; the SwiGLU output is rounded to bf16 (RNE)
  *        before the down product.
  * W4A4:  activations are NVFP4-quantised (tensor scale from the batch amax);
@@ -88,6 +95,7 @@ typedef struct {
     int32_t mode;         /* moe_mode */
     int32_t has_shared;   /* 1: a shared expert is added to every token */
     int32_t shared_inter; /* shared expert's intermediate (multiple of 128, at most 8192) */
+    int32_t router_dtype; /* moe_router_dtype of router_w in moe_route / moe_forward */
 } moe_config;
 
 /* One NVFP4 weight stacked over `count` experts: codes [count][N][K/2],
@@ -117,7 +125,8 @@ moe_status moe_plan_destroy(moe_plan plan);
 
 /* Router + grouping only (the steps "route" and "group by expert").
  *   x_bf16      [T][H] bf16 activations
- *   router_w    [E][H] fp32
+ *   router_w    [E][H] fp32, or bf16 words when cfg.router_dtype is
+ *               MOE_ROUTER_BF16 (16-byte aligned either way)
  *   router_bias [E] fp32 or NULL; added to the logits, so it moves both the
  *               selection and the weights
  * Outputs (device, caller-owned):
@@ -131,7 +140,7 @@ moe_status moe_plan_destroy(moe_plan plan);
  * sums are combined by an xor butterfly over offsets 16, 8, 4, 2, 1, and the
  * bias is added last.  Indices and offsets are therefore reproducible bit for
  * bit. */
-moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w,
+moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const void *router_w,
                      const float *router_bias, int32_t *topk_ids, float *topk_w,
                      int32_t *expert_offsets, int32_t *sorted_rows, void *stream);
 
@@ -141,7 +150,7 @@ moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const float *
  *   shared: NULL, or the shared expert (count 1) when cfg.has_shared
  *   out_bf16 [T][H] bf16, written with one round-to-nearest-even of the fp32
  *            sum.  T = 0 is a no-op. */
-moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w,
+moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const void *router_w,
                        const float *router_bias, const moe_expert_set *routed,
                        const moe_expert_set *shared, void *out_bf16, void *stream);
 
@@ -150,7 +159,7 @@ moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const float
  * the result back to out_bf16_host.  The weights stay device pointers.
  * The copies are ordered on `stream`; the call returns before they finish
  * (synchronise the stream before reading out_bf16_host). */
-moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, const float *router_w,
+moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, const void *router_w,
                             const float *router_bias, const moe_expert_set *routed,
                             const moe_expert_set *shared, void *out_bf16_host, void *stream);
 
@@ -259,7 +268,8 @@ moe_status moe_plan_check_timeout(moe_plan plan, int64_t wait_ns, void *stream);
  * capture.  Every call shares the one array: calls that overlap on the GPU
  * (other streams, other threads) race and must be serialised by the caller.
  * The counts are cleared at the start of each call.  Outputs and argument
- * layout are moe_route's; router: moe_router_kind; renormalize: 0 or 1.
+ * layout are moe_route's, with an fp32 router weight; router:
+ * moe_router_kind; renormalize: 0 or 1.
  * Device-side findings (a non-finite activation) are not reported here. */
 moe_status moe_route_static(const void *x_bf16, int32_t T, int32_t hidden, const float *router_w,
                             const float *router_bias, int32_t num_experts, int32_t top_k, int32_t router,

@@ -18,6 +18,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = _build.LIB
 
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
+ROUTER_F32, ROUTER_BF16 = 0, 1
 W4A16, W4A4 = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
@@ -43,7 +44,7 @@ class MoeError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "inter", "num_experts", "top_k", "max_tokens", "router", "renormalize", "mode",
-        "has_shared", "shared_inter")]
+        "has_shared", "shared_inter", "router_dtype")]
 
 
 class Nvfp4(ctypes.Structure):
@@ -155,9 +156,9 @@ class Plan:
     """A moe_plan: configuration plus device workspace for up to max_tokens tokens."""
 
     def __init__(self, hidden, inter, num_experts, top_k, max_tokens, router=ROUTER_SOFTMAX, renormalize=True,
-                 mode=W4A16, has_shared=False, shared_inter=0):
+                 mode=W4A16, has_shared=False, shared_inter=0, router_dtype=ROUTER_F32):
         self.cfg = Config(hidden, inter, num_experts, top_k, max_tokens, router, int(bool(renormalize)), mode,
-                          int(bool(has_shared)), shared_inter if has_shared else 0)
+                          int(bool(has_shared)), shared_inter if has_shared else 0, router_dtype)
         h = ctypes.c_void_p()
         _check(lib().moe_plan_create(ctypes.byref(self.cfg), ctypes.byref(h)), "moe_plan_create")
         self.handle = h

@@ -46,6 +46,7 @@ moe_status check_config(const moe_config *c) {
     if (c->mode != MOE_W4A16 && c->mode != MOE_W4A4) return MOE_ERR_INVALID_ARG;
     if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
     if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_INVALID_ARG;
+    if (c->router_dtype != MOE_ROUTER_F32 && c->router_dtype != MOE_ROUTER_BF16) return MOE_ERR_INVALID_ARG;
     if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return MOE_ERR_INVALID_ARG;
     if (c->hidden < 256 || c->hidden % 256 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (c->inter < 128 || c->inter % 128 || c->inter > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -136,7 +137,7 @@ void carve(Plan &p, Carver &c) {
 }
 
 
-moe_status check_call(moe_plan plan, const void *x, int32_t T, const float *rw, const float *bias) {
+moe_status check_call(moe_plan plan, const void *x, int32_t T, const void *rw, const float *bias) {
     if (!plan || T < 0 || T > plan->p.cfg.max_tokens) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!x || !rw)) return MOE_ERR_INVALID_ARG;
     if ((x && !aligned16(x)) || (rw && !aligned16(rw)) || (bias && !aligned4(bias))) return MOE_ERR_MISALIGNED;
@@ -167,7 +168,7 @@ struct Stage {
     }
 };
 
-moe_status forward_device(moe_plan plan, const void *x, int32_t T, const float *rw, const float *bias,
+moe_status forward_device(moe_plan plan, const void *x, int32_t T, const void *rw, const float *bias,
                           const moe_expert_set *routed, const moe_expert_set *shared, void *out, cudaStream_t st) {
     Plan &p = plan->p;
     cudaError_t e = cudaMemsetAsync(p.scratch, 0, scratch_bytes(p), st);
@@ -338,7 +339,7 @@ moe_status moe_plan_destroy(moe_plan plan) {
     return cuda_status(e);
 }
 
-moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
+moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const void *router_w, const float *router_bias,
                      int32_t *topk_ids, float *topk_w, int32_t *expert_offsets, int32_t *sorted_rows, void *stream) {
     moe_status st = check_call(plan, x_bf16, T, router_w, router_bias);
     if (st != MOE_OK) return st;
@@ -356,7 +357,7 @@ moe_status moe_route(moe_plan plan, const void *x_bf16, int32_t T, const float *
     return cuda_status(moe::launch_group(p, T, topk_ids, expert_offsets, sorted_rows, false, s));
 }
 
-moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const float *router_w, const float *router_bias,
+moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const void *router_w, const float *router_bias,
                        const moe_expert_set *routed, const moe_expert_set *shared, void *out_bf16, void *stream) {
     moe_status st = check_call(plan, x_bf16, T, router_w, router_bias);
     if (st != MOE_OK) return st;
@@ -373,7 +374,7 @@ moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const float
                           static_cast<cudaStream_t>(stream));
 }
 
-moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, const float *router_w,
+moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, const void *router_w,
                             const float *router_bias, const moe_expert_set *routed, const moe_expert_set *shared,
                             void *out_bf16_host, void *stream) {
     if (!plan || T < 0 || T > plan->p.cfg.max_tokens) return MOE_ERR_INVALID_ARG;

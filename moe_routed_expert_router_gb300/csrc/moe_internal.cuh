@@ -273,7 +273,7 @@ struct ExpertPtrs {
 
 int router_launches(int T);
 bool router_groups(int T);
-cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias,
+cudaError_t launch_router(const Plan &p, const void *x, int T, const void *rw, const float *bias,
                           int32_t *ids, float *wts, cudaStream_t st, bool with_group = false);
 int group_launches(const Plan &p, int T);
 cudaError_t launch_group(const Plan &p, int T, const int32_t *ids, int32_t *offsets_out,

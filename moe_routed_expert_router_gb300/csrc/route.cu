@@ -51,11 +51,17 @@ __device__ __forceinline__ void cp_async16(void *dst, const void *src, bool vali
 // order, and a warp's reads are 32 consecutive elements (no bank conflicts).
 constexpr int kRT = 16, kRE = 32, kRSlab = 128, kRStages = 4;
 constexpr int kRXBytes = kRT * kRSlab * 2;          // 4 KB
-constexpr int kRWBytes = kRE * kRSlab * 4;          // 16 KB
+constexpr int kRWBytes = kRE * kRSlab * 4;          // 16 KB (fp32 router words; bf16 words use half)
 constexpr int kRouterTiledSmem = kRStages * (kRXBytes + kRWBytes);
 
+// A router weight word as fp32: fp32 as it is, bf16 widened (exact), so the
+// logits keep the same fixed order and fp32 arithmetic whatever the word type.
+__device__ __forceinline__ float rw_f32(float w) { return w; }
+__device__ __forceinline__ float rw_f32(__nv_bfloat16 w) { return __uint_as_float((uint32_t)__bfloat16_as_ushort(w) << 16); }
+
+template <typename W>
 __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restrict__ x, int T, int H,
-                                                         const float *__restrict__ rw, const float *__restrict__ bias,
+                                                         const W *__restrict__ rw, const float *__restrict__ bias,
                                                          int E, float *__restrict__ logits, int *err,
                                                          unsigned int *x_amax) {
     extern __shared__ __align__(16) uint8_t rsmem[];
@@ -64,8 +70,9 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
     const int tw = (warp >> 2) * 8, ew = (warp & 3) * 8;
     const int slabs = H / kRSlab;
     const bool check = (blockIdx.x == 0);
+    constexpr int kWPer16 = 16 / sizeof(W);   // router words a 16-byte copy moves
     auto xs = [&](int b) { return reinterpret_cast<uint16_t *>(rsmem + b * (kRXBytes + kRWBytes)); };
-    auto ws = [&](int b) { return reinterpret_cast<float *>(rsmem + b * (kRXBytes + kRWBytes) + kRXBytes); };
+    auto ws = [&](int b) { return reinterpret_cast<W *>(rsmem + b * (kRXBytes + kRWBytes) + kRXBytes); };
     auto load = [&](int s) {
         if (s < slabs) {
             const int b = s % kRStages;
@@ -74,11 +81,13 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
                 const bool v = t0 + row < T;
                 cp_async16(xs(b) + row * kRSlab + c * 8, x + (size_t)(v ? t0 + row : 0) * H + s * kRSlab + c * 8, v);
             }
+            constexpr int kChunks = kRSlab / kWPer16;   // 16-byte chunks a router row of the slab
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {   // weights: 32 rows x 32 chunks of 4 floats
-                const int idx = tid + 256 * i, row = idx >> 5, c = idx & 31;
+            for (int i = 0; i < kRE * kChunks / 256; ++i) {   // weights: 32 rows x kChunks chunks
+                const int idx = tid + 256 * i, row = idx / kChunks, c = idx % kChunks;
                 const bool v = e0 + row < E;
-                cp_async16(ws(b) + row * kRSlab + c * 4, rw + (size_t)(v ? e0 + row : 0) * H + s * kRSlab + c * 4, v);
+                cp_async16(ws(b) + row * kRSlab + c * kWPer16,
+                           rw + (size_t)(v ? e0 + row : 0) * H + s * kRSlab + c * kWPer16, v);
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -97,7 +106,7 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
         asm volatile("cp.async.wait_group %0;" ::"n"(kRStages - 1) : "memory");
         __syncthreads();
         const uint16_t *xb = xs(s % kRStages);
-        const float *wb = ws(s % kRStages);
+        const W *wb = ws(s % kRStages);
         if (check && (warp & 3) == 0) {   // warps of expert sub-tile 0 check their tokens once
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
@@ -119,7 +128,7 @@ __global__ void __launch_bounds__(256, 2) k_router_tiled(const uint16_t *__restr
             for (int t = 0; t < 8; ++t) xv[t] = __uint_as_float((uint32_t)xb[(tw + t) * kRSlab + h] << 16);
 #pragma unroll
             for (int p = 0; p < 4; ++p)
-                wv[p] = make_float2(wb[(ew + 2 * p) * kRSlab + h], wb[(ew + 2 * p + 1) * kRSlab + h]);
+                wv[p] = make_float2(rw_f32(wb[(ew + 2 * p) * kRSlab + h]), rw_f32(wb[(ew + 2 * p + 1) * kRSlab + h]));
 #pragma unroll
             for (int t = 0; t < 8; ++t)
 #pragma unroll
@@ -419,17 +428,20 @@ __host__ __device__ __forceinline__ int decode_slab(int T) { return T <= 8 ? kDS
 // Experts a block of the decode router takes.
 __host__ __device__ __forceinline__ int decode_epb(int T, int E) { return (T > 8 && E % 2 == 0) ? 2 : 1; }
 
-__host__ __device__ __forceinline__ size_t decode_router_smem(int H, int T, int E) {
-    return sizeof(float) * (size_t)H * decode_epb(T, E) + (size_t)kDStages * T * decode_slab(T) * 2;
+// wbytes: bytes of a router weight word (4 fp32, 2 bf16)
+__host__ __device__ __forceinline__ size_t decode_router_smem(int H, int T, int E, int wbytes) {
+    return (size_t)wbytes * H * decode_epb(T, E) + (size_t)kDStages * T * decode_slab(T) * 2;
 }
 
-template <int NPL>
+template <int NPL, typename W>
 __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
-    const uint16_t *__restrict__ x, int T, int H, const float *__restrict__ rw, const float *__restrict__ bias,
+    const uint16_t *__restrict__ x, int T, int H, const W *__restrict__ rw, const float *__restrict__ bias,
     int E, int k, int kind, int renorm, float *__restrict__ logits, int32_t *__restrict__ ids,
     float *__restrict__ wts, int32_t *__restrict__ counts, CallScratch *sc, int *err, GroupArgs grp) {
     pdl_trigger();   // the next kernel may be scheduled on free SMs (it waits for this one to finish)
-    extern __shared__ __align__(16) float wrow[];     // [H], per-token x rings [T][kDStages][slab] bf16, grouping
+    extern __shared__ __align__(16) uint8_t dsmem[];  // router rows [epb][H], per-token x rings [T][kDStages][slab] bf16, grouping
+    W *wrow = reinterpret_cast<W *>(dsmem);
+    constexpr int kWPer16 = 16 / sizeof(W);
     __shared__ float s_amax[kDecodeRouterThreads / 32];
     __shared__ int s_bad[kDecodeRouterThreads / 32];
     __shared__ int s_last;
@@ -437,8 +449,8 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
     const int epb = decode_epb(T, E), e = blockIdx.x * epb;   // this block's experts: e .. e + epb - 1
     const int slab = decode_slab(T);
     const int slabs = (H + slab - 1) / slab;
-    for (int c = tid; c < epb * H / 4; c += kDecodeRouterThreads)
-        cp_async16(wrow + 4 * c, rw + (size_t)e * H + 4 * c, true);
+    for (int c = tid; c < epb * H / kWPer16; c += kDecodeRouterThreads)
+        cp_async16(wrow + kWPer16 * c, rw + (size_t)e * H + kWPer16 * c, true);
     asm volatile("cp.async.commit_group;" ::: "memory");
     uint16_t *ring = reinterpret_cast<uint16_t *>(wrow + (size_t)epb * H) + (size_t)warp * kDStages * slab;
     const uint16_t *xr = x + (size_t)warp * H;
@@ -495,7 +507,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
             asm volatile("cp.async.wait_group %0;" ::"n"(kDStages - 1) : "memory");
             __syncwarp();
             const uint16_t *xs = ring + (sl % kDStages) * slab;
-            const float *wr = wrow + sl * slab, *wr1 = wr + H;
+            const W *wr = wrow + sl * slab, *wr1 = wr + H;
             const int len = min(slab, H - sl * slab);   // a multiple of 256
             if (epb == 2) {
 #pragma unroll 2
@@ -505,8 +517,8 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         xv[j] = xs[32 * (j0 + j) + lane];
-                        wv[j] = wr[32 * (j0 + j) + lane];
-                        wv1[j] = wr1[32 * (j0 + j) + lane];
+                        wv[j] = rw_f32(wr[32 * (j0 + j) + lane]);
+                        wv1[j] = rw_f32(wr1[32 * (j0 + j) + lane]);
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
@@ -522,7 +534,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         xv[j] = xs[32 * (j0 + j) + lane];
-                        wv[j] = wr[32 * (j0 + j) + lane];
+                        wv[j] = rw_f32(wr[32 * (j0 + j) + lane]);
                     }
 #pragma unroll
                     for (int j = 0; j < 8; ++j) acc = fmaf(__uint_as_float(xv[j] << 16), wv[j], acc);
@@ -556,7 +568,7 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
     if (grp.active) {
         __syncthreads();   // the block's ids are visible to all its threads
-        int *gsm = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(wrow) + decode_router_smem(H, T, E));
+        int *gsm = reinterpret_cast<int *>(dsmem + decode_router_smem(H, T, E, (int)sizeof(W)));
         group_small(grp, ids, T * k, E, T, k, gsm, sc, err);
     }
 }
@@ -869,8 +881,11 @@ __global__ void __launch_bounds__(1024) k_group_place(const int32_t *__restrict_
 
 }  // namespace
 
-cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, const float *bias, int32_t *ids,
-                          float *wts, cudaStream_t st, bool with_group) {
+namespace {
+
+template <typename W>
+cudaError_t launch_router_w(const Plan &p, const void *x, int T, const W *rw, const float *bias, int32_t *ids,
+                            float *wts, cudaStream_t st, bool with_group) {
     const int H = p.cfg.hidden, E = p.cfg.num_experts, k = p.cfg.top_k;
     const uint16_t *xb = static_cast<const uint16_t *>(x);
     const int npl = (E + 31) / 32;
@@ -880,9 +895,9 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
             grp = GroupArgs{1, p.offsets, p.poff, p.sorted, p.inv, p.pad_pair, p.chunks, p.tiles,
                             (int)p.rows_pad_max, p.tile_rows, p.cfg.has_shared};
         }
-        const size_t smem = decode_router_smem(H, T, E) + (with_group ? group_small_smem(E, T * k) : 0);
+        const size_t smem = decode_router_smem(H, T, E, (int)sizeof(W)) + (with_group ? group_small_smem(E, T * k) : 0);
 #define MOE_DEC(N)                                                                                           \
-    k_router_decode<N><<<E / decode_epb(T, E), kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router,          \
+    k_router_decode<N, W><<<E / decode_epb(T, E), kDecodeRouterThreads, smem, st>>>(xb, T, H, rw, bias, E, k, p.cfg.router, \
                                                               p.cfg.renormalize, p.logits, ids, wts, p.counts, \
                                                               p.scratch, p.err, grp)
         if (npl <= 1) MOE_DEC(1);
@@ -896,7 +911,7 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     }
     unsigned int *amax = &p.scratch->x_amax;   // batch amax of x (W4A4 quantiser, f16 range of W4A16)
     dim3 gt((E + kRE - 1) / kRE, (T + kRT - 1) / kRT);
-    k_router_tiled<<<gt, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
+    k_router_tiled<W><<<gt, 256, kRouterTiledSmem, st>>>(xb, T, H, rw, bias, E, p.logits, p.err, amax);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     dim3 g((T + 3) / 4);
@@ -909,6 +924,17 @@ cudaError_t launch_router(const Plan &p, const void *x, int T, const float *rw, 
     else MOE_TOPK(32);
 #undef MOE_TOPK
     return cudaGetLastError();
+}
+
+}  // namespace
+
+// The router weight's word type comes from the plan: fp32, or bf16 words
+// (MOE_ROUTER_BF16) widened to fp32 as they are read.
+cudaError_t launch_router(const Plan &p, const void *x, int T, const void *rw, const float *bias, int32_t *ids,
+                          float *wts, cudaStream_t st, bool with_group) {
+    if (p.cfg.router_dtype == MOE_ROUTER_BF16)
+        return launch_router_w(p, x, T, static_cast<const __nv_bfloat16 *>(rw), bias, ids, wts, st, with_group);
+    return launch_router_w(p, x, T, static_cast<const float *>(rw), bias, ids, wts, st, with_group);
 }
 
 // Kernels launch_router issues for T tokens (hidden is always a multiple of 256).
@@ -933,12 +959,21 @@ cudaError_t configure_group_kernel() {
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(mu);
     if (done[dev]) return cudaSuccess;
-    e = cudaFuncSetAttribute(k_router_tiled, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
+    e = cudaFuncSetAttribute(k_router_tiled<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouterTiledSmem);
     if (e != cudaSuccess) return e;
-    const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32, 2) +
+    e = cudaFuncSetAttribute(k_router_tiled<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRouterTiledSmem);
+    if (e != cudaSuccess) return e;
+    const int dec = (int)(decode_router_smem(8192, kDecodeRouterThreads / 32, 2, 4) +
                           group_small_smem(kMaxExperts, kDecodeRouterThreads / 32 * kMaxTopK));
-    for (auto f : {k_router_decode<1>, k_router_decode<2>, k_router_decode<4>, k_router_decode<8>,
-                   k_router_decode<16>, k_router_decode<32>}) {
+    for (auto f : {k_router_decode<1, float>, k_router_decode<2, float>, k_router_decode<4, float>,
+                   k_router_decode<8, float>, k_router_decode<16, float>, k_router_decode<32, float>}) {
+        e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
+        if (e != cudaSuccess) return e;
+    }
+    for (auto f : {k_router_decode<1, __nv_bfloat16>, k_router_decode<2, __nv_bfloat16>,
+                   k_router_decode<4, __nv_bfloat16>, k_router_decode<8, __nv_bfloat16>,
+                   k_router_decode<16, __nv_bfloat16>, k_router_decode<32, __nv_bfloat16>}) {
         e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, dec);
         if (e != cudaSuccess) return e;
     }

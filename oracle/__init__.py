@@ -252,7 +252,13 @@ def quant_decisions(x, ts: float, margin: float = FLIP_MARGIN):
 # ------------------------------------------------------------------ router
 
 def router_logits(x_bf16: np.ndarray, router_w: np.ndarray, bias: np.ndarray | None) -> np.ndarray:
+    """Router logits in the fixed fp32 order (moe_oracle.c).  router_w is fp32
+    [E][H], or uint16 bf16 words [E][H] (the router kept in its BF16 words,
+    "NVIDIA FP4-Local checkpoints on DGX Spark ... #565", section 4 Round 1,
+    #732): those widen to fp32 exactly, so the same fp32 sums follow."""
     x = np.ascontiguousarray(x_bf16, np.uint16)
+    if np.asarray(router_w).dtype == np.uint16:
+        router_w = bf16_to_f32(router_w)
     w = np.ascontiguousarray(router_w, np.float32)
     T, H = x.shape
     E = w.shape[0]
@@ -428,19 +434,37 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
     return res
 
 
+def bf16_half_ulp(ref) -> np.ndarray:
+    """Half a bf16 ulp at each |ref|: the most an exactly rounded bf16 output
+    can differ from the FP64 value it rounds (bf16 has 8 significant bits)."""
+    a = np.abs(np.asarray(ref, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(np.maximum(e, -126.0) - 8.0), 2.0 ** -134)
+
+
 def compare_output(got_bf16: np.ndarray, ref_f64: np.ndarray, band: np.ndarray | None = None):
-    """Output tolerance: |d| <= 2e-2 * RMS(ref) (+ band) element-wise and
-    ||d||_2 / ||ref||_2 <= 5e-3.  `band` (W4A4) is forward()'s bound on what
-    the SwiGLU quantiser's near-boundary decisions can move; it is zero where
-    no such decision touches an output."""
+    """Output tolerance.  Element-wise |d| <= 2e-2 * RMS(ref) + half a bf16 ulp
+    of ref (+ band), and ||d||_2 / ||ref||_2 <= 5e-3.
+
+    The output is bf16, rounded once from the exact sum: half an ulp of the
+    result is the format's own rounding, which an exact implementation also
+    makes, so the 2e-2 * RMS bound applies to the computation error on top of
+    it.  (With outputs reaching 5 RMS, as the 4096-token prompt's do, the
+    exactly rounded output alone can differ from the FP64 value by 2e-2 * RMS.)
+    `band` (W4A4) is forward()'s bound on what the SwiGLU quantiser's
+    near-boundary decisions can move; it is zero where no such decision
+    touches an output."""
     got = bf16_to_f64(got_bf16)
     d = np.abs(got - ref_f64)
     rms = float(np.sqrt(np.mean(ref_f64 ** 2)))
     max_abs = float(np.max(d)) if d.size else 0.0
     rel_l2 = float(np.linalg.norm(d) / max(np.linalg.norm(ref_f64), 1e-300))
-    lim = 2e-2 * rms + (0.0 if band is None else band)
+    base = 2e-2 * rms + bf16_half_ulp(ref_f64)
+    lim = base + (0.0 if band is None else band)
     beyond = d > lim
     ok = (not bool(beyond.any())) and (rel_l2 <= 5e-3) and bool(np.all(np.isfinite(got)))
-    excess = d - 2e-2 * rms
+    excess = d - base
     return ok, dict(max_abs=max_abs, rms=rms, max_abs_over_rms=max_abs / max(rms, 1e-300), rel_l2=rel_l2,
+                    max_excess_over_rounding=float(np.max(excess)) / max(rms, 1e-300) if d.size else 0.0,
                     inside_band_only=int(((excess > 0) & ~beyond).sum()), beyond=int(beyond.sum()))

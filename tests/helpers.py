@@ -16,11 +16,11 @@ import moe_routed_expert_router_gb300 as moe
 PROJ = ("gate", "up", "down")
 
 
-def plan_for(w: synth.Workload, max_tokens=None) -> moe.Plan:
+def plan_for(w: synth.Workload, max_tokens=None, router_dtype=moe.ROUTER_F32) -> moe.Plan:
     return moe.Plan(w.hidden, w.inter, w.experts, w.top_k, max_tokens or w.tokens,
                     router=moe.ROUTER_SIGMOID if w.router == "sigmoid" else moe.ROUTER_SOFTMAX,
                     renormalize=w.renormalize, mode=moe.W4A4 if w.mode == "w4a4" else moe.W4A16,
-                    has_shared=w.shared_inter > 0, shared_inter=w.shared_inter)
+                    has_shared=w.shared_inter > 0, shared_inter=w.shared_inter, router_dtype=router_dtype)
 
 
 class Case:
@@ -60,6 +60,9 @@ class Case:
         return self.x.cpu().view(torch.int16).numpy().view(np.uint16)
 
     def rw_host(self):
+        """The router weight as the oracle takes it: fp32, or bf16 words (uint16)."""
+        if self.rw.dtype == torch.bfloat16:
+            return self.rw.cpu().view(torch.int16).numpy().view(np.uint16)
         return self.rw.cpu().numpy()
 
     def bias_host(self):
@@ -79,7 +82,8 @@ class Case:
                               shared=self.oracle_expert("shared") if w.shared_inter else None, keep=keep)
 
     def gpu_forward(self, plan=None):
-        plan = plan or plan_for(self.w)
+        plan = plan or plan_for(self.w, router_dtype=moe.ROUTER_BF16 if self.rw.dtype == torch.bfloat16
+                                else moe.ROUTER_F32)
         out = plan.forward(self.x, self.rw, self.bias, self.routed, self.shared)
         st = plan.sync_status()
         return out, st, plan

@@ -38,6 +38,10 @@ def test_host_side_argument_checks_need_no_gpu():
     assert L.moe_plan_create(ctypes.byref(bad), ctypes.byref(h)) == moe.ERR_UNSUPPORTED_SHAPE
     bad = moe.Config(4096, 1536, 128, 8, 4, 7, 1, 0, 0, 0)          # unknown router kind
     assert L.moe_plan_create(ctypes.byref(bad), ctypes.byref(h)) == moe.ERR_INVALID_ARG
+    bad = moe.Config(4096, 1536, 128, 8, 4, 0, 1, 0, 0, 0, 2)       # unknown router word type
+    assert L.moe_plan_create(ctypes.byref(bad), ctypes.byref(h)) == moe.ERR_INVALID_ARG
+    assert L.moe_convert_f32(None, 16, 7, None, None) == moe.ERR_INVALID_ARG   # unknown format
+    assert L.moe_convert_f32(8, 16, moe.FMT_E2M1, 16, None) == moe.ERR_MISALIGNED
     assert L.moe_quantize_nvfp4(None, 1, 4, 24, None, None, None, None) == moe.ERR_UNSUPPORTED_SHAPE
     assert L.moe_quantize_nvfp4(8, 1, 4, 32, 16, 16, 16, None) == moe.ERR_MISALIGNED
     assert L.moe_forward(None, None, 0, None, None, None, None, None, None) == moe.ERR_INVALID_ARG

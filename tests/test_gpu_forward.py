@@ -242,3 +242,12 @@ def test_forward_replays_from_a_cuda_graph(name):
     ref = case.oracle_forward()
     ok, stats = oracle.compare_output(bf16_bits(out), ref["out"], ref["band"])
     assert ok, stats
+
+
+@pytest.mark.parametrize("name", ["decode4_w4a16", "verify16_w4a4"])
+def test_forward_with_bf16_router_words(name):
+    """moe_forward with the router weight in bf16 words against the oracle on
+    the same words."""
+    case = Case(synth.WORKLOADS[name], 1)
+    case.rw = case.rw.to(torch.bfloat16)
+    _parity(case)

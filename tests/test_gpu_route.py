@@ -13,11 +13,13 @@ pytestmark = pytest.mark.gpu
 
 
 def _check(w, x, rw, bias):
-    with plan_for(w, max_tokens=max(1, x.shape[0])) as plan:
+    bf16 = rw.dtype == torch.bfloat16
+    with plan_for(w, max_tokens=max(1, x.shape[0]), router_dtype=moe.ROUTER_BF16 if bf16 else moe.ROUTER_F32) as plan:
         r = plan.route(x, rw, bias)
         assert plan.sync_status() == moe.OK
     xb = x.cpu().view(torch.int16).numpy().view(np.uint16)
-    ref = oracle.route(xb, rw.cpu().numpy(), None if bias is None else bias.cpu().numpy(), w.top_k,
+    rwh = rw.cpu().view(torch.int16).numpy().view(np.uint16) if bf16 else rw.cpu().numpy()
+    ref = oracle.route(xb, rwh, None if bias is None else bias.cpu().numpy(), w.top_k,
                        oracle.ROUTER_SIGMOID if w.router == "sigmoid" else oracle.ROUTER_SOFTMAX, w.renormalize)
     np.testing.assert_array_equal(r["topk_ids"].cpu().numpy(), ref["ids"])
     np.testing.assert_array_equal(r["expert_offsets"].cpu().numpy(), ref["offsets"])
@@ -26,13 +28,25 @@ def _check(w, x, rw, bias):
     return ref
 
 
+@pytest.mark.parametrize("router_dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("name", list(synth.WORKLOADS))
-def test_route_full_size(name):
+def test_route_full_size(name, router_dtype):
+    """Every workload at full size, with the router weight in fp32 and in bf16
+    words (the same draw rounded to bf16): ids, offsets, order bit for bit."""
     w = synth.WORKLOADS[name]
     for seed in w.seeds[:2]:
-        ref = _check(w, synth.activations(w, seed, device="cuda"), synth.router_weight(w, seed, "cuda"),
-                     synth.router_bias(w, seed, "cuda"))
+        rw = synth.router_weight(w, seed, "cuda")
+        if router_dtype == "bf16":
+            rw = rw.to(torch.bfloat16)
+        ref = _check(w, synth.activations(w, seed, device="cuda"), rw, synth.router_bias(w, seed, "cuda"))
         assert np.all(np.diff(ref["offsets"]) >= 0)
+
+
+@pytest.mark.parametrize("T", [1, 16, 17, 300])
+def test_route_bf16_router_ragged(T):
+    w = synth.scaled(synth.WORKLOADS["verify16_w4a4"], tokens=T, hidden=1024, experts=96)
+    _check(w, synth.activations(w, 8, device="cuda"), synth.router_weight(w, 8, "cuda").to(torch.bfloat16),
+           synth.router_bias(w, 8, "cuda"))
 
 
 @pytest.mark.parametrize("T", [1, 3, 37, 130])

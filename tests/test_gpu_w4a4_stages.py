@@ -124,6 +124,10 @@ def check_end_to_end(case, out, record_property):
     stats["h_flips"] = ref["h_flips"]
     record_property("h_flips", ref["h_flips"])
     record_property("inside_band_only", stats["inside_band_only"])
+    record_property("max_abs_over_rms", stats["max_abs_over_rms"])
+    # the oracle's own exactly rounded bf16 output against its FP64 value
+    own = oracle.compare_output(ref["out_bf16"], ref["out"])[1]
+    record_property("oracle_rounding_max_abs_over_rms", own["max_abs_over_rms"])
     assert ok, stats
     # the band explains a small minority of outputs only
     assert stats["inside_band_only"] <= max(8, 1e-3 * out.numel()), stats

@@ -122,3 +122,22 @@ def test_flip_band_covers_every_flip_of_small_perturbations():
     assert changed.sum() >= 5, "the perturbations should flip a few decisions in 256K values"
     assert np.all(flip[changed] >= moved[changed] * (1 - 1e-12))
     assert n < 0.01 * x.size                 # few decisions sit that close to a boundary
+
+
+def test_bf16_half_ulp_and_output_tolerance():
+    """Half a bf16 ulp: 2^(e-8) in [2^e, 2^(e+1)).  The output check lets an
+    exactly rounded bf16 output pass even where its rounding alone exceeds
+    2e-2 * RMS, and still fails an output two ulps away."""
+    assert oracle.bf16_half_ulp(np.array([1.0, 1.99, 4.0, 6.5, -0.75, 0.0])).tolist() == \
+        [2 ** -8, 2 ** -8, 2 ** -6, 2 ** -6, 2 ** -9, 2 ** -134]
+    rng = np.random.default_rng(7)
+    ref = rng.normal(0, 0.7, 4096)
+    ref[5] = 4.0 + 0.999 * 2 ** -5 / 2            # just below the midpoint of 4 and 4 + 2^-5
+    exact = oracle.f64_to_bf16(ref)               # the exactly rounded output
+    rms = np.sqrt(np.mean(ref ** 2))
+    assert abs(oracle.bf16_to_f64(exact[5:6])[0] - ref[5]) > 2e-2 * rms   # rounding alone exceeds the plain bar
+    ok, st = oracle.compare_output(exact, ref)
+    assert ok, st
+    worse = exact.copy()
+    worse[5] += 2                                  # two bf16 ulps up: 4.0625
+    assert not oracle.compare_output(worse, ref)[0]

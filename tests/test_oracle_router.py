@@ -108,3 +108,21 @@ def test_route_permutation_covers_every_pair_once():
         seg = r["sorted_rows"][r["offsets"][e]:r["offsets"][e + 1]]
         assert np.all(r["ids"].ravel()[seg] == e)
         assert np.all(np.diff(seg) > 0)
+
+
+def test_bf16_router_words_widen_exactly():
+    """A bf16 router weight gives the logits of its exact fp32 widening (same
+    fixed order), and words off the fp32 grid of 8 bits still count in full:
+    0x3F81 is 1 + 2^-7, so x = 1 at one position gives exactly that logit."""
+    rng = np.random.default_rng(21)
+    T, H, E = 5, 256, 7
+    x = _bf16(rng.normal(0, 1, (T, H)))
+    w16 = _bf16(rng.normal(0, H ** -0.5, (E, H)))
+    widened = (w16.astype(np.uint32) << 16).view(np.float32)
+    np.testing.assert_array_equal(oracle.router_logits(x, w16, None), oracle.router_logits(x, widened, None))
+    one = np.zeros((1, H), np.uint16)
+    one[0, 3] = 0x3F80                               # x = 1.0 at h = 3
+    w = np.zeros((2, H), np.uint16)
+    w[0, 3] = 0x3F81                                 # 1.0078125
+    w[1, 3] = 0xBF00                                 # -0.5
+    assert oracle.router_logits(one, w, None).tolist() == [[1.0078125, -0.5]]
