@@ -604,6 +604,7 @@ struct HcArgs {
     // the gate/up launch gathers its token rows from (no separate permute)
     int rcst, rbst, rbslot;
     const uint16_t *x;
+    int xres;               // gate/up: tokens whose activations sit resident in shared memory (0: token-row ring)
     // split last round (warp-MMA engine): arrival tickets and partial sums
     int tail_split;
     int *tickets;
@@ -1042,8 +1043,21 @@ constexpr int kRXchg = 8 * 4 * 32 * 4 * 4;        // 16 KB: up-operand accumulat
 // fourth stage (a fifth weight stage measured no faster).
 struct RegRings { int cst, bst, bslot; };
 constexpr RegRings kRegSmall{4, 4, 16 * 512}, kRegLarge{4, 3, 32 * 512};
+// Per-CTA table of the launch's items, filled once by warp 1 at the start with
+// all their global reads in flight together (the work list, the token and the
+// routing weight of every row, the tensor scales), so the compute warps start
+// each item from shared memory instead of a chain of dependent global loads.
+// A CTA with more items than the table holds decodes the rest as it goes.
+constexpr int kMetaItems = 32;
+struct RegMeta {
+    int e, row0, valid, f, sh, kc0, kc1, part, parts, slot, ok, pad;
+    float ts0, ts1, pad2[2];
+    int tok[32];      // token of row n (rows < valid)
+    float w[32];      // routing weight of row n (1 for the shared expert)
+};
+constexpr size_t kMetaBytes = sizeof(RegMeta) * kMetaItems;
 constexpr size_t reg_smem(RegRings r) {
-    return (size_t)r.cst * kHCodeStage + (size_t)r.bst * r.bslot + kRXchg + 512 + 1024;
+    return (size_t)r.cst * kHCodeStage + (size_t)r.bst * r.bslot + kRXchg + kMetaBytes + 512 + 1024;
 }
 constexpr size_t kRSmemBytes = reg_smem(kRegSmall) > reg_smem(kRegLarge) ? reg_smem(kRegSmall) : reg_smem(kRegLarge);
 static_assert(kRSmemBytes <= 227 * 1024, "register-path pipeline exceeds shared memory");
@@ -1055,8 +1069,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
                  : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-template <int NT>
-__device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int rg, int lane, float (&acc)[4][4]) {
+// One 256-value K stage of a compute warp.  Token rows come from the token-row
+// ring slot `bst` (RES = false), or (RES = true, one 8-row token tile) from the
+// resident activations: `bst` is then the shared-memory address of this lane's
+// token row, `xsw` its 16-byte chunk swizzle and `kc` the stage index.
+template <int NT, bool RES = false>
+__device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int rg, int lane, float (&acc)[4][4],
+                                          int kc = 0, uint32_t xsw = 0) {
     const int g = lane >> 2, q = lane & 3;
     const int r0 = rg * 16 + g, r1 = r0 + 8;
     const uint32_t crow0 = st + op * kHCodeTile + r0 * 128, crow1 = st + op * kHCodeTile + r1 * 128;
@@ -1088,12 +1107,19 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
         }
         // token-row fragments: row n = 8 nt + g, K values 64 sb + 16 q .. +16 (box sb of the stage)
         uint4 bx[NT][2];
+        if (RES) {
+            // K values kc*256 + 64 sb + 16 q .. +16 of the token: 16-byte chunks c0, c0 + 1
+            const uint32_t c0 = (uint32_t)(kc * 32 + sb * 8 + 2 * q);
+            bx[0][0] = lds128(bst + ((c0 ^ xsw) << 4));
+            bx[0][1] = lds128(bst + (((c0 + 1) ^ xsw) << 4));
+        } else {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            const int n = nt * 8 + g;
-            const uint32_t brow = bst + (uint32_t)sb * (NT > 2 ? 32 : 16) * 128 + n * 128;
-            bx[nt][0] = lds128(brow + (((uint32_t)(2 * q) ^ (uint32_t)(n & 7)) << 4));
-            bx[nt][1] = lds128(brow + (((uint32_t)(2 * q + 1) ^ (uint32_t)(n & 7)) << 4));
+            for (int nt = 0; nt < NT; ++nt) {
+                const int n = nt * 8 + g;
+                const uint32_t brow = bst + (uint32_t)sb * (NT > 2 ? 32 : 16) * 128 + n * 128;
+                bx[nt][0] = lds128(brow + (((uint32_t)(2 * q) ^ (uint32_t)(n & 7)) << 4));
+                bx[nt][1] = lds128(brow + (((uint32_t)(2 * q + 1) ^ (uint32_t)(n & 7)) << 4));
+            }
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -1107,11 +1133,68 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
     }
 }
 
-// Compute warps of k_gemm_reg (warps 1..16).
+// Items of this CTA: blockIdx.x + j * gridDim.x for j < cta_items.
+__device__ __forceinline__ int cta_items(int n_items) {
+    return n_items > (int)blockIdx.x ? (n_items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x : 0;
+}
+
+// Warp 1: fill the item table.  Lane j decodes item j; then the token and
+// routing weight of every row of every item are read, four items' reads in
+// flight at a time.  Returns the number of entries.
+template <int EPI>
+__device__ __forceinline__ int reg_fill_meta(const HcArgs &a, const RegSplit &rs, RegMeta *meta, int lane) {
+    const int n_tab = min(cta_items(rs.n_items), kMetaItems);
+    if (lane < n_tab) {
+        Item it;
+        RegMeta &m = meta[lane];
+        const bool ok = decode_item_r(a, rs, (int)blockIdx.x + lane * (int)gridDim.x, EPI, it);
+        m.ok = ok;
+        if (ok) {
+            m.e = it.e;
+            m.row0 = it.row0;
+            m.valid = it.valid;
+            m.f = it.f;
+            m.sh = it.sh;
+            m.kc0 = it.kc0;
+            m.kc1 = it.kc1;
+            m.part = it.part;
+            m.parts = it.parts;
+            m.slot = it.slot;
+            const int mm = it.sh ? 1 : 0, e = it.sh ? 0 : it.e;
+            m.ts0 = a.ts_a0[mm][e];
+            m.ts1 = EPI == kSwiGLU ? a.ts_a1[mm][e] : 0.0f;
+        }
+    }
+    __syncwarp();
+    for (int j0 = 0; j0 < n_tab; j0 += 4) {
+        int pr[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u;
+            pr[u] = -1;
+            if (j < n_tab && meta[j].ok && lane < meta[j].valid) pr[u] = a.pad_pair[meta[j].row0 + lane];
+        }
+        float wv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wv[u] = (EPI == kScatter && pr[u] >= 0 && pr[u] < a.P) ? a.wts[pr[u]] : 1.0f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int j = j0 + u;
+            if (j < n_tab) {
+                meta[j].tok[lane] = pr[u] < 0 ? 0 : (pr[u] >= a.P ? pr[u] - a.P : pr[u] / a.k);
+                meta[j].w[lane] = wv[u];
+            }
+        }
+    }
+    return n_tab;
+}
+
+// Compute warps of k_gemm_reg (warps 2..17).
 template <int EPI>
 __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
                                             float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
-                                            uint64_t *bempty, uint64_t *xfull, uint64_t *xempty) {
+                                            uint64_t *bempty, uint64_t *xfull, uint64_t *xempty,
+                                            const RegMeta *meta, uint64_t *meta_ready, uint64_t *x_full) {
     const RegSplit rs = reg_split(a);
     const int n_items = rs.n_items;
     const int cw = warp - 2, rg = cw & 7, op = cw >> 3;
@@ -1119,49 +1202,128 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
     const uint32_t ring0 = smem_u32(code_ring), bring0 = smem_u32(b_ring);
     const int xs = f16_shift(a.scratch->x_amax);
     const float xunscale = __uint_as_float((uint32_t)(127 + xs) << 23);   // 2^s
+    const bool res = EPI == kSwiGLU && a.xres > 0;
+    bool ok = true, range_bad = false;
+    if (res) {
+        // resident activations: the raw bf16 rows (copied at launch) -> f16 x 2^-s
+        // in place, each 128-byte group of a row written with its 16-byte chunks
+        // permuted by the token's row index (c -> c ^ (t & 7)), so the lanes
+        // reading different tokens' rows hit different banks
+        ok = mbar_wait(x_full, 0, a.err);
+        const float scale = __uint_as_float((uint32_t)(127 - xs) << 23);   // 2^-s
+        const int gpr = a.H * 2 / 128;                                       // groups a row
+        for (int gi = cw * 32 + lane; ok && gi < a.xres * gpr; gi += 16 * 32) {
+            const uint32_t base = bring0 + (uint32_t)gi * 128, sw = (uint32_t)((gi / gpr) & 7);
+            uint4 v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] = lds128(base + 16 * c);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t u[4] = {v[c].x, v[c].y, v[c].z, v[c].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    __half2 hh = __floats2half2_rn(__uint_as_float(u[h] << 16) * scale,
+                                                   __uint_as_float(u[h] & 0xFFFF0000u) * scale);
+                    u[h] = *reinterpret_cast<uint32_t *>(&hh);
+                }
+                v[c] = make_uint4(u[0], u[1], u[2], u[3]);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sts128(base + 16 * ((uint32_t)c ^ sw), v[c]);
+        }
+        asm volatile("bar.sync 1, 512;" ::: "memory");   // the 16 compute warps
+        ok = __all_sync(0xffffffffu, ok);
+    }
+    const int n_tab = min(cta_items(n_items), kMetaItems);
+    if (ok && n_tab > 0) ok = mbar_wait(meta_ready, 0, a.err);
     RingPos cs, bs;
     uint32_t xph = 0;
-    bool ok = true, range_bad = false;
+    int ji = -1;   // index of the item among this CTA's
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        ++ji;
         Item it;
-        if (!decode_item_r(a, rs, item, EPI, it)) continue;
-        const int nt_n = (it.valid + 7) >> 3;
-        // epilogue inputs, loaded now so their latency hides behind the K loop:
-        // tensor scales, and the (token, weight) of this lane's first two columns
-        const int m = it.sh ? 1 : 0;
-        const int e = it.sh ? 0 : it.e;
-        const float ts0 = a.ts_a0[m][e], ts1 = EPI == kSwiGLU ? a.ts_a1[m][e] : 0.0f;
+        float ts0, ts1;
+        // epilogue inputs: tensor scales and the (token, weight) of this lane's
+        // first two columns (from the item table, or read now so their latency
+        // hides behind the K loop)
         int tk[2] = {0, 0};
         float wt[2] = {0.0f, 0.0f};
-        if (EPI == kScatter) {
+        int xtok = 0;   // resident activations: this lane's token row (row g; padding rows read row 0's)
+        if (ji < n_tab) {
+            const RegMeta &m = meta[ji];
+            if (!m.ok) continue;
+            it.e = m.e;
+            it.row0 = m.row0;
+            it.valid = m.valid;
+            it.f = m.f;
+            it.sh = m.sh;
+            it.kc0 = m.kc0;
+            it.kc1 = m.kc1;
+            it.part = m.part;
+            it.parts = m.parts;
+            it.slot = m.slot;
+            ts0 = m.ts0;
+            ts1 = m.ts1;
+            if (EPI == kScatter) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int n = 2 * q + c;
-                if (n < it.valid) {
-                    const int pair = a.pad_pair[it.row0 + n];
-                    tk[c] = pair >= a.P ? pair - a.P : pair / a.k;
-                    wt[c] = pair >= a.P ? 1.0f : a.wts[pair];
+                for (int c = 0; c < 2; ++c) {
+                    const int n = 2 * q + c;
+                    if (n < it.valid) { tk[c] = m.tok[n]; wt[c] = m.w[n]; }
                 }
             }
+            if (res) xtok = m.tok[g < it.valid ? g : 0];
+        } else {
+            if (!decode_item_r(a, rs, item, EPI, it)) continue;
+            const int mm = it.sh ? 1 : 0;
+            const int e = it.sh ? 0 : it.e;
+            ts0 = a.ts_a0[mm][e];
+            ts1 = EPI == kSwiGLU ? a.ts_a1[mm][e] : 0.0f;
+            if (EPI == kScatter) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const int n = 2 * q + c;
+                    if (n < it.valid) {
+                        const int pair = a.pad_pair[it.row0 + n];
+                        tk[c] = pair >= a.P ? pair - a.P : pair / a.k;
+                        wt[c] = pair >= a.P ? 1.0f : a.wts[pair];
+                    }
+                }
+            }
+            if (res) {
+                const int pair = a.pad_pair[it.row0 + (g < it.valid ? g : 0)];
+                xtok = pair >= a.P ? pair - a.P : pair / a.k;
+            }
         }
+        const int nt_n = (it.valid + 7) >> 3;
+        const uint32_t xrow = bring0 + (uint32_t)xtok * (uint32_t)a.H * 2u, xsw = (uint32_t)(xtok & 7);
         float acc[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = 0.0f;
+            for (int jj = 0; jj < 4; ++jj) acc[i][jj] = 0.0f;
         for (int kc = it.kc0; kc < it.kc1; ++kc) {
-            if (!mbar_wait(cfull + cs.s, cs.ph, a.err) || !mbar_wait(bfull + bs.s, bs.ph, a.err)) { ok = false; break; }
+            if (!mbar_wait(cfull + cs.s, cs.ph, a.err) || (!res && !mbar_wait(bfull + bs.s, bs.ph, a.err))) {
+                ok = false;
+                break;
+            }
             const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * a.rbslot;
-            switch (nt_n) {
-                case 1: reg_stage<1>(st, bst, op, rg, lane, acc); break;
-                case 2: reg_stage<2>(st, bst, op, rg, lane, acc); break;
-                case 3: reg_stage<3>(st, bst, op, rg, lane, acc); break;
-                default: reg_stage<4>(st, bst, op, rg, lane, acc); break;
+            if (res) {
+                reg_stage<1, true>(st, xrow, op, rg, lane, acc, kc, xsw);
+            } else {
+                switch (nt_n) {
+                    case 1: reg_stage<1>(st, bst, op, rg, lane, acc); break;
+                    case 2: reg_stage<2>(st, bst, op, rg, lane, acc); break;
+                    case 3: reg_stage<3>(st, bst, op, rg, lane, acc); break;
+                    default: reg_stage<4>(st, bst, op, rg, lane, acc); break;
+                }
             }
             __syncwarp();
-            if (lane == 0) { mbar_arrive(cempty + cs.s); mbar_arrive(bempty + bs.s); }
+            if (lane == 0) {
+                mbar_arrive(cempty + cs.s);
+                if (!res) mbar_arrive(bempty + bs.s);
+            }
             cs.next(a.rcst);
-            bs.next(a.rbst);
+            if (!res) bs.next(a.rbst);
         }
         if (!ok) break;
         if (EPI == kSwiGLU) {
@@ -1354,35 +1516,48 @@ __device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b
 
 template <int EPI>
 __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *code_ring = smem;
+    uint8_t *b_ring = code_ring + (size_t)a.rcst * kHCodeStage;   // token-row ring, or the resident activations
+    float *xchg = reinterpret_cast<float *>(b_ring + (size_t)a.rbst * a.rbslot);
+    RegMeta *meta = reinterpret_cast<RegMeta *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
+    uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(meta) + kMetaBytes);
+    uint64_t *cempty = cfull + a.rcst;
+    uint64_t *bfull = cempty + a.rcst;
+    uint64_t *bempty = bfull + a.rbst;
+    uint64_t *xfull = bempty + a.rbst;           // [8] up accumulators written (SwiGLU)
+    uint64_t *xempty = xfull + 8;                // [8] and read
+    uint64_t *meta_ready = xempty + 8;           // item table filled
+    uint64_t *x_full = meta_ready + 1;           // resident activations copied
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.rcst; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
+        for (int i = 0; i < a.rbst; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
+        for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
+        mbar_init(meta_ready, 1);
+        mbar_init(x_full, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    // Resident activations (gate/up, a.xres tokens): the raw bf16 rows of x are
+    // this launch's input, not the previous kernel's output, so their copy is
+    // issued before the dependency wait and overlaps the router's tail.
+    if (EPI == kSwiGLU && a.xres > 0 && threadIdx.x == 32) {
+        mbar_expect_tx(x_full, (uint32_t)(a.xres * a.H * 2));
+        for (int t = 0; t < a.xres; ++t)
+            bulk_copy(b_ring + (size_t)t * a.H * 2, a.x + (size_t)t * a.H, (uint32_t)(a.H * 2), x_full);
+    }
     // gate/up: the routing results come from the previous kernel. down: only
     // its token rows (h) do, so only their producer waits (below); the weights,
     // the work list and the routing weights were complete before the gate/up
     // kernel passed its own wait, and the weight stream starts at once.
     if (EPI != kScatter) pdl_wait();
     pdl_trigger();
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *code_ring = smem;
-    uint8_t *b_ring = code_ring + (size_t)a.rcst * kHCodeStage;
-    float *xchg = reinterpret_cast<float *>(b_ring + (size_t)a.rbst * a.rbslot);
-    uint64_t *cfull = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) + kRXchg);
-    uint64_t *cempty = cfull + a.rcst;
-    uint64_t *bfull = cempty + a.rcst;
-    uint64_t *bempty = bfull + a.rbst;
-    uint64_t *xfull = bempty + a.rbst;           // [8] up accumulators written (SwiGLU)
-    uint64_t *xempty = xfull + 8;                // [8] and read
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const RegSplit rs = reg_split(a);
     const int n_items = rs.n_items;
-    const bool gather = EPI == kSwiGLU && a.x != nullptr;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < a.rcst; ++i) { mbar_init(cfull + i, 1); mbar_init(cempty + i, 16); }
-        for (int i = 0; i < a.rbst; ++i) { mbar_init(bfull + i, 1); mbar_init(bempty + i, 16); }
-        for (int i = 0; i < 8; ++i) { mbar_init(xfull + i, 1); mbar_init(xempty + i, 1); }
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
+    const bool gather = EPI == kSwiGLU && a.x != nullptr && a.xres == 0;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -1413,8 +1588,17 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             }
             for (int t = 0; t < a.rcst; ++t)
                 if (used & (1u << t)) mbar_wait(cfull + t, (last_ph >> t) & 1u, a.err);
-        } else if (lane == 1 && !gather) {
-            // ---------------------------------------- TMA producer of the token-row ring
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------- item table, then the token rows
+        const int n_tab = reg_fill_meta<EPI>(a, rs, meta, lane);
+        __syncwarp();
+        if (lane == 0 && n_tab > 0) mbar_arrive(meta_ready);
+        if (gather) {
+            reg_gather<EPI>(a, lane, b_ring, bfull, bempty, rs);
+        } else if (EPI == kScatter && lane == 0) {
+            // TMA producer of the token-row ring, in a warp of its own: its
+            // dependency wait must not hold up the weight stream of warp 0
             pdl_wait();   // the token rows are the previous kernel's output
             RingPos b;
             bool ok = true;
@@ -1438,10 +1622,9 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
             for (int t = 0; t < a.rbst; ++t)
                 if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
         }
-    } else if (warp == 1) {
-        if (gather) reg_gather<EPI>(a, lane, b_ring, bfull, bempty, rs);
     } else {
-        reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty);
+        reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty, meta,
+                         meta_ready, x_full);
     }
 }
 
@@ -1608,6 +1791,9 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     if (part == 0) {
         if (warp_mma) {
             a.x = static_cast<const uint16_t *>(x);   // the gate/up launch gathers its token rows itself
+            // few tokens (every tile within one 8-row MMA tile): the whole of x
+            // fits the token-row ring's space and stays resident for the launch
+            if (T <= 8 && (size_t)T * H * 2 <= (size_t)rr.bst * rr.bslot) a.xres = T;
         } else {
             k_permute_f16<<<p.num_sms * 4, 256, 0, st>>>(static_cast<const uint16_t *>(x), p.pad_pair, p.poff,
                                                          p.scratch, E, H, a.P, c.top_k, p.xp16);
