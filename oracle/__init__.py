@@ -27,8 +27,9 @@ into the combine (#701), the shared expert added beside the routed ones (#686);
 "bloomery 0.3.9", New: an f64 oracle with a band for sums whose order is the
 hardware's.
 
-Parity status: the codecs, quantiser, router, top-k, grouping and the FFN are
-pinned by the tests in ``tests/test_oracle_*.py`` (tables, library
+Parity status: the codecs (E2M1, E4M3, E8M0), the NVFP4 and MXFP4
+quantisers, router, top-k, grouping and the FFN are pinned by the tests in
+``tests/test_oracle_*.py`` (tables, library
 conversions, brute force, identities, a hand-worked example, a dense-MLP
 special case).  Nothing here is "parity unpinned".
 """
@@ -52,6 +53,8 @@ ROUTER_SOFTMAX = 0
 ROUTER_SIGMOID = 1
 MODE_W4A16 = 0
 MODE_W4A4 = 1
+FMT_NVFP4 = 0      # E2M1 codes, E4M3 scale a 16-value block, fp32 tensor scale
+FMT_MXFP4 = 1      # E2M1 codes, E8M0 scale a 32-value block (OCP MX), no tensor scale
 
 
 def build_library(force: bool = False) -> str:
@@ -98,6 +101,10 @@ def lib():
             L.oracle_router_logits.argtypes = [P, c.c_int32, c.c_int32, P, c.c_int32, P, P]
             L.oracle_topk.argtypes = [P, c.c_int32, c.c_int32, c.c_int32, c.c_int32, c.c_int32, P, P]
             L.oracle_group.argtypes = [P, c.c_int64, c.c_int32, P, P]
+            L.oracle_e8m0_value.argtypes = [c.c_int]
+            L.oracle_e8m0_value.restype = c.c_double
+            L.oracle_e8m0_table.argtypes = [P]
+            L.oracle_mxfp4_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P]
             _lib = L
     return _lib
 
@@ -190,6 +197,41 @@ def dequantize(codes, scales, ts) -> np.ndarray:
     return e2m1_table()[q] * s * float(ts)
 
 
+# ------------------------------------------------------------------ MXFP4
+
+def e8m0_table() -> np.ndarray:
+    out = np.zeros(256, np.float64)
+    lib().oracle_e8m0_table(_p(out))
+    return out
+
+
+def quantize_mx(x):
+    """MXFP4-quantise a [rows][cols] fp32 matrix (OCP MX: E8M0 scale a
+    32-value block, E2M1 codes).  Returns (codes, scales)."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    assert x.ndim == 2 and x.shape[1] % 32 == 0
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), np.uint8)
+    scales = np.zeros((rows, cols // 32), np.uint8)
+    lib().oracle_mxfp4_quantize(_p(x), rows, cols, _p(codes), _p(scales))
+    return codes, scales
+
+
+def dequantize_mx(codes, scales) -> np.ndarray:
+    """MXFP4 -> FP64: E2M1(code) * 2^(scale - 127)."""
+    q = unpack_codes(codes)
+    s = np.repeat(e8m0_table()[np.asarray(scales, np.uint8)], 32, axis=-1)
+    return e2m1_table()[q] * s
+
+
+def dequant(w, fmt: int = FMT_NVFP4) -> np.ndarray:
+    """One packed weight as the expert callback gives it: (codes, scales, ts)
+    for NVFP4, (codes, scales[, ignored]) for MXFP4."""
+    if fmt == FMT_MXFP4:
+        return dequantize_mx(w[0], w[1])
+    return dequantize(*w)
+
+
 # Decisions of the quantiser that lie this close to their rounding boundary
 # (relative to the E4M3 argument for a scale, to the block's largest |x/den|
 # for a code) are the ones a different fp32 summation order of the quantised
@@ -247,6 +289,44 @@ def quant_decisions(x, ts: float, margin: float = FLIP_MARGIN):
         alt = e2m1_table()[e2m1_from_f32(xb[r, b] / d_alt)] * (s_alt[r, b] * float(ts))
         fb[r, b] += np.abs(alt - deq[r, 16 * b:16 * b + 16])
     return deq, flip, int(code_flag.sum() + scale_flag.sum())
+
+
+def mx_quant_decisions(x, margin: float = FLIP_MARGIN):
+    """MXFP4 counterpart of quant_decisions: quantise fp32 rows x, and bound
+    what the decisions within `margin` of their boundary could change.  A
+    block scale (E = floor(log2(amax)) - 2) is near its boundary when amax is
+    within margin * amax of a power of two: the block is re-quantised with the
+    neighbouring exponent.  A code is near its boundary when |x| / 2^E is
+    within margin * (the block's largest |x| / 2^E) of an E2M1 midpoint: the
+    neighbouring E2M1 value.  Returns (deq, flip, n)."""
+    x = np.ascontiguousarray(np.asarray(x, np.float32))
+    R, C = x.shape
+    codes, scales = quantize_mx(x)
+    deq = dequantize_mx(codes, scales)
+    flip = np.zeros((R, C), np.float64)
+    if R == 0:
+        return deq, flip, 0
+    xb = x.reshape(R, C // 32, 32).astype(np.float64)
+    X = e8m0_table()[scales.astype(np.int64)]                     # [R][C/32]
+    bamax = np.abs(xb).max(axis=2)
+    with np.errstate(divide="ignore"):
+        lg = np.log2(np.where(bamax > 0, bamax, 1.0))
+    m = np.round(lg)
+    near = (bamax > 0) & (np.abs(bamax - np.exp2(m)) < margin * bamax)
+    v = np.abs(xb) / X[..., None]
+    dist = np.abs(v[..., None] - _E2M1_MIDS)
+    mi = dist.argmin(axis=-1)
+    vmax = v.max(axis=2, keepdims=True)
+    code_flag = dist.min(axis=-1) < margin * vmax
+    fb = flip.reshape(R, C // 32, 32)
+    fb += np.where(code_flag, _E2M1_STEP[mi] * X[..., None], 0.0)
+    for r, b in zip(*np.nonzero(near)):
+        s_alt = int(scales[r, b]) + (1 if bamax[r, b] < np.exp2(m[r, b]) else -1)
+        s_alt = min(max(s_alt, 0), 254)
+        Xa = np.float32(np.ldexp(1.0, s_alt - 127))
+        alt = e2m1_table()[e2m1_from_f32(x[r, 32 * b:32 * b + 32] / Xa)] * float(Xa)
+        fb[r, b] += np.abs(alt - deq[r, 32 * b:32 * b + 32])
+    return deq, flip, int(code_flag.sum() + near.sum())
 
 
 # ------------------------------------------------------------------ router
@@ -332,7 +412,7 @@ def swiglu_quantize(h_list):
 
 
 def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormalize=True,
-            mode=MODE_W4A16, shared=None, keep=False, h_in=None):
+            mode=MODE_W4A16, shared=None, keep=False, h_in=None, fmt=FMT_NVFP4):
     """The whole MoE FFN in FP64.
 
     expert(e) -> ((gc, gs, gts), (uc, us, uts), (dc, ds, dts)): expert e's packed
@@ -343,6 +423,13 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
     routed expert the batch touches, plus "shared": [T][Is] when a shared expert
     is given.  The oracle then skips the gate/up products and rounds or
     quantises these h values by the mode's rule, then runs down and combine.
+    fmt: FMT_NVFP4, or FMT_MXFP4 (MXFP4 weights; expert(e) gives (codes,
+    scales, ignored) triples).  In W4A4 the activations and the SwiGLU output
+    are then quantised to the same format: MXFP4 blocks of 32 with their own
+    E8M0 scales, with no tensor scale ("MXFP4 routed prompt GEMM on the
+    block-scaled tensor cores", "NVIDIA FP4-Local checkpoints on DGX Spark
+    ... #565", section 6 Round 3; E8M0 blocks of 32 as in the pages' MXFP8
+    weights, #521).
     Returns a dict with the route, the FP64 output and its bf16 bit patterns.
     """
     x_bf16 = np.ascontiguousarray(x_bf16, np.uint16)
@@ -350,7 +437,11 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
     E = router_w.shape[0]
     r = route(x_bf16, router_w, router_bias, k, router_kind, renormalize)
     res = dict(r)
-    if mode == MODE_W4A4:
+    if mode == MODE_W4A4 and fmt == FMT_MXFP4:
+        xc, xs = quantize_mx(bf16_to_f32(x_bf16))
+        xin = dequantize_mx(xc, xs)
+        res.update(x_codes=xc, x_scales=xs, x_ts=1.0)
+    elif mode == MODE_W4A4:
         xc, xs, xts = quantize_activations(x_bf16)
         xin = dequantize(xc, xs, xts)
         res.update(x_codes=xc, x_scales=xs, x_ts=xts)
@@ -362,14 +453,12 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
     out = np.zeros((T, H), np.float64)
 
     def up_part(weights, X):
-        (gc, gs, gts), (uc, us, uts), _ = weights
-        g = X @ dequantize(gc, gs, gts).T
-        u = X @ dequantize(uc, us, uts).T
+        g = X @ dequant(weights[0], fmt).T
+        u = X @ dequant(weights[1], fmt).T
         return silu(g) * u
 
     def down_part(weights, h):
-        _, _, (dc, ds, dts) = weights
-        return h @ dequantize(dc, ds, dts).T
+        return h @ dequant(weights[2], fmt).T
 
     def round_h_bf16(h):
         """W4A16: the SwiGLU output is rounded to bf16 (nearest even) before the
@@ -378,9 +467,13 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         return bf16_to_f64(f64_to_bf16(h))
 
     def quant_h(h_all):
-        """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax.
-        Also returns, per matrix, the flip band of its near-boundary decisions."""
+        """W4A4: SwiGLU output rounded to fp32, quantised with its batch amax
+        (MXFP4: block by block, no tensor scale).  Also returns, per matrix,
+        the flip band of its near-boundary decisions."""
         h32 = [h.astype(np.float32) for h in h_all]
+        if fmt == FMT_MXFP4:
+            qs = [mx_quant_decisions(h) for h in h32]
+            return [q[0] for q in qs], 1.0, [q[1] for q in qs], sum(q[2] for q in qs)
         ts = swiglu_tensor_scale(h32)
         qs = [quant_decisions(h, ts) for h in h32]
         return [q[0] for q in qs], ts, [q[1] for q in qs], sum(q[2] for q in qs)
@@ -411,8 +504,7 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
         y = down_part(expert(e), hs[e])
         np.add.at(out, pr // k, wflat[pr][:, None] * y)
         if e in flips and flips[e].any():
-            _, _, (dc, ds, dts) = expert(e)
-            np.add.at(band, pr // k, np.abs(wflat[pr])[:, None] * (flips[e] @ np.abs(dequantize(dc, ds, dts)).T))
+            np.add.at(band, pr // k, np.abs(wflat[pr])[:, None] * (flips[e] @ np.abs(dequant(expert(e)[2], fmt)).T))
 
     if shared is not None:
         hsh = np.asarray(h_in["shared"]) if h_in is not None else up_part(shared, xin)
@@ -421,8 +513,7 @@ def forward(x_bf16, router_w, router_bias, expert, *, k, router_kind, renormaliz
             n_flip += ns
             res["shared_h_ts"] = ts_s
             if fs.any():
-                _, _, (dc, ds, dts) = shared
-                band += fs @ np.abs(dequantize(dc, ds, dts)).T
+                band += fs @ np.abs(dequant(shared[2], fmt)).T
         else:
             hsh = round_h_bf16(hsh)
         out += down_part(shared, hsh)

@@ -217,6 +217,58 @@ void oracle_nvfp4_quantize(const float *x, int64_t rows, int64_t cols, float ts,
     }
 }
 
+/* ----------------------------------------------------- MXFP4 (OCP MX) */
+
+/* E8M0: an unsigned power of two, value 2^(byte - 127); 0xFF is NaN. */
+double oracle_e8m0_value(int byte)
+{
+    return byte == 255 ? NAN : ldexp(1.0, byte - 127);
+}
+
+void oracle_e8m0_table(double *out256)
+{
+    for (int b = 0; b < 256; ++b) out256[b] = oracle_e8m0_value(b);
+}
+
+/* MXFP4 quantiser, following the OCP Microscaling (MX) v1.0 conversion: for
+ * every block of 32 consecutive values of a row,
+ *   amax  = max |x|;
+ *   E     = floor(log2(amax)) - 2       (2: exponent of E2M1's largest value, 6 = 1.5 * 2^2)
+ *   scale = E + 127, clamped to [0, 254] (an all-zero block: 0)
+ *   code  = E2M1_rne_sat(x / 2^(scale - 127))   (fp32 division by a power of two)
+ * codes: [rows][cols/2], element 2i in bits 0..3; scales: [rows][cols/32].
+ * cols must be a multiple of 32. */
+void oracle_mxfp4_quantize(const float *x, int64_t rows, int64_t cols, uint8_t *codes, uint8_t *scales)
+{
+    int64_t nb = cols / 32;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *blk = x + r * cols + b * 32;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                float a = fabsf(blk[i]);
+                if (a > amax) amax = a;
+            }
+            int s = 0;
+            if (amax > 0.0f) {
+                int e2;
+                frexp((double)amax, &e2);           /* amax = m * 2^e2, m in [0.5, 1) */
+                int e = (e2 - 1) - 2;               /* floor(log2(amax)) - 2 */
+                s = e + 127;
+                if (s < 0) s = 0;
+                if (s > 254) s = 254;
+            }
+            const float X = ldexpf(1.0f, s - 127);
+            uint8_t q[32];
+            for (int i = 0; i < 32; ++i) q[i] = oracle_e2m1_from_f32(blk[i] / X);
+            scales[r * nb + b] = (uint8_t)s;
+            uint8_t *dst = codes + r * (cols / 2) + b * 16;
+            for (int i = 0; i < 16; ++i) dst[i] = (uint8_t)(q[2 * i] | (q[2 * i + 1] << 4));
+        }
+    }
+}
+
 /* ------------------------------------------------------------------ router */
 
 /* Router logits l[t][e] = x[t] . Wr[e] (+ bias[e]) in fp32, in a fixed order

@@ -5,7 +5,8 @@ that the pins which guard that part of it fail:
   * codes unpacked with the nibbles swapped (element 2i read from bits 4..7);
   * an expert offset off by one;
   * the last pairs of the last expert's segment dropped (a lost last tile);
-  * the per-expert tensor scale left out of the dequantisation.
+  * the per-expert tensor scale left out of the dequantisation;
+  * MXFP4 block scales applied to 16-value blocks.
 The mistakes are planted by replacing a function of the oracle module for the
 duration of one test (monkeypatch); nothing here touches the CUDA path."""
 import numpy as np
@@ -85,3 +86,13 @@ def test_missing_tensor_scale_is_caught(monkeypatch):
     monkeypatch.setattr(oracle, "dequantize", _no_tensor_scale)
     _fails(ffn.test_hand_worked_one_token_two_experts)
     _fails(ffn.test_w4a4_hand_worked_swiglu_tensor_scales)
+
+
+def test_mx_scale_block_of_the_wrong_size_is_caught(monkeypatch):
+    import test_oracle_mx as mx
+    def bad(codes, scales):   # each scale applied to 16 values, the row's scales then reused
+        s16 = np.repeat(oracle.e8m0_table()[np.asarray(scales, np.uint8)], 16, axis=-1)
+        return oracle.e2m1_table()[oracle.unpack_codes(codes)] * np.concatenate([s16, s16], axis=-1)
+    monkeypatch.setattr(oracle, "dequantize_mx", bad)
+    _fails(mx.test_error_bound_and_clipping)
+    _fails(mx.test_quantiser_is_idempotent_on_its_grid)
