@@ -76,6 +76,25 @@ typedef enum { MOE_ROUTER_SOFTMAX = 0, MOE_ROUTER_SIGMOID = 1 } moe_router_kind;
  * router reads half the bytes. */
 typedef enum { MOE_ROUTER_F32 = 0, MOE_ROUTER_BF16 = 1 } moe_router_dtype;
 
+/* Block format of the expert weights.
+ *   NVFP4: E2M1 codes, one E4M3 scale a 16-value block, one fp32 tensor scale a
+ *          weight (the format described above).
+ *   MXFP4: E2M1 codes, one E8M0 scale (2^(byte - 127)) a 32-value block, no
+ *          tensor scale; the OCP Microscaling conversion: byte =
+ *          clamp(floor(log2(block amax)) - 2 + 127, 0, 254), code =
+ *          E2M1_rne_sat(x / 2^(byte - 127)).  The pages name MXFP4 routed
+ *          experts and an MXFP4 routed prompt GEMM on block-scaled tensor cores
+ *          ("NVIDIA FP4-Local checkpoints on DGX Spark ... #565", section 6
+ *          Round 3; "bloomery 0.3.13", Also, #1154) and MX blocks of 32 with an
+ *          E8M0 scale (#521).  In W4A4 the activations and the SwiGLU output
+ *          are then MXFP4 as well (every block on its own scale, no batch
+ *          amax).  MXFP4 plans need H, I (and the shared I) multiples of 512;
+ *          they run on the CUDA cores, and W4A16 also on the warp MMAs (whose
+ *          f16 operands hold code x scale exactly only for block scales from
+ *          2^-23 to 2^13: a weight block outside that range is a device error
+ *          there). */
+typedef enum { MOE_WEIGHTS_NVFP4 = 0, MOE_WEIGHTS_MXFP4 = 1 } moe_weight_format;
+
 /* W4A16: activations stay bf16; the SwiGLU output is rounded to bf16 (RNE)
  *        before the down product.
  * W4A4:  activations are NVFP4-quantised (tensor scale from the batch amax);
@@ -96,10 +115,13 @@ typedef struct {
     int32_t has_shared;   /* 1: a shared expert is added to every token */
     int32_t shared_inter; /* shared expert's intermediate (multiple of 128, at most 8192) */
     int32_t router_dtype; /* moe_router_dtype of router_w in moe_route / moe_forward */
+    int32_t weight_format; /* moe_weight_format of the expert weights */
 } moe_config;
 
-/* One NVFP4 weight stacked over `count` experts: codes [count][N][K/2],
- * scales [count][N][K/16], tensor_scale [count] (all device memory). */
+/* One weight stacked over `count` experts: codes [count][N][K/2] and
+ *   NVFP4: scales [count][N][K/16] (E4M3), tensor_scale [count] fp32;
+ *   MXFP4: scales [count][N][K/32] (E8M0), tensor_scale ignored (may be NULL).
+ * All device memory. */
 typedef struct {
     const uint8_t *codes;
     const uint8_t *scales;
@@ -166,7 +188,8 @@ moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, c
 /* W4A4 activation quantisation on its own (the step moe_forward runs first in
  * W4A4): tensor scale from the amax of all of x[T][H], then per 16-block
  * E4M3 scales and E2M1 codes.
- *   codes [T][H/2], scales [T][H/16], tensor_scale [1] fp32 (device). */
+ *   codes [T][H/2], scales [T][H/16], tensor_scale [1] fp32 (device).
+ * An MXFP4 plan writes MXFP4 instead: scales [T][H/32] E8M0, tensor_scale 1. */
 moe_status moe_quantize_act(moe_plan plan, const void *x_bf16, int32_t T, uint8_t *codes,
                             uint8_t *scales, float *tensor_scale, void *stream);
 
@@ -187,6 +210,12 @@ moe_status moe_quantize_nvfp4(const float *w, int32_t batch, int32_t rows, int32
  * Needs no plan.  MOE_ERR_INVALID_ARG for an unknown format or n < 0. */
 typedef enum { MOE_FMT_E4M3 = 0, MOE_FMT_E2M1 = 1 } moe_format;
 moe_status moe_convert_f32(const float *src, int64_t n, int32_t format, uint8_t *dst, void *stream);
+
+/* MXFP4 quantisation (OCP MX, see moe_weight_format) of fp32 weights
+ * w[rows][cols] (device; stack experts as rows): codes [rows][cols/2], E8M0
+ * scales [rows][cols/32].  cols must be a multiple of 32.  Needs no plan. */
+moe_status moe_quantize_mxfp4(const float *w, int64_t rows, int32_t cols, uint8_t *codes, uint8_t *scales,
+                              void *stream);
 
 /* Synchronise `stream`, then return and clear the plan's device error word
  * (MOE_OK, MOE_ERR_NONFINITE, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE). */

@@ -19,6 +19,7 @@ LIB_PATH = _build.LIB
 
 ROUTER_SOFTMAX, ROUTER_SIGMOID = 0, 1
 ROUTER_F32, ROUTER_BF16 = 0, 1
+WEIGHTS_NVFP4, WEIGHTS_MXFP4 = 0, 1
 W4A16, W4A4 = 0, 1
 
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED_SHAPE", 3: "MOE_ERR_MISALIGNED",
@@ -29,7 +30,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_NONFINITE, ERR_T
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_route", "moe_forward", "moe_forward_host",
            "moe_quantize_act", "moe_quantize_nvfp4", "moe_plan_sync_status", "moe_plan_debug_buffer",
            "moe_plan_set_profiling", "moe_plan_read_profile", "moe_plan_set_path", "moe_plan_check_timeout",
-           "moe_route_static", "moe_convert_f32", "moe_status_string", "moe_version"]
+           "moe_route_static", "moe_convert_f32", "moe_quantize_mxfp4", "moe_status_string", "moe_version"]
 FMT_E4M3, FMT_E2M1 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_WARP_MMA = 0, 1, 2, 3
 STAGES = ["route", "group", "quant_x", "permute", "gate_up", "quant_h", "down", "finalize"]
@@ -44,7 +45,7 @@ class MoeError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "hidden", "inter", "num_experts", "top_k", "max_tokens", "router", "renormalize", "mode",
-        "has_shared", "shared_inter", "router_dtype")]
+        "has_shared", "shared_inter", "router_dtype", "weight_format")]
 
 
 class Nvfp4(ctypes.Structure):
@@ -81,6 +82,7 @@ def lib():
         L.moe_route_static.argtypes = [P, I32, I32, P, P, I32, I32, I32, I32, P, P, P, P, P]
         L.moe_plan_read_profile.argtypes = [P, P, P, P]
         L.moe_convert_f32.argtypes = [P, ctypes.c_int64, I32, P, P]
+        L.moe_quantize_mxfp4.argtypes = [P, ctypes.c_int64, I32, P, P, P]
         L.moe_status_string.argtypes = [I32]
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_version.restype = ctypes.c_char_p
@@ -143,6 +145,21 @@ def quantize_nvfp4(w: torch.Tensor, out: NvfpTensor | None = None, stream=None) 
     return out
 
 
+def quantize_mxfp4(w: torch.Tensor, out: NvfpTensor | None = None, stream=None) -> NvfpTensor:
+    """MXFP4-quantise fp32 weights [batch][rows][cols] (or [rows][cols]) on the
+    device: E2M1 codes and E8M0 block-of-32 scales (no tensor scale: ts is None)."""
+    assert w.is_cuda and w.dtype == torch.float32 and w.is_contiguous()
+    if w.dim() == 2:
+        w = w.unsqueeze(0)
+    b, r, c = w.shape
+    if out is None:
+        out = NvfpTensor(torch.empty(b, r, c // 2, dtype=torch.uint8, device=w.device),
+                         torch.empty(b, r, c // 32, dtype=torch.uint8, device=w.device), None)
+    _check(lib().moe_quantize_mxfp4(_ptr(w), b * r, c, _ptr(out.codes), _ptr(out.scales), _stream(stream)),
+           "moe_quantize_mxfp4")
+    return out
+
+
 def convert_f32(src: torch.Tensor, fmt: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """The device's fp32 -> E4M3 byte (FMT_E4M3) or E2M1 code (FMT_E2M1) conversion, element-wise."""
     assert src.is_cuda and src.dtype == torch.float32 and src.is_contiguous()
@@ -156,9 +173,9 @@ class Plan:
     """A moe_plan: configuration plus device workspace for up to max_tokens tokens."""
 
     def __init__(self, hidden, inter, num_experts, top_k, max_tokens, router=ROUTER_SOFTMAX, renormalize=True,
-                 mode=W4A16, has_shared=False, shared_inter=0, router_dtype=ROUTER_F32):
+                 mode=W4A16, has_shared=False, shared_inter=0, router_dtype=ROUTER_F32, weight_format=WEIGHTS_NVFP4):
         self.cfg = Config(hidden, inter, num_experts, top_k, max_tokens, router, int(bool(renormalize)), mode,
-                          int(bool(has_shared)), shared_inter if has_shared else 0, router_dtype)
+                          int(bool(has_shared)), shared_inter if has_shared else 0, router_dtype, weight_format)
         h = ctypes.c_void_p()
         _check(lib().moe_plan_create(ctypes.byref(self.cfg), ctypes.byref(h)), "moe_plan_create")
         self.handle = h
@@ -219,7 +236,8 @@ class Plan:
     def quantize_act(self, x, stream=None):
         T, H = x.shape
         codes = torch.empty(T, H // 2, dtype=torch.uint8, device=x.device)
-        scales = torch.empty(T, H // 16, dtype=torch.uint8, device=x.device)
+        scales = torch.empty(T, H // (32 if self.cfg.weight_format == WEIGHTS_MXFP4 else 16), dtype=torch.uint8,
+                             device=x.device)
         ts = torch.empty(1, dtype=torch.float32, device=x.device)
         _check(lib().moe_quantize_act(self.handle, _ptr(x), T, _ptr(codes), _ptr(scales), _ptr(ts), _stream(stream)),
                "moe_quantize_act")

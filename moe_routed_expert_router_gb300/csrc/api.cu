@@ -47,6 +47,10 @@ moe_status check_config(const moe_config *c) {
     if (c->renormalize != 0 && c->renormalize != 1) return MOE_ERR_INVALID_ARG;
     if (c->has_shared != 0 && c->has_shared != 1) return MOE_ERR_INVALID_ARG;
     if (c->router_dtype != MOE_ROUTER_F32 && c->router_dtype != MOE_ROUTER_BF16) return MOE_ERR_INVALID_ARG;
+    if (c->weight_format != MOE_WEIGHTS_NVFP4 && c->weight_format != MOE_WEIGHTS_MXFP4) return MOE_ERR_INVALID_ARG;
+    if (c->weight_format == MOE_WEIGHTS_MXFP4 &&
+        (c->hidden % 512 || c->inter % 512 || (c->has_shared && c->shared_inter % 512)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return MOE_ERR_INVALID_ARG;
     if (c->hidden < 256 || c->hidden % 256 || c->hidden > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (c->inter < 128 || c->inter % 128 || c->inter > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -58,21 +62,25 @@ moe_status check_config(const moe_config *c) {
     return MOE_OK;
 }
 
-moe_status check_nvfp4(const moe_nvfp4 &w) {
-    if (!w.codes || !w.scales || !w.tensor_scale) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(w.codes) || !aligned4(w.tensor_scale)) return MOE_ERR_MISALIGNED;
+moe_status check_nvfp4(const moe_nvfp4 &w, bool mx) {
+    if (!w.codes || !w.scales || (!mx && !w.tensor_scale)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w.codes) || (!mx && !aligned4(w.tensor_scale))) return MOE_ERR_MISALIGNED;
     return MOE_OK;
 }
 
-moe_status check_set(const moe_expert_set *s) {
+moe_status check_set(const moe_expert_set *s, bool mx) {
     if (!s) return MOE_ERR_INVALID_ARG;
     moe_status r;
-    if ((r = check_nvfp4(s->gate)) != MOE_OK) return r;
-    if ((r = check_nvfp4(s->up)) != MOE_OK) return r;
-    return check_nvfp4(s->down);
+    if ((r = check_nvfp4(s->gate, mx)) != MOE_OK) return r;
+    if ((r = check_nvfp4(s->up, mx)) != MOE_OK) return r;
+    return check_nvfp4(s->down, mx);
 }
 
-moe::ExpertPtrs ptrs(const moe_expert_set &s) {
+// MXFP4 weights have no tensor scale: the kernels read the plan's array of ones.
+moe::ExpertPtrs ptrs(const moe_expert_set &s, const moe::Plan &p) {
+    if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4)
+        return moe::ExpertPtrs{s.gate.codes, s.gate.scales, s.up.codes, s.up.scales, s.down.codes, s.down.scales,
+                               p.ones, p.ones, p.ones};
     return moe::ExpertPtrs{s.gate.codes, s.gate.scales, s.up.codes, s.up.scales, s.down.codes, s.down.scales,
                            s.gate.tensor_scale, s.up.tensor_scale, s.down.tensor_scale};
 }
@@ -132,6 +140,7 @@ void carve(Plan &p, Carver &c) {
     p.hts = c.take<float>(64);
     p.acc = c.take<float>(sizeof(float) * T * H);
     p.err = c.take<int>(64);
+    p.ones = c.take<float>(sizeof(float) * (E + 1));
     p.x_stage = c.take<void>(2 * T * H);
     p.out_stage = c.take<void>(2 * T * H);
 }
@@ -182,6 +191,10 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const void *r
     if (plan->path == MOE_PATH_AUTO) {
         wm = moe::warp_mma_supported(p) && T * p.cfg.top_k < 2 * p.cfg.num_experts;
         tc = wm || (moe::tc_supported(p) && (p.cfg.mode == MOE_W4A16 || T * p.cfg.top_k >= 64));
+        if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4) {   // the warp MMAs (W4A16) or the CUDA cores
+            wm = moe::warp_mma_supported(p);
+            tc = wm;
+        }
     }
     // rows a tensor-core tile covers: 32 for the warp MMAs, 64 for the W4A16
     // tcgen05 GEMMs, 128 for the W4A4 ones
@@ -204,8 +217,8 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const void *r
         if (s.done(moe::launch_quant_act(p, x, T, p.xq, p.xsc, p.xts, true, st), 1) != cudaSuccess)
             return MOE_ERR_CUDA;
     }
-    moe::ExpertPtrs r = ptrs(*routed), sh{};
-    if (shared) sh = ptrs(*shared);
+    moe::ExpertPtrs r = ptrs(*routed, p), sh{};
+    if (shared) sh = ptrs(*shared, p);
     const moe::ExpertPtrs *shp = shared ? &sh : nullptr;
     {
         Stage s(plan, MOE_STAGE_GATE_UP, st);
@@ -280,6 +293,10 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
     real.base = static_cast<char *>(p.ws);
     carve(p, real);
     cudaError_t e = cudaMemset(p.ws, 0, p.ws_bytes);
+    if (e == cudaSuccess) {
+        std::vector<float> ones((size_t)cfg->num_experts + 1, 1.0f);
+        e = cudaMemcpy(p.ones, ones.data(), sizeof(float) * ones.size(), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = moe::configure_group_kernel();
     if (e == cudaSuccess) e = moe::configure_simt();
     if (e == cudaSuccess && moe::tc_supported(p)) e = moe::configure_tc(p);
@@ -295,7 +312,9 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
 
 moe_status moe_plan_set_path(moe_plan plan, int32_t path) {
     if (!plan || path < MOE_PATH_AUTO || path > MOE_PATH_WARP_MMA) return MOE_ERR_INVALID_ARG;
-    if (path == MOE_PATH_TENSOR_CORE && !moe::tc_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (path == MOE_PATH_TENSOR_CORE &&
+        (!moe::tc_supported(plan->p) || plan->p.cfg.weight_format == MOE_WEIGHTS_MXFP4))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_WARP_MMA && !moe::warp_mma_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     plan->path = path;
     return MOE_OK;
@@ -361,9 +380,10 @@ moe_status moe_forward(moe_plan plan, const void *x_bf16, int32_t T, const void 
                        const moe_expert_set *routed, const moe_expert_set *shared, void *out_bf16, void *stream) {
     moe_status st = check_call(plan, x_bf16, T, router_w, router_bias);
     if (st != MOE_OK) return st;
-    if ((st = check_set(routed)) != MOE_OK) return st;
+    const bool mx = plan->p.cfg.weight_format == MOE_WEIGHTS_MXFP4;
+    if ((st = check_set(routed, mx)) != MOE_OK) return st;
     if (plan->p.cfg.has_shared) {
-        if ((st = check_set(shared)) != MOE_OK) return st;
+        if ((st = check_set(shared, mx)) != MOE_OK) return st;
     } else if (shared) {
         return MOE_ERR_INVALID_ARG;
     }
@@ -384,8 +404,9 @@ moe_status moe_forward_host(moe_plan plan, const void *x_bf16_host, int32_t T, c
     const size_t bytes = (size_t)T * p.cfg.hidden * 2;
     moe_status st = check_call(plan, p.x_stage, T, router_w, router_bias);
     if (st != MOE_OK) return st;
-    if ((st = check_set(routed)) != MOE_OK) return st;
-    if (p.cfg.has_shared && (st = check_set(shared)) != MOE_OK) return st;
+    const bool mx = p.cfg.weight_format == MOE_WEIGHTS_MXFP4;
+    if ((st = check_set(routed, mx)) != MOE_OK) return st;
+    if (p.cfg.has_shared && (st = check_set(shared, mx)) != MOE_OK) return st;
     if (!p.cfg.has_shared && shared) return MOE_ERR_INVALID_ARG;
     if (T == 0) return MOE_OK;
     if (cudaMemcpyAsync(p.x_stage, x_bf16_host, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -416,6 +437,16 @@ moe_status moe_quantize_nvfp4(const float *w, int32_t batch, int32_t rows, int32
     if (!aligned16(w) || !aligned16(codes) || !aligned4(tensor_scale)) return MOE_ERR_MISALIGNED;
     return cuda_status(moe::launch_quant_nvfp4(w, batch, rows, cols, codes, scales, tensor_scale,
                                                static_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_quantize_mxfp4(const float *w, int64_t rows, int32_t cols, uint8_t *codes, uint8_t *scales,
+                              void *stream) {
+    if (rows < 0 || cols < 0) return MOE_ERR_INVALID_ARG;
+    if (cols % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0 || cols == 0) return MOE_OK;
+    if (!w || !codes || !scales) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(codes)) return MOE_ERR_MISALIGNED;
+    return cuda_status(moe::launch_quant_mxfp4(w, rows, cols, codes, scales, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status moe_convert_f32(const float *src, int64_t n, int32_t format, uint8_t *dst, void *stream) {

@@ -1,4 +1,4 @@
-// Decode-shaped expert FFN on the CUDA cores: each expert's NVFP4 weight rows
+// Decode-shaped expert FFN on the CUDA cores: each expert's NVFP4 (or MXFP4) weight rows
 // are streamed once (128-bit loads of codes, 16-bit loads of scale pairs) for
 // all the rows routed to it, E2M1 is decoded in registers, and the dot products
 // run in fp32.  Work is a list of chunks (up to kChunkRows rows of one expert)
@@ -59,10 +59,11 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
 // rows held in shared memory (swizzled), accumulated into acc[].  The unit is
 // decoded once (E2M1 -> f16x2 -> fp32 pairs) and used for all NR rows; the 16
 // products of a scale block are summed in fp32 pairs, then scaled.
-template <int NR>
+// MX (MXFP4 weights): one E8M0 scale byte for the whole 32-value unit.
+template <int NR, int MX = 0>
 __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const float *xs, int K, int u,
                                          float (&acc)[kChunkRows]) {
-    const float2 scf = f16x2_to_f32x2(e4m3x2_to_f16x2(sp));
+    const float2 scf = MX ? make_float2(e8m0_to_f32(sp), e8m0_to_f32(sp)) : f16x2_to_f32x2(e4m3x2_to_f16x2(sp));
     const uint32_t words[4] = {c.x, c.y, c.z, c.w};
     const int cs = K >> 3;   // floats between chunk j and chunk j+1 of a unit (K/32 units x 4)
     const float *xu = xs + u * 4;
@@ -92,7 +93,7 @@ __device__ __forceinline__ void unit_dot(const uint4 &c, uint32_t sp, const floa
     }
 }
 
-template <int MODE>
+template <int MODE, int MX>
 __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
     const int H = a.H;
     for (int idx = threadIdx.x; idx < ch.z * (H / 16); idx += blockDim.x) {
@@ -111,7 +112,8 @@ __device__ void stage_x(const FfnArgs &a, const int4 &ch, float *xs) {
                 }
             } else {
                 const uint2 cw = *reinterpret_cast<const uint2 *>(a.xq + (size_t)tok * (H / 2) + b * 8);
-                const float sc = e4m3_to_f32(a.xsc[(size_t)tok * (H / 16) + b]);
+                const float sc = MX ? e8m0_to_f32(a.xsc[(size_t)tok * (H / 32) + b / 2])
+                                    : e4m3_to_f32(a.xsc[(size_t)tok * (H / 16) + b]);
                 uint32_t h[8];
                 e2m1x8_to_f16x8(cw.x, *reinterpret_cast<uint32_t(*)[4]>(h));
                 e2m1x8_to_f16x8(cw.y, *reinterpret_cast<uint32_t(*)[4]>(h + 4));
@@ -165,6 +167,7 @@ __device__ __forceinline__ int gateup_items(const FfnArgs &a) {
 // Issue step q of a warp's gate/up stream (lane 0): feature
 // fg*128 + warp*16 + (q % 16) of item q / 16's chunk, i.e. one gate row and one
 // up row (codes + scales) into slot q.  Returns false past the last item.
+template <int MX>
 __device__ __forceinline__ bool gateup_issue(const FfnArgs &a, const Ring &rg, int q, int n_items, int nw, int warp) {
     const int per_warp = 128 / nw;
     const int item = blockIdx.x + (q / per_warp) * gridDim.x;
@@ -178,15 +181,16 @@ __device__ __forceinline__ bool gateup_issue(const FfnArgs &a, const Ring &rg, i
     uint8_t *dst = rg.slot(q);
     uint64_t *bar = rg.bar(q);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, 2 * (H / 2) + 2 * (H / 16));
+    const int sb = MX ? H / 32 : H / 16;   // scale bytes a row
+    mbar_expect_tx(bar, 2 * (H / 2) + 2 * sb);
     bulk_copy(dst, W.gc + row * (H / 2), H / 2, bar);
     bulk_copy(dst + H / 2, W.uc + row * (H / 2), H / 2, bar);
-    bulk_copy(dst + H, W.gs + row * (H / 16), H / 16, bar);
-    bulk_copy(dst + H + H / 16, W.us + row * (H / 16), H / 16, bar);
+    bulk_copy(dst + H, W.gs + row * sb, sb, bar);
+    bulk_copy(dst + H + sb, W.us + row * sb, sb, bar);
     return true;
 }
 
-template <int MODE, int NR>
+template <int MODE, int NR, int MX>
 __device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *slot, const int4 &ch, int i,
                                                const float *xs, float tsg, float tsu, float &lmax) {
     const int lane = threadIdx.x & 31;
@@ -197,10 +201,16 @@ __device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *
     for (int u = lane; u < units; u += 32) {
         const uint4 cg = *reinterpret_cast<const uint4 *>(slot + u * 16);
         const uint4 cu = *reinterpret_cast<const uint4 *>(slot + H / 2 + u * 16);
-        const uint32_t sg = *reinterpret_cast<const unsigned short *>(slot + H + u * 2);
-        const uint32_t su = *reinterpret_cast<const unsigned short *>(slot + H + H / 16 + u * 2);
-        unit_dot<NR>(cg, sg, xs, H, u, ag);
-        unit_dot<NR>(cu, su, xs, H, u, au);
+        uint32_t sg, su;
+        if (MX) {
+            sg = slot[H + u];
+            su = slot[H + H / 32 + u];
+        } else {
+            sg = *reinterpret_cast<const unsigned short *>(slot + H + u * 2);
+            su = *reinterpret_cast<const unsigned short *>(slot + H + H / 16 + u * 2);
+        }
+        unit_dot<NR, MX>(cg, sg, xs, H, u, ag);
+        unit_dot<NR, MX>(cu, su, xs, H, u, au);
     }
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
@@ -228,13 +238,13 @@ __device__ __forceinline__ void gateup_compute(const FfnArgs &a, const uint8_t *
 // Gate + up + SwiGLU.  Dynamic shared memory: x tile [kChunkRows][H] fp32,
 // then nw warps x `slots` slots of (2 code rows + 2 scale rows), then the
 // slot barriers.
-template <int MODE>
+template <int MODE, int MX>
 __global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int H = a.H;
     float *xs = reinterpret_cast<float *>(smem);
-    const int slot_bytes = H + H / 8;
+    const int slot_bytes = H + (MX ? H / 16 : H / 8);
     uint8_t *rings = smem + (size_t)kChunkRows * H * 4;
     uint64_t *bars = reinterpret_cast<uint64_t *>(rings + (size_t)nw * slots * slot_bytes);
     Ring rg{rings + (size_t)warp * slots * slot_bytes, bars + warp * slots, slot_bytes, slots};
@@ -244,10 +254,11 @@ __global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
     __syncthreads();
     const int n_items = gateup_items(a);
     const int per_warp = 128 / nw;
-    const float xscale = (MODE == MOE_W4A4) ? __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f) : 1.0f;
+    // W4A4 activation tensor scale (MXFP4 activations have none)
+    const float xscale = (MODE == MOE_W4A4 && !MX) ? __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f) : 1.0f;
     int issued = 0;
     if (lane == 0)
-        while (issued < slots && gateup_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+        while (issued < slots && gateup_issue<MX>(a, rg, issued, n_items, nw, warp)) ++issued;
     issued = __shfl_sync(0xffffffffu, issued, 0);
     bool ok = true;
     int q = 0, done = 0;
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
         const ExpertPtrs &W = sh ? a.s : a.r;
         const int e = sh ? 0 : ch.x;
         __syncthreads();
-        stage_x<MODE>(a, ch, xs);
+        stage_x<MODE, MX>(a, ch, xs);
         __syncthreads();
         const float tsg = W.gts[e] * xscale, tsu = W.uts[e] * xscale;
         float lmax = 0.0f;
@@ -269,14 +280,14 @@ __global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
                 const uint8_t *slot = rg.slot(q);
                 const int i = fg * 128 + warp * per_warp + f;
                 switch (ch.z) {
-                    case 1: gateup_compute<MODE, 1>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
-                    case 2: gateup_compute<MODE, 2>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
-                    case 3: gateup_compute<MODE, 3>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
-                    default: gateup_compute<MODE, 4>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    case 1: gateup_compute<MODE, 1, MX>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    case 2: gateup_compute<MODE, 2, MX>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    case 3: gateup_compute<MODE, 3, MX>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
+                    default: gateup_compute<MODE, 4, MX>(a, slot, ch, i, xs, tsg, tsu, lmax); break;
                 }
             }
             __syncwarp();
-            if (lane == 0 && ok && issued == q + slots && gateup_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+            if (lane == 0 && ok && issued == q + slots && gateup_issue<MX>(a, rg, issued, n_items, nw, warp)) ++issued;
             issued = __shfl_sync(0xffffffffu, issued, 0);
         }
         if (MODE == MOE_W4A4) {
@@ -288,7 +299,7 @@ __global__ void __launch_bounds__(512) k_gateup_stream(FfnArgs a, int slots) {
     for (int d = done; d < issued; ++d) mbar_wait(rg.bar(d), rg.parity(d), a.err);
 }
 
-template <int MODE>
+template <int MODE, int MX>
 __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
     for (int idx = threadIdx.x; idx < ch.z * (I / 16); idx += blockDim.x) {
         const int r = idx / (I / 16), b = idx % (I / 16);
@@ -307,7 +318,8 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
                 }
             } else {
                 const uint2 cw = *reinterpret_cast<const uint2 *>(a.hq + row * (a.hstride / 2) + b * 8);
-                const float sc = e4m3_to_f32(a.hsc[row * (a.hstride / 16) + b]);
+                const float sc = MX ? e8m0_to_f32(a.hsc[row * (a.hstride / 32) + b / 2])
+                                    : e4m3_to_f32(a.hsc[row * (a.hstride / 16) + b]);
                 uint32_t h[8];
                 e2m1x8_to_f16x8(cw.x, *reinterpret_cast<uint32_t(*)[4]>(h));
                 e2m1x8_to_f16x8(cw.y, *reinterpret_cast<uint32_t(*)[4]>(h + 4));
@@ -331,6 +343,7 @@ __device__ void stage_h(const FfnArgs &a, const int4 &ch, int I, float *hs) {
 // og*128 + w*rpw .. +rpw, streamed kDownRows rows per slot.
 constexpr int kDownRows = 8;
 
+template <int MX>
 __device__ __forceinline__ bool down_issue(const FfnArgs &a, const Ring &rg, int q, int n_items, int nw, int warp) {
     const int steps = 128 / nw / kDownRows;
     const int item = blockIdx.x + (q / steps) * gridDim.x;
@@ -345,13 +358,14 @@ __device__ __forceinline__ bool down_issue(const FfnArgs &a, const Ring &rg, int
     uint8_t *dst = rg.slot(q);
     uint64_t *bar = rg.bar(q);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    mbar_expect_tx(bar, kDownRows * (I / 2 + I / 16));
+    const int sb = MX ? I / 32 : I / 16;   // scale bytes a row
+    mbar_expect_tx(bar, kDownRows * (I / 2 + sb));
     bulk_copy(dst, W.dc + row * (I / 2), kDownRows * (I / 2), bar);
-    bulk_copy(dst + kDownRows * (I / 2), W.ds + row * (I / 16), kDownRows * (I / 16), bar);
+    bulk_copy(dst + kDownRows * (I / 2), W.ds + row * sb, kDownRows * sb, bar);
     return true;
 }
 
-template <int NR>
+template <int NR, int MX>
 __device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *slot, int I, int j0, const float *hs,
                                              float scale, float wrow, int tok) {
     const int lane = threadIdx.x & 31;
@@ -365,8 +379,9 @@ __device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *sl
 #pragma unroll
         for (int q = 0; q < kDownRows; ++q) {
             const uint4 c = *reinterpret_cast<const uint4 *>(slot + q * (I / 2) + u * 16);
-            const uint32_t s = *reinterpret_cast<const unsigned short *>(slot + kDownRows * (I / 2) + q * (I / 16) + u * 2);
-            unit_dot<NR>(c, s, hs, I, u, acc[q]);
+            const uint32_t s = MX ? (uint32_t)slot[kDownRows * (I / 2) + q * (I / 32) + u]
+                                  : *reinterpret_cast<const unsigned short *>(slot + kDownRows * (I / 2) + q * (I / 16) + u * 2);
+            unit_dot<NR, MX>(c, s, hs, I, u, acc[q]);
         }
     }
 #pragma unroll
@@ -385,13 +400,13 @@ __device__ __forceinline__ void down_compute(const FfnArgs &a, const uint8_t *sl
     if (q < kDownRows) atomicAdd(a.acc + (size_t)tk * a.H + j0 + q, y * scale * wr);
 }
 
-template <int MODE>
+template <int MODE, int MX>
 __global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
     const int Imax = max(a.I, a.Is);
     float *hs = reinterpret_cast<float *>(smem);
-    const int slot_bytes = kDownRows * (Imax / 2 + Imax / 16);
+    const int slot_bytes = kDownRows * (Imax / 2 + (MX ? Imax / 32 : Imax / 16));
     uint8_t *rings = smem + (size_t)kChunkRows * Imax * 4;
     uint64_t *bars = reinterpret_cast<uint64_t *>(rings + (size_t)nw * slots * slot_bytes);
     Ring rg{rings + (size_t)warp * slots * slot_bytes, bars + warp * slots, slot_bytes, slots};
@@ -404,7 +419,7 @@ __global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
     const int steps = 128 / nw / kDownRows;
     int issued = 0;
     if (lane == 0)
-        while (issued < slots && down_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+        while (issued < slots && down_issue<MX>(a, rg, issued, n_items, nw, warp)) ++issued;
     issued = __shfl_sync(0xffffffffu, issued, 0);
     bool ok = true;
     int q = 0, done = 0;
@@ -414,7 +429,7 @@ __global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
         const bool sh = (ch.x == a.E);
         const int I = sh ? a.Is : a.I;
         __syncthreads();
-        stage_h<MODE>(a, ch, I, hs);
+        stage_h<MODE, MX>(a, ch, I, hs);
         __syncthreads();
         const ExpertPtrs &W = sh ? a.s : a.r;
         const int e = sh ? 0 : ch.x;
@@ -434,14 +449,14 @@ __global__ void __launch_bounds__(256) k_down_stream(FfnArgs a, int slots) {
                 const uint8_t *slot = rg.slot(q);
                 const int j0 = og * 128 + warp * (128 / nw) + st * kDownRows;
                 switch (ch.z) {
-                    case 1: down_compute<1>(a, slot, I, j0, hs, scale, wrow, tok); break;
-                    case 2: down_compute<2>(a, slot, I, j0, hs, scale, wrow, tok); break;
-                    case 3: down_compute<3>(a, slot, I, j0, hs, scale, wrow, tok); break;
-                    default: down_compute<4>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    case 1: down_compute<1, MX>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    case 2: down_compute<2, MX>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    case 3: down_compute<3, MX>(a, slot, I, j0, hs, scale, wrow, tok); break;
+                    default: down_compute<4, MX>(a, slot, I, j0, hs, scale, wrow, tok); break;
                 }
             }
             __syncwarp();
-            if (lane == 0 && ok && issued == q + slots && down_issue(a, rg, issued, n_items, nw, warp)) ++issued;
+            if (lane == 0 && ok && issued == q + slots && down_issue<MX>(a, rg, issued, n_items, nw, warp)) ++issued;
             issued = __shfl_sync(0xffffffffu, issued, 0);
         }
     }
@@ -480,22 +495,23 @@ bool pick_config1(size_t fixed, size_t slot_bytes, int &nw, int &slots) {
     return false;
 }
 
-template <int MODE>
+template <int MODE, int MX>
 cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st) {
     int nw = 0, slots = 0;
     if (part == 0) {
-        const size_t fixed = (size_t)kChunkRows * a.H * 4, slot = (size_t)a.H + a.H / 8;
+        const size_t fixed = (size_t)kChunkRows * a.H * 4, slot = (size_t)a.H + (MX ? a.H / 16 : a.H / 8);
         if (!pick_config(fixed, slot, 16, nw, slots) && !pick_config1(fixed, slot, nw, slots))
             return cudaErrorInvalidValue;
         const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
-        k_gateup_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
+        k_gateup_stream<MODE, MX><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
         return cudaGetLastError();
     }
     const int Imax = max(a.I, a.Is);
-    const size_t fixed = (size_t)kChunkRows * Imax * 4, slot = (size_t)kDownRows * (Imax / 2 + Imax / 16);
+    const size_t fixed = (size_t)kChunkRows * Imax * 4,
+                 slot = (size_t)kDownRows * (Imax / 2 + (MX ? Imax / 32 : Imax / 16));
     if (!pick_config(fixed, slot, 8, nw, slots) && !pick_config1(fixed, slot, nw, slots)) return cudaErrorInvalidValue;
     const size_t smem = fixed + (size_t)nw * slots * slot + (size_t)nw * slots * 8 + 128;
-    k_down_stream<MODE><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
+    k_down_stream<MODE, MX><<<p.num_sms, nw * 32, smem, st>>>(a, slots);
     return cudaGetLastError();
 }
 
@@ -505,10 +521,15 @@ cudaError_t run_mode(const FfnArgs &a, const Plan &p, int part, cudaStream_t st)
 // that moe_forward makes no configuration call and can be graph-captured.
 cudaError_t configure_simt() {
     const int lim = (int)kSmemBudget;
-    cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A16>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A4>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    const cudaFuncAttribute at = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A16, 0>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A4, 0>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A16, 0>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A4, 0>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A16, 1>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gateup_stream<MOE_W4A4, 1>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A16, 1>, at, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_down_stream<MOE_W4A4, 1>, at, lim);
     return e;
 }
 
@@ -540,7 +561,9 @@ cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtr
     a.r = routed;
     if (shared) a.s = *shared;
     else a.s = routed;
-    return p.cfg.mode == MOE_W4A4 ? run_mode<MOE_W4A4>(a, p, part, st) : run_mode<MOE_W4A16>(a, p, part, st);
+    if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4)
+        return p.cfg.mode == MOE_W4A4 ? run_mode<MOE_W4A4, 1>(a, p, part, st) : run_mode<MOE_W4A16, 1>(a, p, part, st);
+    return p.cfg.mode == MOE_W4A4 ? run_mode<MOE_W4A4, 0>(a, p, part, st) : run_mode<MOE_W4A16, 0>(a, p, part, st);
 }
 
 }  // namespace moe

@@ -605,6 +605,7 @@ struct HcArgs {
     int rcst, rbst, rbslot;
     const uint16_t *x;
     int xres;               // gate/up: tokens whose activations sit resident in shared memory (0: token-row ring)
+    int mx;                 // MXFP4 weights: E8M0 scales, one 16-byte scale box a row for a pair of stages
     // split last round (warp-MMA engine): arrival tickets and partial sums
     int tail_split;
     int *tickets;
@@ -1073,9 +1074,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], 
 // ring slot `bst` (RES = false), or (RES = true, one 8-row token tile) from the
 // resident activations: `bst` is then the shared-memory address of this lane's
 // token row, `xsw` its 16-byte chunk swizzle and `kc` the stage index.
+// E8M0 scale byte -> f16 bits of 2^(byte - 127), for MXFP4 weights on the f16
+// MMAs: code x scale is exact in f16 for byte 104 .. 140 (2^-23 .. 2^13); byte
+// 0 (an all-zero block) gives 0; any other byte gives 0 and sets `bad`.
+__device__ __forceinline__ uint32_t e8m0_f16_bits(uint32_t e, bool &bad) {
+    if (e >= 113 && e <= 140) return (e - 112) << 10;   // normal f16
+    if (e >= 104 && e < 113) return 1u << (e - 103);    // subnormal f16
+    bad |= e != 0;
+    return 0;
+}
+
 template <int NT, bool RES = false>
 __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int rg, int lane, float (&acc)[4][4],
-                                          int kc = 0, uint32_t xsw = 0) {
+                                          int kc = 0, uint32_t xsw = 0, int mx = 0, bool *bad = nullptr) {
     const int g = lane >> 2, q = lane & 3;
     const int r0 = rg * 16 + g, r1 = r0 + 8;
     const uint32_t crow0 = st + op * kHCodeTile + r0 * 128, crow1 = st + op * kHCodeTile + r1 * 128;
@@ -1089,8 +1100,19 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
         uint2 c0, c1;
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c0.x), "=r"(c0.y) : "r"(crow0 + ((ch ^ (uint32_t)(r0 & 7)) << 4) + (q & 1) * 8) : "memory");
         asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(c1.x), "=r"(c1.y) : "r"(crow1 + ((ch ^ (uint32_t)(r1 & 7)) << 4) + (q & 1) * 8) : "memory");
-        // scale bytes of block 4 sb + q for rows r0 (low byte) and r1 (next byte)
-        const uint32_t sc = e4m3x2_to_f16x2(__byte_perm(sw0[sb], sw1[sb], ssel));
+        // scale bytes of block 4 sb + q for rows r0 (low byte) and r1 (next byte);
+        // MXFP4: the slot's 16 scale bytes a row cover this stage and its pair
+        // (stage kc & 1 of them), block 2 sb + q / 2 of the stage
+        uint32_t sc;
+        if (mx) {
+            const int w = 2 * (kc & 1) + (sb >> 1), bsel = 2 * (sb & 1) + (q >> 1);
+            const uint32_t two = __byte_perm(sw0[w], sw1[w], (uint32_t)bsel | ((uint32_t)(4 + bsel) << 4));
+            bool b = false;
+            sc = e8m0_f16_bits(two & 0xFFu, b) | (e8m0_f16_bits((two >> 8) & 0xFFu, b) << 16);
+            if (b) *bad = true;
+        } else {
+            sc = e4m3x2_to_f16x2(__byte_perm(sw0[sb], sw1[sb], ssel));
+        }
         __half2 sc0 = __low2half2(*reinterpret_cast<const __half2 *>(&sc));
         __half2 sc1 = __high2half2(*reinterpret_cast<const __half2 *>(&sc));
         uint32_t h0[8], h1[8];
@@ -1308,13 +1330,13 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             }
             const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * a.rbslot;
             if (res) {
-                reg_stage<1, true>(st, xrow, op, rg, lane, acc, kc, xsw);
+                reg_stage<1, true>(st, xrow, op, rg, lane, acc, kc, xsw, a.mx, &range_bad);
             } else {
                 switch (nt_n) {
-                    case 1: reg_stage<1>(st, bst, op, rg, lane, acc); break;
-                    case 2: reg_stage<2>(st, bst, op, rg, lane, acc); break;
-                    case 3: reg_stage<3>(st, bst, op, rg, lane, acc); break;
-                    default: reg_stage<4>(st, bst, op, rg, lane, acc); break;
+                    case 1: reg_stage<1>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
+                    case 2: reg_stage<2>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
+                    case 3: reg_stage<3>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
+                    default: reg_stage<4>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
                 }
             }
             __syncwarp();
@@ -1579,8 +1601,9 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                     mbar_expect_tx(cfull + c.s, kHCodeStage);
                     tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
                     tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
-                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, kc * 16, r0);
-                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, kc * 16, r1);
+                    const int sx = a.mx ? (kc >> 1) * 16 : kc * 16;   // MXFP4: the stage pair's 16 scale bytes
+                    tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, sx, r0);
+                    tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, sx, r1);
                     used |= 1u << c.s;
                     last_ph = (last_ph & ~(1u << c.s)) | (c.ph << c.s);
                     c.next(a.rcst);
@@ -1782,6 +1805,8 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     a.tail_split = (p.tail_part && p.tail_tickets) ? 1 : 0;
     a.tickets = p.tail_tickets;
     a.tail_part = p.tail_part;
+    a.mx = c.weight_format == MOE_WEIGHTS_MXFP4 ? 1 : 0;
+    const int sbk = a.mx ? 32 : 16;   // K values a scale byte covers
     const RegRings rr = T <= 16 ? kRegSmall : kRegLarge;   // T <= 16: every tile has at most 16 rows
     a.rcst = rr.cst;
     a.rbst = rr.bst;
@@ -1802,12 +1827,12 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         }
         ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
         ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
-        ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
-        ok &= make_map(&a.s1[0], r.us, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.s0[0], r.gs, H / sbk, (uint64_t)E * I, H / sbk, 16, 128, false);
+        ok &= make_map(&a.s1[0], r.us, H / sbk, (uint64_t)E * I, H / sbk, 16, 128, false);
         ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
-        ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
-        ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
+        ok &= make_map(&a.s0[1], sp.gs, H / sbk, Is_, H / sbk, 16, 128, false);
+        ok &= make_map(&a.s1[1], sp.us, H / sbk, Is_, H / sbk, 16, 128, false);
         for (int k2 = 0; k2 < 3; ++k2)
             ok &= make_map(&a.b[k2], p.xp16, H, p.rows_pad_max, (uint64_t)H * 2, 64, 16u << k2, true, true);
         a.nf = Imax / 128;
@@ -1825,9 +1850,9 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         return cudaGetLastError();
     }
     ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
-    ok &= make_map(&a.s0[0], r.ds, I / 16, (uint64_t)E * H, I / 16, 16, 128, false);
+    ok &= make_map(&a.s0[0], r.ds, I / sbk, (uint64_t)E * H, I / sbk, 16, 128, false);
     ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 128, 128, true);
-    ok &= make_map(&a.s0[1], sp.ds, Is_ / 16, H, Is_ / 16, 16, 128, false);
+    ok &= make_map(&a.s0[1], sp.ds, Is_ / sbk, H, Is_ / sbk, 16, 128, false);
     a.a1[0] = a.a0[0];
     a.a1[1] = a.a0[1];
     a.s1[0] = a.s0[0];

@@ -86,6 +86,7 @@ struct Plan {
     int32_t *tail_tickets = nullptr;   // [8 * num_sms] arrivals per split gate/up item and row group (per-call scratch)
     float *tail_part = nullptr;        // [num_sms][8192] partial gate/up sums of split items (W4A16 warp MMAs)
     int *err = nullptr;             // device error word
+    float *ones = nullptr;          // [E + 1] 1.0f: the tensor scales of MXFP4 weights, which have none
     void *x_stage = nullptr;        // [Tmax][H] bf16 (moe_forward_host)
     void *out_stage = nullptr;      // [Tmax][H] bf16
 };
@@ -163,6 +164,36 @@ __device__ __forceinline__ void quant_block16(const float (&v)[16], float ts, ui
     codes.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
     codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
     scale = s;
+}
+
+// MXFP4 (OCP MX) conversion of one 32-value block: E8M0 scale byte
+// s = clamp(floor(log2(amax)) - 2 + 127, 0, 254) (0 for an all-zero block),
+// codes = E2M1_rne_sat(v * 2^(127 - s)), a multiplication by a power of two
+// that is exact.  For a normal amax floor(log2(amax)) + 127 is its biased
+// exponent field, so s = max(field - 2, 0); a subnormal amax gives s = 0.
+__device__ __forceinline__ void quant_block32_mx(const float (&v)[32], uint4 &codes, uint32_t &scale) {
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int field = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+    const int s = field > 2 ? field - 2 : 0;
+    const float inv = __uint_as_float((uint32_t)(254 - s) << 23);   // 2^(127 - s), s <= 252
+    uint32_t b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = f32x2_to_e2m1x2(__fmul_rn(v[2 * i], inv), __fmul_rn(v[2 * i + 1], inv));
+    codes.x = b[0] | (b[1] << 8) | (b[2] << 16) | (b[3] << 24);
+    codes.y = b[4] | (b[5] << 8) | (b[6] << 16) | (b[7] << 24);
+    codes.z = b[8] | (b[9] << 8) | (b[10] << 16) | (b[11] << 24);
+    codes.w = b[12] | (b[13] << 8) | (b[14] << 16) | (b[15] << 24);
+    scale = (uint32_t)s;
+}
+
+// E8M0 byte -> fp32 2^(byte - 127) (byte 0: the subnormal 2^-127; 255: NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t byte) {
+    byte &= 0xFFu;
+    if (byte == 0) return __uint_as_float(0x00400000u);
+    if (byte == 255) return __uint_as_float(0x7FC00000u);
+    return __uint_as_float(byte << 23);
 }
 
 __device__ __forceinline__ void atomic_max_nonneg(unsigned int *addr, float v) {
@@ -282,6 +313,8 @@ cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes
                              float *ts_out, bool amax_ready, cudaStream_t st);
 cudaError_t launch_quant_nvfp4(const float *w, int batch, int rows, int cols, uint8_t *codes, uint8_t *scales,
                                float *ts, cudaStream_t st);
+cudaError_t launch_quant_mxfp4(const float *w, int64_t rows, int cols, uint8_t *codes, uint8_t *scales,
+                               cudaStream_t st);
 // part 0: gate + up + SwiGLU; part 1: down + routing weight + scatter-add.
 cudaError_t launch_ffn_simt(const Plan &p, const void *x, int T, const ExpertPtrs &routed,
                             const ExpertPtrs *shared, int part, cudaStream_t st);

@@ -108,6 +108,83 @@ __global__ void __launch_bounds__(kThreads) k_quant_act(const uint16_t *__restri
     }
 }
 
+// MXFP4 weights: one thread per 32-value block of fp32 rows (any number of rows).
+__global__ void __launch_bounds__(kThreads) k_quant_mx_f32(const float *__restrict__ w, int64_t nblocks,
+                                                          uint4 *__restrict__ codes, uint8_t *__restrict__ scales) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblocks; i += (int64_t)gridDim.x * blockDim.x) {
+        const float4 *p = reinterpret_cast<const float4 *>(w + i * 32);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 q = p[j];
+            v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+        }
+        uint4 c;
+        uint32_t s;
+        quant_block32_mx(v, c, s);
+        codes[i] = c;
+        scales[i] = (uint8_t)s;
+    }
+}
+
+// MXFP4 activations (W4A4 with MXFP4 weights): one thread per 32-value block of
+// bf16 x; no tensor scale (ts_out, when given, receives 1).
+__global__ void __launch_bounds__(kThreads) k_quant_act_mx(const uint16_t *__restrict__ x, int64_t nblocks,
+                                                          uint4 *__restrict__ codes, uint8_t *__restrict__ scales,
+                                                          float *ts_out) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && ts_out) *ts_out = 1.0f;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < nblocks; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(x + i * 32);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 q = p[j];
+            const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * j + 2 * h] = __uint_as_float(u[h] << 16);
+                v[8 * j + 2 * h + 1] = __uint_as_float(u[h] & 0xFFFF0000u);
+            }
+        }
+        uint4 c;
+        uint32_t s;
+        quant_block32_mx(v, c, s);
+        codes[i] = c;
+        scales[i] = (uint8_t)s;
+    }
+}
+
+// MXFP4 SwiGLU output (W4A4 with MXFP4 weights, CUDA-core engine): fp32 h rows
+// -> codes [row][stride/2], scales [row][stride/32]; every block on its own,
+// no tensor scale (hts receives 1, 1).
+__global__ void __launch_bounds__(kThreads) k_quant_h_mx(const float *__restrict__ h, int stride,
+                                                        const int32_t *__restrict__ poff, int E, int I, int Is,
+                                                        const int32_t *__restrict__ pad_pair, uint4 *__restrict__ codes,
+                                                        uint8_t *__restrict__ scales, float *hts) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) { hts[0] = 1.0f; hts[1] = 1.0f; }
+    const int shared_row0 = poff[E];
+    const int rows = poff[E + 1];
+    const int bpr = stride / 32;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < (int64_t)rows * bpr;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int row = (int)(i / bpr), blk = (int)(i % bpr);
+        if (pad_pair[row] < 0) continue;
+        if (blk >= (row >= shared_row0 ? Is : I) / 32) continue;
+        const float4 *p = reinterpret_cast<const float4 *>(h + (int64_t)row * stride + blk * 32);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 q = p[j];
+            v[4 * j] = q.x; v[4 * j + 1] = q.y; v[4 * j + 2] = q.z; v[4 * j + 3] = q.w;
+        }
+        uint4 c;
+        uint32_t s;
+        quant_block32_mx(v, c, s);
+        codes[(int64_t)row * (stride / 32) + blk] = c;
+        scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+    }
+}
+
 // W4A4 SwiGLU output: fp32 h rows (padded layout, row stride `stride` values)
 // -> NVFP4 codes [row][stride/2] and scales [row][stride/16].  Rows of the
 // routed segment use the routed amax, rows of the shared segment the shared one.
@@ -210,6 +287,12 @@ int device_sms() {
 cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes, uint8_t *scales, float *ts_out,
                              bool amax_ready, cudaStream_t st) {
     const int64_t n = (int64_t)T * p.cfg.hidden;
+    if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4) {
+        k_quant_act_mx<<<grid_for(n / 32, p.num_sms), kThreads, 0, st>>>(static_cast<const uint16_t *>(x), n / 32,
+                                                                         reinterpret_cast<uint4 *>(codes), scales,
+                                                                         ts_out);
+        return cudaGetLastError();
+    }
     if (!amax_ready) {
         k_amax_bf16<<<grid_for(n / 8, p.num_sms), kThreads, 0, st>>>(static_cast<const uint4 *>(x), n / 8,
                                                                      &p.scratch->x_amax);
@@ -222,10 +305,23 @@ cudaError_t launch_quant_act(const Plan &p, const void *x, int T, uint8_t *codes
 
 cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st) {
     const int Imax = p.cfg.has_shared ? max(p.cfg.inter, p.cfg.shared_inter) : p.cfg.inter;
+    if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4) {
+        k_quant_h_mx<<<p.num_sms * 8, kThreads, 0, st>>>(p.hbuf, Imax, p.poff, p.cfg.num_experts, p.cfg.inter,
+                                                         p.cfg.shared_inter, p.pad_pair, reinterpret_cast<uint4 *>(p.hq),
+                                                         p.hsc, p.hts);
+        return cudaGetLastError();
+    }
     k_quant_h<<<p.num_sms * 8, kThreads, 0, st>>>(p.hbuf, Imax, p.poff, p.cfg.num_experts, p.cfg.inter,
                                                   p.cfg.shared_inter, p.pad_pair, p.scratch,
                                                   reinterpret_cast<uint2 *>(p.hq), p.hsc,
                                                   tc_layout ? p.hq_atoms : nullptr, p.hts);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mxfp4(const float *w, int64_t rows, int cols, uint8_t *codes, uint8_t *scales,
+                               cudaStream_t st) {
+    const int64_t nb = rows * (cols / 32);
+    k_quant_mx_f32<<<grid_for(nb, device_sms()), kThreads, 0, st>>>(w, nb, reinterpret_cast<uint4 *>(codes), scales);
     return cudaGetLastError();
 }
 

@@ -40,12 +40,14 @@ def atoms_to_plain(atoms: np.ndarray, rows: int, blocks: int) -> np.ndarray:
     return atoms[idx]
 
 
-def gpu_h_state(plan, w, offsets, tc: bool):
+def gpu_h_state(plan, w, offsets, tc: bool, mx: bool = False):
     """The GPU's SwiGLU stage after a forward: per routed expert its fp32 h rows
-    (grouped order), codes and plain scales; the shared expert's; both tensor scales."""
+    (grouped order), codes and plain scales; the shared expert's; both tensor
+    scales.  mx: MXFP4 (one scale byte a 32-value block)."""
     E, T = w.experts, w.tokens
     I, Is = w.inter, w.shared_inter
     Imax = max(I, Is)
+    bk = 32 if mx else 16
     poff = _view(plan, "padded_offsets", torch.int32)
     rows = int(poff[E + 1])
     h = _view(plan, "h", torch.float32)[:rows * Imax].reshape(rows, Imax)
@@ -54,7 +56,7 @@ def gpu_h_state(plan, w, offsets, tc: bool):
         atoms = _view(plan, "h_scale_atoms", torch.uint8)
         scales = atoms_to_plain(atoms, rows, Imax // 16)
     else:
-        scales = _view(plan, "h_scales", torch.uint8)[:rows * Imax // 16].reshape(rows, Imax // 16)
+        scales = _view(plan, "h_scales", torch.uint8)[:rows * Imax // bk].reshape(rows, Imax // bk)
     ts = _view(plan, "h_ts", torch.float32)[:2]
     st = dict(h={}, codes={}, scales={}, ts=float(ts[0]), shared_ts=float(ts[1]))
     for e in range(E):
@@ -63,12 +65,12 @@ def gpu_h_state(plan, w, offsets, tc: bool):
             r0 = int(poff[e])
             st["h"][e] = h[r0:r0 + n, :I].copy()
             st["codes"][e] = codes[r0:r0 + n, :I // 2].copy()
-            st["scales"][e] = scales[r0:r0 + n, :I // 16].copy()
+            st["scales"][e] = scales[r0:r0 + n, :I // bk].copy()
     if Is:
         r0 = int(poff[E])
         st["h"]["shared"] = h[r0:r0 + T, :Is].copy()
         st["codes"]["shared"] = codes[r0:r0 + T, :Is // 2].copy()
-        st["scales"]["shared"] = scales[r0:r0 + T, :Is // 16].copy()
+        st["scales"]["shared"] = scales[r0:r0 + T, :Is // bk].copy()
     return st
 
 
