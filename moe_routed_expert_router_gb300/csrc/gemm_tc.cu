@@ -605,7 +605,7 @@ struct HcArgs {
     int rcst, rbst, rbslot;
     const uint16_t *x;
     int xres;               // gate/up: tokens whose activations sit resident in shared memory (0: token-row ring)
-    int mx;                 // MXFP4 weights: E8M0 scales, one 16-byte scale box a row for a pair of stages
+    int mx;                 // MXFP4 weights (selects the k_gemm_reg instantiation)
     // split last round (warp-MMA engine): arrival tickets and partial sums
     int tail_split;
     int *tickets;
@@ -1084,9 +1084,9 @@ __device__ __forceinline__ uint32_t e8m0_f16_bits(uint32_t e, bool &bad) {
     return 0;
 }
 
-template <int NT, bool RES = false>
+template <int NT, bool RES = false, int MX = 0>
 __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int rg, int lane, float (&acc)[4][4],
-                                          int kc = 0, uint32_t xsw = 0, int mx = 0, bool *bad = nullptr) {
+                                          int kc = 0, uint32_t xsw = 0, bool *bad = nullptr) {
     const int g = lane >> 2, q = lane & 3;
     const int r0 = rg * 16 + g, r1 = r0 + 8;
     const uint32_t crow0 = st + op * kHCodeTile + r0 * 128, crow1 = st + op * kHCodeTile + r1 * 128;
@@ -1104,7 +1104,7 @@ __device__ __forceinline__ void reg_stage(uint32_t st, uint32_t bst, int op, int
         // MXFP4: the slot's 16 scale bytes a row cover this stage and its pair
         // (stage kc & 1 of them), block 2 sb + q / 2 of the stage
         uint32_t sc;
-        if (mx) {
+        if (MX) {
             const int w = 2 * (kc & 1) + (sb >> 1), bsel = 2 * (sb & 1) + (q >> 1);
             const uint32_t two = __byte_perm(sw0[w], sw1[w], (uint32_t)bsel | ((uint32_t)(4 + bsel) << 4));
             bool b = false;
@@ -1212,7 +1212,7 @@ __device__ __forceinline__ int reg_fill_meta(const HcArgs &a, const RegSplit &rs
 }
 
 // Compute warps of k_gemm_reg (warps 2..17).
-template <int EPI>
+template <int EPI, int MX>
 __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane, uint8_t *code_ring, uint8_t *b_ring,
                                             float *xchg, uint64_t *cfull, uint64_t *cempty, uint64_t *bfull,
                                             uint64_t *bempty, uint64_t *xfull, uint64_t *xempty,
@@ -1330,13 +1330,13 @@ __device__ __forceinline__ void reg_compute(const HcArgs &a, int warp, int lane,
             }
             const uint32_t st = ring0 + cs.s * kHCodeStage, bst = bring0 + bs.s * a.rbslot;
             if (res) {
-                reg_stage<1, true>(st, xrow, op, rg, lane, acc, kc, xsw, a.mx, &range_bad);
+                reg_stage<1, true, MX>(st, xrow, op, rg, lane, acc, kc, xsw, &range_bad);
             } else {
                 switch (nt_n) {
-                    case 1: reg_stage<1>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
-                    case 2: reg_stage<2>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
-                    case 3: reg_stage<3>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
-                    default: reg_stage<4>(st, bst, op, rg, lane, acc, kc, 0, a.mx, &range_bad); break;
+                    case 1: reg_stage<1, false, MX>(st, bst, op, rg, lane, acc, kc, 0, &range_bad); break;
+                    case 2: reg_stage<2, false, MX>(st, bst, op, rg, lane, acc, kc, 0, &range_bad); break;
+                    case 3: reg_stage<3, false, MX>(st, bst, op, rg, lane, acc, kc, 0, &range_bad); break;
+                    default: reg_stage<4, false, MX>(st, bst, op, rg, lane, acc, kc, 0, &range_bad); break;
                 }
             }
             __syncwarp();
@@ -1536,7 +1536,8 @@ __device__ __forceinline__ void reg_gather(const HcArgs &a, int lane, uint8_t *b
     }
 }
 
-template <int EPI>
+// MX: MXFP4 weights (E8M0 scales, a 16-byte scale box a row for a pair of stages).
+template <int EPI, int MX>
 __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant__ HcArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1601,7 +1602,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                     mbar_expect_tx(cfull + c.s, kHCodeStage);
                     tma_2d(st, &a.a0[m], cfull + c.s, kc * 128, r0);
                     tma_2d(st + kHCodeTile, A1, cfull + c.s, kc * 128, r1);
-                    const int sx = a.mx ? (kc >> 1) * 16 : kc * 16;   // MXFP4: the stage pair's 16 scale bytes
+                    const int sx = MX ? (kc >> 1) * 16 : kc * 16;   // MXFP4: the stage pair's 16 scale bytes
                     tma_2d(st + 2 * kHCodeTile, &a.s0[m], cfull + c.s, sx, r0);
                     tma_2d(st + 2 * kHCodeTile + 2048, S1, cfull + c.s, sx, r1);
                     used |= 1u << c.s;
@@ -1646,7 +1647,7 @@ __global__ void __launch_bounds__(kRThreads, 1) k_gemm_reg(const __grid_constant
                 if (used & (1u << t)) mbar_wait(bfull + t, (last_ph >> t) & 1u, a.err);
         }
     } else {
-        reg_compute<EPI>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty, meta,
+        reg_compute<EPI, MX>(a, warp, lane, code_ring, b_ring, xchg, cfull, cempty, bfull, bempty, xfull, xempty, meta,
                          meta_ready, x_full);
     }
 }
@@ -1765,9 +1766,13 @@ cudaError_t configure_tc(const Plan &) {
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_gemm_f16<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_gemm_reg<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
+        e = cudaFuncSetAttribute(k_gemm_reg<kSwiGLU, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_gemm_reg<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
+        e = cudaFuncSetAttribute(k_gemm_reg<kSwiGLU, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_reg<kScatter, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_reg<kScatter, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmemBytes);
     return e;
 }
 
@@ -1843,7 +1848,8 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
         if (!ok) return cudaErrorInvalidValue;
         cudaError_t e0;
         if (warp_mma)
-            e0 = launch_pdl(k_gemm_reg<kSwiGLU>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
+            e0 = a.mx ? launch_pdl(k_gemm_reg<kSwiGLU, 1>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a)
+                      : launch_pdl(k_gemm_reg<kSwiGLU, 0>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
         else
             e0 = launch_pdl(k_gemm_f16<kSwiGLU>, dim3(p.num_sms), dim3(kHThreads), kHSmemBytes, st, a);
         if (e0 != cudaSuccess) return e0;
@@ -1867,7 +1873,8 @@ cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertP
     if (!ok) return cudaErrorInvalidValue;
     cudaError_t e0;
     if (warp_mma)
-        e0 = launch_pdl(k_gemm_reg<kScatter>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
+        e0 = a.mx ? launch_pdl(k_gemm_reg<kScatter, 1>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a)
+                  : launch_pdl(k_gemm_reg<kScatter, 0>, dim3(p.num_sms), dim3(kRThreads), rsmem, st, a);
     else
         e0 = launch_pdl(k_gemm_f16<kScatter>, dim3(p.num_sms), dim3(kHThreads), kHSmemBytes, st, a);
     if (e0 != cudaSuccess) return e0;
