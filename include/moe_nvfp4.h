@@ -89,10 +89,11 @@ typedef enum { MOE_ROUTER_F32 = 0, MOE_ROUTER_BF16 = 1 } moe_router_dtype;
  *          E8M0 scale (#521).  In W4A4 the activations and the SwiGLU output
  *          are then MXFP4 as well (every block on its own scale, no batch
  *          amax).  MXFP4 plans need H, I (and the shared I) multiples of 512;
- *          they run on the CUDA cores, and W4A16 also on the warp MMAs (whose
- *          f16 operands hold code x scale exactly only for block scales from
- *          2^-23 to 2^13: a weight block outside that range is a device error
- *          there). */
+ *          they run on the CUDA cores, W4A4 also on the tcgen05 block-scaled
+ *          MMAs (kind::mxf4, E8M0 scales), and W4A16 also on the warp MMAs
+ *          (whose f16 operands hold code x scale exactly only for block scales
+ *          from 2^-23 to 2^13: a weight block outside that range is a device
+ *          error there). */
 typedef enum { MOE_WEIGHTS_NVFP4 = 0, MOE_WEIGHTS_MXFP4 = 1 } moe_weight_format;
 
 /* W4A16: activations stay bf16; the SwiGLU output is rounded to bf16 (RNE)
@@ -238,7 +239,8 @@ moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, si
  * of up to 32 token rows.  AUTO picks WARP_MMA for W4A16 batches with fewer
  * than 2 (token, expert) pairs an expert on average (decode), the tcgen05
  * GEMMs for larger W4A16 batches and for W4A4 batches of 64 or more pairs,
- * and CUDA_CORE otherwise; the tensor paths need H and I multiples of 256.  All compute the
+ * and CUDA_CORE otherwise; the tensor paths need H and I multiples of 256.
+ * MXFP4 W4A16 plans take no TENSOR_CORE (AUTO: WARP_MMA).  All compute the
  * same function (the tolerance of the parity tests covers their different
  * summation orders). */
 typedef enum { MOE_PATH_AUTO = 0, MOE_PATH_CUDA_CORE = 1, MOE_PATH_TENSOR_CORE = 2, MOE_PATH_WARP_MMA = 3 } moe_path;

@@ -191,7 +191,7 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const void *r
     if (plan->path == MOE_PATH_AUTO) {
         wm = moe::warp_mma_supported(p) && T * p.cfg.top_k < 2 * p.cfg.num_experts;
         tc = wm || (moe::tc_supported(p) && (p.cfg.mode == MOE_W4A16 || T * p.cfg.top_k >= 64));
-        if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4) {   // the warp MMAs (W4A16) or the CUDA cores
+        if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4 && p.cfg.mode == MOE_W4A16) {   // warp MMAs or CUDA cores
             wm = moe::warp_mma_supported(p);
             tc = wm;
         }
@@ -312,8 +312,11 @@ moe_status moe_plan_create(const moe_config *cfg, moe_plan *out) {
 
 moe_status moe_plan_set_path(moe_plan plan, int32_t path) {
     if (!plan || path < MOE_PATH_AUTO || path > MOE_PATH_WARP_MMA) return MOE_ERR_INVALID_ARG;
+    // MXFP4 takes the tcgen05 GEMMs for W4A4 only (kind::mxf4); its W4A16 runs on
+    // the warp MMAs or the CUDA cores
     if (path == MOE_PATH_TENSOR_CORE &&
-        (!moe::tc_supported(plan->p) || plan->p.cfg.weight_format == MOE_WEIGHTS_MXFP4))
+        (!moe::tc_supported(plan->p) ||
+         (plan->p.cfg.weight_format == MOE_WEIGHTS_MXFP4 && plan->p.cfg.mode == MOE_W4A16)))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_WARP_MMA && !moe::warp_mma_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     plan->path = path;

@@ -97,7 +97,7 @@ struct TcArgs {
     int P, k;
     float *acc;             // G2 output [T][H]
     int *err;
-    int colfirst;           // down items column group first (large T; see decode_item)
+    int colfirst;           // down items: column groups a chunk (large T; 0: tile by tile; see decode_item)
 };
 
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
@@ -133,6 +133,36 @@ __device__ __forceinline__ void mma_fp4(uint32_t d, uint64_t a, uint64_t b, uint
         "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
         ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
         : "memory");
+}
+
+// MXFP4 (kind::mxf4, UE8M0 scales, one a 32-value block): a K = 64 MMA takes
+// two scale bytes a row.  A 32-bit scale cell of tensor memory holds four
+// (K = 128, two MMAs); the descriptor's scale-factor ids (A: bits 29-30, B:
+// bits 4-5) pick bytes 0-1 (id 0) or 2-3 (id 2) of the cell.
+__device__ __forceinline__ uint32_t idesc_mx4(uint32_t n, int kk) {
+    const uint32_t id = 2u * (uint32_t)(kk & 1);
+    return idesc_fp4(n) | (1u << 23) | (id << 29) | (id << 4);
+}
+
+__device__ __forceinline__ void mma_mx4(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa, uint32_t sfb,
+                                        uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+        : "memory");
+}
+
+// One block-scaled FP4 MMA of K chunk kk: NVFP4 (cell = four 16-value blocks =
+// one K chunk) or MXFP4 (cell = four 32-value blocks = two K chunks).
+// sfa0 / sfb0: the stage's first scale column of the A / B operand.
+template <int MX>
+__device__ __forceinline__ void mma_blk(uint32_t d, uint64_t a, uint64_t b, uint32_t n, int kk, uint32_t sfa0,
+                                        uint32_t sfb0, uint32_t acc) {
+    if (MX)
+        mma_mx4(d, a, b, idesc_mx4(n, kk), sfa0 + 4 * (kk >> 1), sfb0 + 4 * (kk >> 1), acc);
+    else
+        mma_fp4(d, a, b, idesc_fp4(n), sfa0 + 4 * kk, sfb0 + 4 * kk, acc);
 }
 
 // Token rows a tile loads and multiplies: 32, 64 or 128 (index into TcArgs::b).
@@ -177,15 +207,28 @@ struct Item {
 };
 
 // Items run tile by tile (one tile's token rows against every weight group).
-// For many tokens the down items run column group by column group instead, so
-// the scatter-add into the fp32 accumulator touches a [T][256] slice of it at
-// a time and the slice stays in L2 (for few tokens that order would make the
-// CTAs running at the same time add into the same few addresses).
+// For many tokens the down items run in chunks of C = colfirst column groups
+// instead, tile by tile within a chunk: the scatter-add into the fp32
+// accumulator then touches a [T][256 C] slice of it at a time, which stays in
+// L2, and the token rows of a tile are read once a chunk (C = 1 would read
+// every tile's SwiGLU codes once per 256 output columns).  For few tokens the
+// chunked order would make the CTAs running at the same time add into the same
+// few addresses.
 __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, Item &it) {
     const int nt = a.scratch->n_tiles;
-    const bool cf = epi == kScatter && a.colfirst;
-    const int4 t = a.tiles[cf ? item % nt : item / a.nf];
-    it.f = cf ? item / nt : item % a.nf;
+    int tile;
+    if (epi == kScatter && a.colfirst) {
+        const int C = a.colfirst;
+        const int q = item / (nt * C);             // chunk
+        const int cq = min(C, a.nf - q * C);       // its column groups (the last may be short)
+        const int rem = item - q * nt * C;
+        tile = rem / cq;
+        it.f = q * C + (rem - tile * cq);
+    } else {
+        tile = item / a.nf;
+        it.f = item % a.nf;
+    }
+    const int4 t = a.tiles[tile];
     it.e = t.x;
     it.row0 = t.y;
     it.valid = t.z;
@@ -199,7 +242,10 @@ __device__ __forceinline__ bool decode_item(const TcArgs &a, int item, int epi, 
     return true;
 }
 
-template <int EPI>
+// MX: MXFP4 operands (weights and token rows): E8M0 scales, a cell of four
+// 32-value blocks, so a 256-value stage has two scale cells an operand; the
+// weights' 16-byte scale box a row covers a pair of stages.
+template <int EPI, int MX>
 __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_constant__ TcArgs a) {
     constexpr int kMmaWarps = mma_warps(EPI), kScaleWarps = scale_warps(EPI), kEpiWarp0 = epi_warp0(EPI);
     pdl_wait();      // routing, permute or gate/up results come from the previous kernel
@@ -261,16 +307,18 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                 const uint32_t b_bytes = (32u << rc) * kRowBytes;
                 const uint8_t *batoms = a.b_atoms + (size_t)(it.row0 / 128) * a.b_atoms_per_block * 512;
                 const int ks_n = it.K / kBK;
+                constexpr uint32_t kBSf = MX ? kSf / 2 : kSf;   // token-row scale atoms a stage
                 for (int ks = 0; ks < ks_n; ++ks) {
                     if (!mbar_wait(empty + s, ph ^ 1, a.err)) { ok = false; break; }
                     uint8_t *st = smem + s * kStageBytes;
-                    mbar_expect_tx(full + s, 2 * kTile + b_bytes + 3 * kSf);
+                    mbar_expect_tx(full + s, 2 * kTile + b_bytes + 2 * kSf + kBSf);
                     tma_2d(st, &a.a0[m], full + s, ks * kRowBytes, r0);
                     tma_2d(st + kTile, A1, full + s, ks * kRowBytes, r1);
                     tma_2d(st + 2 * kTile, &a.b[rc], full + s, ks * kRowBytes, it.row0);
-                    tma_2d(st + 3 * kTile, &a.s0[m], full + s, ks * 16, r0);
-                    tma_2d(st + 3 * kTile + kSf, S1, full + s, ks * 16, r1);
-                    bulk_copy(st + 3 * kTile + 2 * kSf, batoms + (size_t)ks * 4 * 512, kSf, full + s);
+                    const int sx = MX ? (ks >> 1) * 16 : ks * 16;
+                    tma_2d(st + 3 * kTile, &a.s0[m], full + s, sx, r0);
+                    tma_2d(st + 3 * kTile + kSf, S1, full + s, sx, r1);
+                    bulk_copy(st + 3 * kTile + 2 * kSf, batoms + (size_t)ks * kBSf, kBSf, full + s);
                     used |= 1u << s;
                     last_ph = (last_ph & ~(1u << s)) | (ph << s);
                     if (++s == kStages) { s = 0; ph ^= 1; }
@@ -295,7 +343,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                 if (!mbar_wait(acc_empty, aph ^ 1, a.err)) break;
                 aph ^= 1;
                 tc_fence_after();
-                const uint32_t idesc = idesc_fp4(32u << rows_class(it.valid));
+                const uint32_t nrows = 32u << rows_class(it.valid);
                 const int ks_n = it.K / kBK;
                 for (int ks = 0; ks < ks_n; ++ks) {
                     if (!mbar_wait(sf_ready + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
@@ -312,9 +360,9 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                         const uint64_t dS = desc_sf(base + 3 * kTile);
                         for (int h = h0; h < h0 + nh; ++h) {
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                sf_copy(sf + 16 * h + 4 * kk, dS + h * (kSf >> 4) + 32 * kk);
-                                sf_copy(sf + 32 + 16 * h + 4 * kk, dS + (2 * kSf >> 4) + 32 * kk);
+                            for (int c = 0; c < (MX ? 2 : 4); ++c) {   // the stage's scale cells
+                                sf_copy(sf + 16 * h + 4 * c, dS + h * (kSf >> 4) + 32 * c);
+                                sf_copy(sf + 32 + 16 * h + 4 * c, dS + (2 * kSf >> 4) + 32 * c);
                             }
                         }
                     }
@@ -322,12 +370,12 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t accum = (ks | kk) ? 1u : 0u;
                         if (kMmaWarps == 1) {
-                            mma_fp4(tmem, dA + 2 * kk, dB + 2 * kk, idesc, sf + 4 * kk, sf + 32 + 4 * kk, accum);
-                            mma_fp4(tmem + 128, dA + (kTile >> 4) + 2 * kk, dB + 2 * kk, idesc, sf + 16 + 4 * kk,
-                                    sf + 32 + 4 * kk, accum);
+                            mma_blk<MX>(tmem, dA + 2 * kk, dB + 2 * kk, nrows, kk, sf, sf + 32, accum);
+                            mma_blk<MX>(tmem + 128, dA + (kTile >> 4) + 2 * kk, dB + 2 * kk, nrows, kk, sf + 16,
+                                        sf + 32, accum);
                         } else {
-                            mma_fp4(tmem + 128 * h0, dA + h0 * (kTile >> 4) + 2 * kk, dB + 2 * kk, idesc,
-                                    sf + 16 * h0 + 4 * kk, sf + 32 + 16 * h0 + 4 * kk, accum);
+                            mma_blk<MX>(tmem + 128 * h0, dA + h0 * (kTile >> 4) + 2 * kk, dB + 2 * kk, nrows, kk,
+                                        sf + 16 * h0, sf + 32 + 16 * h0, accum);
                         }
                     }
                     mma_commit(empty + s);
@@ -363,10 +411,20 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
 #pragma unroll
                     for (int q = 0; q < 4; ++q) v[q] = lds128(tile + 16 * (lane + 32 * q));
                     __syncwarp();
-                    sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
-                    sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
-                    sts128(tile + 16 * (2 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
-                    sts128(tile + 16 * (3 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
+                    if (MX) {   // this stage's two cells: words 2 (ks & 1) and 2 (ks & 1) + 1 of a row
+                        if (ks & 1) {
+                            sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
+                            sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
+                        } else {
+                            sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
+                            sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
+                        }
+                    } else {
+                        sts128(tile + 16 * (0 * 32 + lane), make_uint4(v[0].x, v[1].x, v[2].x, v[3].x));
+                        sts128(tile + 16 * (1 * 32 + lane), make_uint4(v[0].y, v[1].y, v[2].y, v[3].y));
+                        sts128(tile + 16 * (2 * 32 + lane), make_uint4(v[0].z, v[1].z, v[2].z, v[3].z));
+                        sts128(tile + 16 * (3 * 32 + lane), make_uint4(v[0].w, v[1].w, v[2].w, v[3].w));
+                    }
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
@@ -408,19 +466,25 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
 #pragma unroll
                 for (int op = 0; op < 2; ++op) {
                     const uint4 v = lds128(sfb + op * kSf + 16 * (lane + 32 * quad));
+                    // NVFP4: cells 0-3 are words x, y, z, w; MXFP4: the row's 16 bytes
+                    // cover a pair of stages, this stage's two cells are words
+                    // 2 (ks & 1) and 2 (ks & 1) + 1 (cells 2, 3 unused)
+                    const uint32_t c0 = (MX && (ks & 1)) ? v.z : v.x, c1 = (MX && (ks & 1)) ? v.w : v.y;
+                    const uint32_t c2 = MX ? 0u : v.z, c3 = MX ? 0u : v.w;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
-                        o[j] = v.x;
-                        o[4 + j] = v.y;
-                        o[8 + j] = v.z;
-                        o[12 + j] = v.w;
+                        o[j] = c0;
+                        o[4 + j] = c1;
+                        o[8 + j] = c2;
+                        o[12 + j] = c3;
                     }
                     tmem_st16(t_lane + s * sf_stride(EPI) + 16 * op, o);
                 }
                 {
                     uint4 v[4];
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) v[kk] = lds128(sfb + 2 * kSf + 512 * kk + 16 * lane);
+                    for (int kk = 0; kk < 4; ++kk)
+                        v[kk] = (MX && kk >= 2) ? make_uint4(0u, 0u, 0u, 0u) : lds128(sfb + 2 * kSf + 512 * kk + 16 * lane);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         o[4 * kk] = v[kk].x;
@@ -472,7 +536,8 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
             if (lane == 0) mbar_arrive(acc_empty);
             if (col0 >= n_end) continue;
             if (EPI == kSwiGLU) {
-                const float xts = __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
+                // activation tensor scale (MXFP4 activations have none)
+                const float xts = MX ? 1.0f : __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
                 const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
                 const int feat = it.f * 128 + quad * 32 + lane;
                 float mx = 0.0f;
@@ -1684,15 +1749,17 @@ __global__ void __launch_bounds__(256) k_permute_f16(const uint16_t *__restrict_
 // Gather x's NVFP4 codes into the padded per-expert rows and its scales into
 // the tensor-core scale layout (512-byte atoms of 128 rows x 4 scale bytes:
 // byte (r % 32) * 16 + (r / 32 % 4) * 4 + j of atom (r / 128, c)).
+// sbk: K values a scale byte covers (16 NVFP4, 32 MXFP4); a scale word (one
+// tensor-core scale cell) holds four consecutive scale bytes.
 __global__ void __launch_bounds__(256) k_permute_fp4(const uint8_t *__restrict__ xq, const uint8_t *__restrict__ xsc,
                                                      const int32_t *__restrict__ pad_pair,
                                                      const int32_t *__restrict__ poff, int E, int H, int P, int k,
-                                                     uint8_t *__restrict__ xp, uint8_t *__restrict__ xp_atoms) {
+                                                     uint8_t *__restrict__ xp, uint8_t *__restrict__ xp_atoms, int sbk) {
     const int rows = poff[E + 1];
     const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
     const int nwarps = (gridDim.x * blockDim.x) >> 5;
     const int cb = H / 2 / 16;    // uint4 per code row
-    const int sw = H / 16 / 4;    // scale words per row
+    const int sw = H / sbk / 4;   // scale words per row
     for (int r = warp; r < rows; r += nwarps) {
         const int pair = pad_pair[r];
         if (pair < 0) continue;
@@ -1700,9 +1767,9 @@ __global__ void __launch_bounds__(256) k_permute_fp4(const uint8_t *__restrict__
         const uint4 *src = reinterpret_cast<const uint4 *>(xq + (size_t)t * (H / 2));
         uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * (H / 2));
         for (int i = lane; i < cb; i += 32) dst[i] = src[i];
-        const uint32_t *ss = reinterpret_cast<const uint32_t *>(xsc + (size_t)t * (H / 16));
+        const uint32_t *ss = reinterpret_cast<const uint32_t *>(xsc + (size_t)t * (H / sbk));
         const int rb = r >> 7, rr = r & 127;
-        uint8_t *ab = xp_atoms + (size_t)rb * (H / 64) * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
+        uint8_t *ab = xp_atoms + (size_t)rb * sw * 512 + (rr & 31) * 16 + (rr >> 5) * 4;
         for (int c = lane; c < sw; c += 32) *reinterpret_cast<uint32_t *>(ab + (size_t)c * 512) = ss[c];
     }
 }
@@ -1758,9 +1825,14 @@ bool tc_supported(const Plan &p) {
 }
 
 cudaError_t configure_tc(const Plan &) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_fp4<kSwiGLU, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(k_gemm_fp4<kScatter>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        e = cudaFuncSetAttribute(k_gemm_fp4<kScatter, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_fp4<kSwiGLU, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_gemm_fp4<kScatter, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_gemm_f16<kSwiGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kHSmemBytes);
     if (e == cudaSuccess)
@@ -1781,6 +1853,17 @@ cudaError_t configure_tc(const Plan &) {
 bool warp_mma_supported(const Plan &p) { return p.cfg.mode == MOE_W4A16 && tc_supported(p); }
 
 namespace {
+
+// Column groups (256 output columns each) of a chunk of the W4A4 down items
+// for T tokens: as many as keep the accumulator slice a chunk adds into,
+// T x 256 C fp32, within 16 MB of L2.
+int down_col_chunk(int T, int H) {
+    const int64_t per_group = (int64_t)T * 256 * 4;
+    int64_t c = ((int64_t)16 << 20) / per_group;
+    if (c < 1) c = 1;
+    if (c > H / 256) c = H / 256;
+    return (int)c;
+}
 
 // W4A16 on the tensor cores (see k_gemm_f16).
 cudaError_t launch_ffn_tc_f16(const Plan &p, const void *x, int T, const ExpertPtrs &r, const ExpertPtrs *s, int part,
@@ -1906,57 +1989,61 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
     a.pad_pair = p.pad_pair;
     a.wts = p.wts;
     a.P = T * c.top_k;
-    a.colfirst = T >= 128;
+    a.colfirst = T >= 128 ? down_col_chunk(T, H) : 0;
     a.k = c.top_k;
     a.acc = p.acc;
     a.err = p.err;
     a.b_ts = p.hts;
+    const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
+    const int sbk = mx ? 32 : 16;   // K values a scale byte covers
     bool ok = true;
     if (part == 0) {
         // permute x codes/scales into the padded rows first
         k_permute_fp4<<<p.num_sms * 4, 256, 0, st>>>(p.xq, p.xsc, p.pad_pair, p.poff, E, H, a.P, c.top_k, p.xp,
-                                                     p.xp_atoms);
+                                                     p.xp_atoms, sbk);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         ok &= make_map(&a.a0[0], r.gc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
         ok &= make_map(&a.a1[0], r.uc, H / 2, (uint64_t)E * I, H / 2, 128, 128, true);
-        ok &= make_map(&a.s0[0], r.gs, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
-        ok &= make_map(&a.s1[0], r.us, H / 16, (uint64_t)E * I, H / 16, 16, 128, false);
+        ok &= make_map(&a.s0[0], r.gs, H / sbk, (uint64_t)E * I, H / sbk, 16, 128, false);
+        ok &= make_map(&a.s1[0], r.us, H / sbk, (uint64_t)E * I, H / sbk, 16, 128, false);
         ok &= make_map(&a.a0[1], sp.gc, H / 2, Is_, H / 2, 128, 128, true);
         ok &= make_map(&a.a1[1], sp.uc, H / 2, Is_, H / 2, 128, 128, true);
-        ok &= make_map(&a.s0[1], sp.gs, H / 16, Is_, H / 16, 16, 128, false);
-        ok &= make_map(&a.s1[1], sp.us, H / 16, Is_, H / 16, 16, 128, false);
+        ok &= make_map(&a.s0[1], sp.gs, H / sbk, Is_, H / sbk, 16, 128, false);
+        ok &= make_map(&a.s1[1], sp.us, H / sbk, Is_, H / sbk, 16, 128, false);
         for (int c = 0; c < 3; ++c) ok &= make_map(&a.b[c], p.xp, H / 2, p.rows_pad_max, H / 2, 128, 32u << c, true);
         a.b_atoms = p.xp_atoms;
-        a.b_atoms_per_block = H / 64;
+        a.b_atoms_per_block = H / sbk / 4;
         a.nf = Imax / 128;
         a.ts_a0[0] = r.gts;
         a.ts_a1[0] = r.uts;
         a.ts_a0[1] = sp.gts;
         a.ts_a1[1] = sp.uts;
         if (!ok) return cudaErrorInvalidValue;
-        cudaError_t e0 = launch_pdl(k_gemm_fp4<kSwiGLU>, dim3(p.num_sms), dim3(fp4_threads(kSwiGLU)), kSmemBytes, st, a);
+        cudaError_t e0 = launch_pdl(mx ? k_gemm_fp4<kSwiGLU, 1> : k_gemm_fp4<kSwiGLU, 0>, dim3(p.num_sms),
+                                     dim3(fp4_threads(kSwiGLU)), kSmemBytes, st, a);
         if (e0 != cudaSuccess) return e0;
         return cudaGetLastError();
     }
     ok &= make_map(&a.a0[0], r.dc, I / 2, (uint64_t)E * H, I / 2, 128, 128, true);
-    ok &= make_map(&a.s0[0], r.ds, I / 16, (uint64_t)E * H, I / 16, 16, 128, false);
+    ok &= make_map(&a.s0[0], r.ds, I / sbk, (uint64_t)E * H, I / sbk, 16, 128, false);
     ok &= make_map(&a.a0[1], sp.dc, Is_ / 2, H, Is_ / 2, 128, 128, true);
-    ok &= make_map(&a.s0[1], sp.ds, Is_ / 16, H, Is_ / 16, 16, 128, false);
+    ok &= make_map(&a.s0[1], sp.ds, Is_ / sbk, H, Is_ / sbk, 16, 128, false);
     a.a1[0] = a.a0[0];
     a.a1[1] = a.a0[1];
     a.s1[0] = a.s0[0];
     a.s1[1] = a.s0[1];
     for (int c = 0; c < 3; ++c) ok &= make_map(&a.b[c], p.hq, Imax / 2, p.rows_pad_max, Imax / 2, 128, 32u << c, true);
     a.b_atoms = p.hq_atoms;
-    a.b_atoms_per_block = Imax / 64;
+    a.b_atoms_per_block = Imax / sbk / 4;
     a.nf = H / 256;
     a.ts_a0[0] = r.dts;
     a.ts_a0[1] = sp.dts;
     a.ts_a1[0] = r.dts;
     a.ts_a1[1] = sp.dts;
     if (!ok) return cudaErrorInvalidValue;
-    cudaError_t e0 = launch_pdl(k_gemm_fp4<kScatter>, dim3(p.num_sms), dim3(fp4_threads(kScatter)), kSmemBytes, st, a);
+    cudaError_t e0 = launch_pdl(mx ? k_gemm_fp4<kScatter, 1> : k_gemm_fp4<kScatter, 0>, dim3(p.num_sms),
+                                 dim3(fp4_threads(kScatter)), kSmemBytes, st, a);
     if (e0 != cudaSuccess) return e0;
     return cudaGetLastError();
 }

@@ -154,13 +154,15 @@ __global__ void __launch_bounds__(kThreads) k_quant_act_mx(const uint16_t *__res
     }
 }
 
-// MXFP4 SwiGLU output (W4A4 with MXFP4 weights, CUDA-core engine): fp32 h rows
-// -> codes [row][stride/2], scales [row][stride/32]; every block on its own,
-// no tensor scale (hts receives 1, 1).
+// MXFP4 SwiGLU output (W4A4 with MXFP4 weights): fp32 h rows -> codes
+// [row][stride/2] and scales, plain [row][stride/32] or (atoms != null) in the
+// tensor-core layout: 512-byte atoms of 128 rows x 4 blocks, stride/128 atoms
+// a 128-row block.  Every block on its own, no tensor scale (hts receives 1, 1).
 __global__ void __launch_bounds__(kThreads) k_quant_h_mx(const float *__restrict__ h, int stride,
                                                         const int32_t *__restrict__ poff, int E, int I, int Is,
                                                         const int32_t *__restrict__ pad_pair, uint4 *__restrict__ codes,
-                                                        uint8_t *__restrict__ scales, float *hts) {
+                                                        uint8_t *__restrict__ scales, uint8_t *__restrict__ atoms,
+                                                        float *hts) {
     if (blockIdx.x == 0 && threadIdx.x == 0) { hts[0] = 1.0f; hts[1] = 1.0f; }
     const int shared_row0 = poff[E];
     const int rows = poff[E + 1];
@@ -181,7 +183,13 @@ __global__ void __launch_bounds__(kThreads) k_quant_h_mx(const float *__restrict
         uint32_t s;
         quant_block32_mx(v, c, s);
         codes[(int64_t)row * (stride / 32) + blk] = c;
-        scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+        if (atoms) {
+            const int rr = row & 127;
+            atoms[((int64_t)(row >> 7) * (stride / 128) + (blk >> 2)) * 512 + (rr & 31) * 16 + (rr >> 5) * 4 +
+                  (blk & 3)] = (uint8_t)s;
+        } else {
+            scales[(int64_t)row * bpr + blk] = (uint8_t)s;
+        }
     }
 }
 
@@ -308,7 +316,7 @@ cudaError_t launch_quant_h(const Plan &p, bool tc_layout, cudaStream_t st) {
     if (p.cfg.weight_format == MOE_WEIGHTS_MXFP4) {
         k_quant_h_mx<<<p.num_sms * 8, kThreads, 0, st>>>(p.hbuf, Imax, p.poff, p.cfg.num_experts, p.cfg.inter,
                                                          p.cfg.shared_inter, p.pad_pair, reinterpret_cast<uint4 *>(p.hq),
-                                                         p.hsc, p.hts);
+                                                         p.hsc, tc_layout ? p.hq_atoms : nullptr, p.hts);
         return cudaGetLastError();
     }
     k_quant_h<<<p.num_sms * 8, kThreads, 0, st>>>(p.hbuf, Imax, p.poff, p.cfg.num_experts, p.cfg.inter,

@@ -1,7 +1,8 @@
 """MXFP4 experts (E2M1 codes, E8M0 scales a 32-value block, no tensor scale)
 on the GPU against the oracle: the device quantisers bit for bit, and
 moe_forward at the stated tolerance on the engines that take MXFP4 (the
-warp-level MMAs for W4A16, the CUDA cores for W4A16 and W4A4)."""
+warp-level MMAs for W4A16, the tcgen05 block-scaled MMAs for W4A4, the CUDA
+cores for both)."""
 import numpy as np
 import pytest
 import torch
@@ -84,6 +85,7 @@ def test_mx_w4a4_on_the_cuda_cores_end_to_end_and_by_stage(T):
     w = _mx("verify16_w4a4", tokens=T, hidden=1024, experts=16, inter=512, shared_inter=512)
     case = Case(w, T, mx=True)
     plan = plan_for(w, mx=True)
+    plan.set_path(moe.PATH_CUDA_CORE)
     out, st, _ = case.gpu_forward(plan)
     assert st == moe.OK, moe.STATUS[st]
     ref = case.oracle_forward()
@@ -104,11 +106,63 @@ def test_mx_w4a4_on_the_cuda_cores_end_to_end_and_by_stage(T):
     assert ok, stats
 
 
-def test_mx_plan_refuses_the_tcgen05_path_and_small_shapes():
+def _mx_stages(case, out, plan, tc):
+    """The GPU's own fp32 h, MXFP4-quantised by the oracle block by block (codes
+    and scales bit for bit), and the oracle's down product and combine on that h
+    at the plain tolerance."""
+    w = case.w
+    ref = case.oracle_forward()
+    state = gpu_h_state(plan, w, ref["offsets"], tc=tc, mx=True)
+    for key, h in state["h"].items():
+        c, s = oracle.quantize_mx(h)
+        np.testing.assert_array_equal(state["scales"][key], s, err_msg=f"h scales of {key}")
+        np.testing.assert_array_equal(state["codes"][key], c, err_msg=f"h codes of {key}")
+    assert state["ts"] == 1.0 and state["shared_ts"] == 1.0
+    ref2 = oracle.forward(case.x_host(), case.rw_host(), case.bias_host(), case.oracle_expert, k=w.top_k,
+                          router_kind=oracle.ROUTER_SIGMOID, mode=oracle.MODE_W4A4,
+                          shared=case.oracle_expert("shared"), h_in=dict(state["h"]), fmt=oracle.FMT_MXFP4)
+    ok, stats = oracle.compare_output(bf16_bits(out), ref2["out"], None)
+    assert ok, stats
+    return ref
+
+
+@pytest.mark.parametrize("T", [8, 64, 129])
+def test_mx_w4a4_on_the_tcgen05_mmas_end_to_end_and_by_stage(T):
+    """kind::mxf4 block-scaled MMAs: 8 tokens (32-row tiles), 64 (64-row
+    tiles), 129 (a ragged last 128-row tile on the shared expert)."""
+    w = _mx("verify16_w4a4", tokens=T, hidden=1024, experts=16, inter=512, shared_inter=1024)
+    case = Case(w, T + 3, mx=True)
+    plan = plan_for(w, mx=True)
+    plan.set_path(moe.PATH_TENSOR_CORE)
+    out, st, _ = case.gpu_forward(plan)
+    assert st == moe.OK, moe.STATUS[st]
+    ref = _mx_stages(case, out, plan, tc=True)
+    plan.close()
+    ok, stats = oracle.compare_output(bf16_bits(out), ref["out"], ref["band"])
+    assert ok, stats
+
+
+def test_mx_w4a4_full_size_verify_batch_on_the_tcgen05_mmas():
+    """The 16-token verification batch at full size (H 7168, 256 experts, I
+    2048, top-8, shared expert) with MXFP4 weights; AUTO takes the tcgen05 GEMMs."""
+    case = Case(_mx("verify16_w4a4"), 0, mx=True)
+    plan = plan_for(case.w, mx=True)
+    out, st, _ = case.gpu_forward(plan)
+    assert st == moe.OK, moe.STATUS[st]
+    ref = _mx_stages(case, out, plan, tc=True)
+    plan.close()
+    ok, stats = oracle.compare_output(bf16_bits(out), ref["out"], ref["band"])
+    assert ok, stats
+
+
+def test_mx_plan_path_rules_and_small_shapes():
     w = _mx("verify16_w4a4", hidden=1024, experts=16, inter=512, shared_inter=512)
     with plan_for(w, mx=True) as plan:
+        plan.set_path(moe.PATH_TENSOR_CORE)          # W4A4: kind::mxf4
+    w16 = _mx("decode4_w4a16", hidden=1024, experts=16, inter=512, shared_inter=512)
+    with plan_for(w16, mx=True) as plan:
         with pytest.raises(moe.MoeError) as e:
-            plan.set_path(moe.PATH_TENSOR_CORE)
+            plan.set_path(moe.PATH_TENSOR_CORE)      # W4A16 MXFP4: warp MMAs or CUDA cores
         assert e.value.status == moe.ERR_UNSUPPORTED_SHAPE
     with pytest.raises(moe.MoeError) as e:
         plan_for(_mx("tiny_w4a16"), mx=True)      # H 256, I 128: MXFP4 needs multiples of 512

@@ -54,7 +54,7 @@ def gpu_h_state(plan, w, offsets, tc: bool, mx: bool = False):
     codes = _view(plan, "h_codes", torch.uint8)[:rows * Imax // 2].reshape(rows, Imax // 2)
     if tc:
         atoms = _view(plan, "h_scale_atoms", torch.uint8)
-        scales = atoms_to_plain(atoms, rows, Imax // 16)
+        scales = atoms_to_plain(atoms, rows, Imax // bk)
     else:
         scales = _view(plan, "h_scales", torch.uint8)[:rows * Imax // bk].reshape(rows, Imax // bk)
     ts = _view(plan, "h_ts", torch.float32)[:2]
