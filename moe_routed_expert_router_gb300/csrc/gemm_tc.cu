@@ -908,6 +908,19 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         const uint32_t ring0 = smem_u32(code_ring);
         RingPos cs, as;
         bool ok = true;
+        // The TMEM store of A stage j completes (tcgen05.wait::st, then afull)
+        // only after stage j + 1 is widened in registers, so the store's
+        // latency overlaps the conversion work instead of adding to it.
+        int pend = -1;   // A slot whose store is in flight
+        auto finish_pending = [&]() {
+            if (pend >= 0) {
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull + pend);
+                pend = -1;
+            }
+        };
         for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
             Item it;
             if (!decode_item_h(a, item, EPI, ks, it)) continue;
@@ -941,18 +954,17 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                             o[blk * 8 + e] = *reinterpret_cast<uint32_t *>(&v);
                         }
                     }
+                    finish_pending();
                     if (ok && !mbar_wait(aempty + as.s, as.ph ^ 1, a.err)) ok = false;
                     if (ok) {
                         tmem_st16(t_lane + as.s * 64, o);
-                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                        tc_fence_before();
+                        pend = as.s;
                     }
-                    __syncwarp();
-                    if (lane == 0 && ok) mbar_arrive(afull + as.s);
                     as.next(kHAStages);
                 }
             }
         }
+        finish_pending();
     } else if (warp == 1 || warp == kHMma2) {
         // ------------------------------------------------ MMA issue: one lane an accumulator half
         if (lane == 0) {
