@@ -610,7 +610,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
 //   B ring     (4 x 16 KB, shared): f16 token rows, 128-byte swizzle, in
 //              boxes of 64 K values; a stage holds 512, 256 or 128 K values
 //              for tiles of up to 16, 32 or 64 rows (MMA N = 16, 32, 64);
-//   A ring     (4 x 64 TMEM columns): both operands widened to f16, 64 K
+//   A ring     (2 x 128 TMEM columns): both operands widened to f16, 128 K
 //              values a stage (row r in lane r, two K values a column);
 //   accumulators (2 x 128 TMEM columns): gate / up (or the two down-row
 //              halves), N <= 64 token columns each, double-buffered so an
@@ -631,11 +631,15 @@ constexpr int kHBK = 64;                         // K values per MMA step
 constexpr int kHBRows = 64;                      // token rows per tile (MMA N <= 64)
 constexpr int kHBTile = 16384;                   // B stage: 16 KB of f16 token rows
 constexpr int kHBStages = 4;
-constexpr int kHAStages = 4;                     // TMEM A ring
+// The A ring's stages are 128 K values (8 MMAs an accumulator half): the MMA
+// lanes' waits, commits and loop overhead come once per 8 MMAs (64 K values
+// a stage measured ~850 cycles a stage against ~340 of MMA issue).
+constexpr int kHAK = 128;                        // K values per A stage
+constexpr int kHAStages = 2;                     // TMEM A ring
 constexpr uint32_t kHACol0 = 256;                // first TMEM column of the A ring
 constexpr int kConvSplit = 2;                    // converter warps per (operand, 32-lane quarter)
 constexpr int kConvWarps = 8 * kConvSplit;
-constexpr int kConvCols = 32 / kConvSplit;       // TMEM columns (2 K values each) a converter fills per A stage
+constexpr int kConvCols = kHAK / 2 / kConvSplit; // TMEM columns (2 K values each) a converter fills per A stage
 static_assert(kConvSplit == 2, "the converter loop below is written for two K halves");
 constexpr int kHEpiWarps = 4;
 // the second MMA lane's warp, after the epilogue warps (warp 1 drives the
@@ -647,7 +651,8 @@ constexpr int kHThreads = 32 * (kHMma2 + 1);
 constexpr size_t kHRingBytes = (size_t)kHCStages * kHCodeStage + (size_t)kHBStages * kHBTile;
 constexpr size_t kHSmemBytes = kHRingBytes + 512 + 1024;
 static_assert(kHSmemBytes <= 227 * 1024, "W4A16 pipeline exceeds shared memory");
-static_assert(kHACol0 + kHAStages * 64 <= 512, "W4A16 TMEM plan exceeds 512 columns");
+static_assert(kHACol0 + kHAStages * kHAK <= 512, "W4A16 TMEM plan exceeds 512 columns");
+static_assert(kHAK == 128 && kConvCols == 32, "the converter and MMA loops below are written for 128-K A stages");
 
 struct HcArgs {
     CUtensorMap a0[2], a1[2];   // NVFP4 codes [rows][K/2], box 128 B x 128 rows, 128-byte swizzle
@@ -904,7 +909,7 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
         const int q = warp & 3;
         const int c = q * 32 + lane;
         const uint32_t sw = (uint32_t)(c & 7);
-        const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + kHACol0 + op * 32 + hf * kConvCols;
+        const uint32_t t_lane = tmem + ((uint32_t)(q * 32) << 16) + kHACol0 + op * (kHAK / 2) + hf * kConvCols;
         const uint32_t ring0 = smem_u32(code_ring);
         RingPos cs, as;
         bool ok = true;
@@ -928,36 +933,46 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 if (!mbar_wait(cfull + cs.s, cs.ph, a.err)) { ok = false; break; }
                 const uint32_t st = ring0 + cs.s * kHCodeStage;
                 const uint32_t row = st + op * kHCodeTile + c * 128;
+                // A stage j (K 128 j .. 128 j + 127): this warp's half hf is the
+                // code chunks 4 j + 2 hf and 4 j + 2 hf + 1 (32 K values each)
                 uint4 cq[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) cq[j] = lds128(row + (((uint32_t)(2 * j + hf) ^ sw) << 4));
+                for (int j = 0; j < 4; ++j)
+                    cq[j] = lds128(row + (((uint32_t)(4 * (j >> 1) + 2 * hf + (j & 1)) ^ sw) << 4));
                 const uint4 scv = lds128(st + 2 * kHCodeTile + op * 2048 + c * 16);
                 const uint32_t scw[4] = {scv.x, scv.y, scv.z, scv.w};
                 __syncwarp();
                 if (lane == 0) mbar_arrive(cempty + cs.s);   // this warp's bytes are in registers
                 cs.next(kHCStages);
 #pragma unroll
-                for (int j = 0; j < kHCK / kHBK; ++j) {
-                    const uint32_t cw4[4] = {cq[j].x, cq[j].y, cq[j].z, cq[j].w};
+                for (int j = 0; j < kHCK / kHAK; ++j) {
                     uint32_t o[kConvCols];
+                    // its scale blocks 8 j + 4 hf .. + 3: word 2 j + hf of the row's 16 bytes
+                    const uint32_t sw4 = scw[2 * j + hf];
 #pragma unroll
-                    for (int blk = 0; blk < 2; ++blk) {
-                        const uint32_t sb = (scw[j] >> (16 * hf + 8 * blk)) & 0xFFu;
-                        const uint32_t sc2 = e4m3x2_to_f16x2(sb * 0x101u);
-                        uint32_t h[8];
-                        e2m1x8_to_f16x8(cw4[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
-                        e2m1x8_to_f16x8(cw4[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
+                    for (int i = 0; i < 2; ++i) {
+                        const uint4 cc = cq[2 * j + i];
+                        const uint32_t cw4[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[e]),
-                                                *reinterpret_cast<const __half2 *>(&sc2));
-                            o[blk * 8 + e] = *reinterpret_cast<uint32_t *>(&v);
+                        for (int blk = 0; blk < 2; ++blk) {
+                            const uint32_t sb = (sw4 >> (8 * (2 * i + blk))) & 0xFFu;
+                            const uint32_t sc2 = e4m3x2_to_f16x2(sb * 0x101u);
+                            uint32_t h[8];
+                            e2m1x8_to_f16x8(cw4[2 * blk], *reinterpret_cast<uint32_t(*)[4]>(h));
+                            e2m1x8_to_f16x8(cw4[2 * blk + 1], *reinterpret_cast<uint32_t(*)[4]>(h + 4));
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&h[e]),
+                                                    *reinterpret_cast<const __half2 *>(&sc2));
+                                o[i * 16 + blk * 8 + e] = *reinterpret_cast<uint32_t *>(&v);
+                            }
                         }
                     }
                     finish_pending();
                     if (ok && !mbar_wait(aempty + as.s, as.ph ^ 1, a.err)) ok = false;
                     if (ok) {
-                        tmem_st16(t_lane + as.s * 64, o);
+                        tmem_st16(t_lane + as.s * kHAK, *reinterpret_cast<const uint32_t(*)[16]>(o));
+                        tmem_st16(t_lane + as.s * kHAK + 16, *reinterpret_cast<const uint32_t(*)[16]>(o + 16));
                         pend = as.s;
                     }
                     as.next(kHAStages);
@@ -981,26 +996,28 @@ __global__ void __launch_bounds__(kHThreads, 1) k_gemm_f16(const __grid_constant
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 128 + 64 * hs;
                 const int rc = hrows_class(it.valid);
-                const int rows = 16 << rc, boxes = 8 >> rc, nq = it.K / kHBK;
+                const int rows = 16 << rc, boxes = 8 >> rc, nqa = it.K / kHAK;
+                constexpr int kBoxesA = kHAK / kHBK;   // B boxes (64 K values each) an A stage takes
                 const uint32_t idesc = idesc_f16((uint32_t)rows);
-                for (int qq = 0; qq < nq; ++qq) {
-                    const int bx = qq % boxes;
-                    if (!mbar_wait(afull + as.s, as.ph, a.err) || (bx == 0 && !mbar_wait(bfull + bs.s, bs.ph, a.err))) {
+                for (int qa = 0; qa < nqa; ++qa) {
+                    const int b0 = (qa * kBoxesA) % boxes;   // the A stage's first box in its B stage
+                    if (!mbar_wait(afull + as.s, as.ph, a.err) || (b0 == 0 && !mbar_wait(bfull + bs.s, bs.ph, a.err))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t at = tmem + kHACol0 + as.s * 64;
-                    const uint32_t bt = smem_u32(b_ring + bs.s * kHBTile) + bx * rows * 128;
+                    const uint32_t at = tmem + kHACol0 + as.s * kHAK + (kHAK / 2) * hs;
+                    const uint64_t bd0 = desc_sw128(smem_u32(b_ring + bs.s * kHBTile) + b0 * rows * 128);
+                    const uint32_t box_units = (uint32_t)(rows * 128) >> 4;   // a box in descriptor address units
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t accum = (qq | kk) ? 1u : 0u;
-                        const uint64_t bd = desc_sw128(bt + 32 * kk);
-                        mma_f16_ts(d, at + 32 * hs + 8 * kk, bd, idesc, accum);
+                    for (int kk = 0; kk < kHAK / 16; ++kk) {
+                        const uint32_t accum = (qa | kk) ? 1u : 0u;
+                        const uint64_t bd = bd0 + (uint64_t)((kk >> 2) * box_units + 2 * (kk & 3));
+                        mma_f16_ts(d, at + 8 * kk, bd, idesc, accum);
                     }
                     mma_commit(aempty + as.s);
                     as.next(kHAStages);
-                    if (bx == boxes - 1 || qq == nq - 1) {
+                    if (b0 + kBoxesA == boxes || qa == nqa - 1) {
                         mma_commit(bempty + bs.s);
                         bs.next(kHBStages);
                     }
