@@ -345,8 +345,12 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                 tc_fence_after();
                 const uint32_t nrows = 32u << rows_class(it.valid);
                 const int ks_n = it.K / kBK;
+#pragma unroll 2
                 for (int ks = 0; ks < ks_n; ++ks) {
-                    if (!mbar_wait(sf_ready + s, ph, a.err) || !mbar_wait(full + s, ph, a.err)) { ok = false; break; }
+                    // sf_ready completes after every scale warp saw the stage's loads
+                    // land (each waits on full first), so it covers full as well: one
+                    // wait, not two (a satisfied wait still costs ~60 cycles here)
+                    if (!mbar_wait(sf_ready + s, ph, a.err)) { ok = false; break; }
                     tc_fence_after();
                     // descriptors of the stage's operands: built once, then stepped by
                     // their 16-byte address units (the smem window is below 256 KB, so
