@@ -231,6 +231,13 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream);
  * Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 
+/* W4A4 with MXFP4 weights on the tensor cores quantises the SwiGLU output in
+ * the gate/up launch (every 32-value block on its own scale, one pass) and by
+ * default writes only its codes and scales.  keep = 1: also store the fp32 h
+ * (debug buffer "h"), for stage-by-stage checks.  Every other path stores h
+ * anyway.  MOE_ERR_INVALID_ARG for a NULL plan. */
+moe_status moe_plan_keep_h(moe_plan plan, int32_t keep);
+
 /* Expert-FFN implementation moe_forward uses.  CUDA_CORE: weight-streaming
  * kernels on the CUDA cores (any shape).  TENSOR_CORE: grouped GEMMs on the
  * 5th-generation tensor cores (tcgen05; W4A4 block-scaled FP4, W4A16 with the

@@ -30,7 +30,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_NONFINITE, ERR_T
 EXPORTS = ["moe_plan_create", "moe_plan_destroy", "moe_route", "moe_forward", "moe_forward_host",
            "moe_quantize_act", "moe_quantize_nvfp4", "moe_plan_sync_status", "moe_plan_debug_buffer",
            "moe_plan_set_profiling", "moe_plan_read_profile", "moe_plan_set_path", "moe_plan_check_timeout",
-           "moe_route_static", "moe_convert_f32", "moe_quantize_mxfp4", "moe_status_string", "moe_version"]
+           "moe_route_static", "moe_convert_f32", "moe_quantize_mxfp4", "moe_plan_keep_h", "moe_status_string",
+           "moe_version"]
 FMT_E4M3, FMT_E2M1 = 0, 1
 PATH_AUTO, PATH_CUDA_CORE, PATH_TENSOR_CORE, PATH_WARP_MMA = 0, 1, 2, 3
 STAGES = ["route", "group", "quant_x", "permute", "gate_up", "quant_h", "down", "finalize"]
@@ -77,6 +78,7 @@ def lib():
         L.moe_plan_sync_status.argtypes = [P, P]
         L.moe_plan_debug_buffer.argtypes = [P, ctypes.c_char_p, ctypes.POINTER(P), ctypes.POINTER(ctypes.c_size_t)]
         L.moe_plan_set_profiling.argtypes = [P, I32]
+        L.moe_plan_keep_h.argtypes = [P, I32]
         L.moe_plan_set_path.argtypes = [P, I32]
         L.moe_plan_check_timeout.argtypes = [P, ctypes.c_int64, P]
         L.moe_route_static.argtypes = [P, I32, I32, P, P, I32, I32, I32, I32, P, P, P, P, P]
@@ -251,6 +253,10 @@ class Plan:
 
     def set_path(self, path: int):
         _check(lib().moe_plan_set_path(self.handle, path), "moe_plan_set_path")
+
+    def keep_h(self, on: bool):
+        """Store the fp32 SwiGLU output also where gate/up quantises it itself (MXFP4 W4A4, tensor cores)."""
+        _check(lib().moe_plan_keep_h(self.handle, int(bool(on))), "moe_plan_keep_h")
 
     def set_profiling(self, on: bool):
         _check(lib().moe_plan_set_profiling(self.handle, int(bool(on))), "moe_plan_set_profiling")

@@ -225,7 +225,9 @@ moe_status forward_device(moe_plan plan, const void *x, int32_t T, const void *r
         e = tc ? moe::launch_ffn_tc(p, x, T, r, shp, 0, st, wm) : moe::launch_ffn_simt(p, x, T, r, shp, 0, st);
         if (s.done(e, (tc && !wm) ? 2 : 1) != cudaSuccess) return MOE_ERR_CUDA;   // + the permute launch
     }
-    if (p.cfg.mode == MOE_W4A4) {
+    // W4A4: the SwiGLU output's quantisation, a pass of its own except for
+    // MXFP4 on the tensor cores, whose gate/up epilogue quantises h itself
+    if (p.cfg.mode == MOE_W4A4 && !(tc && p.cfg.weight_format == MOE_WEIGHTS_MXFP4)) {
         Stage s(plan, MOE_STAGE_QUANT_H, st);
         if (s.done(moe::launch_quant_h(p, tc, st), 1) != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -320,6 +322,12 @@ moe_status moe_plan_set_path(moe_plan plan, int32_t path) {
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (path == MOE_PATH_WARP_MMA && !moe::warp_mma_supported(plan->p)) return MOE_ERR_UNSUPPORTED_SHAPE;
     plan->path = path;
+    return MOE_OK;
+}
+
+moe_status moe_plan_keep_h(moe_plan plan, int32_t keep) {
+    if (!plan) return MOE_ERR_INVALID_ARG;
+    plan->p.keep_h = keep != 0;
     return MOE_OK;
 }
 

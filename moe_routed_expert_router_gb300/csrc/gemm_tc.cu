@@ -98,6 +98,11 @@ struct TcArgs {
     float *acc;             // G2 output [T][H]
     int *err;
     int colfirst;           // down items: column groups a chunk (large T; 0: tile by tile; see decode_item)
+    // MXFP4 gate/up: the SwiGLU output quantised in the epilogue (single pass)
+    uint8_t *hq;            // codes [rows][hstride / 2]
+    uint8_t *hq_atoms;      // E8M0 scales in the tensor-core layout (hstride / 128 atoms a 128-row block)
+    float *hts_out;         // [2] SwiGLU tensor scales: 1 (MXFP4 has none)
+    int keep_h;             // also store the fp32 h (stage-by-stage checks)
 };
 
 __device__ __forceinline__ void tma_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x, int y) {
@@ -262,6 +267,7 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_items = a.scratch->n_tiles * a.nf;
+    if (EPI == kSwiGLU && MX && blockIdx.x == 0 && threadIdx.x == 0) { a.hts_out[0] = 1.0f; a.hts_out[1] = 1.0f; }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -539,7 +545,42 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
             __syncwarp();
             if (lane == 0) mbar_arrive(acc_empty);
             if (col0 >= n_end) continue;
-            if (EPI == kSwiGLU) {
+            if (EPI == kSwiGLU && MX) {
+                // MXFP4: every 32-value block of h has its own scale and no batch
+                // amax is needed, so h is quantised here, in one pass. The
+                // warp's 32 lanes hold 32 consecutive features of a token row,
+                // one MX block: the warp maximum of |h| gives the E8M0 byte
+                // (clamp(floor(log2 amax) - 2 + 127, 0, 254), 0 for a zero
+                // block), each lane its E2M1 code of h * 2^(127 - byte), and lane
+                // pairs / quadruples assemble the block's 16 code bytes.
+                const float sg = a.ts_a0[m][e], su = a.ts_a1[m][e];
+                const int fb = it.f * 128 + quad * 32;   // the block's first feature
+                const int blk = fb >> 5;
+                float *hrow = a.hbuf + (size_t)(it.row0 + col0) * a.hstride + fb + lane;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    if (col0 + j < n_end) {   // the same for every lane
+                        const float gv = v0[j] * sg, uv = v1[j] * su;
+                        const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+                        if (a.keep_h) hrow[(size_t)j * a.hstride] = h;
+                        const uint32_t ab = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h)));
+                        const int field = (int)((ab >> 23) & 0xFFu);
+                        const int sx = field > 2 ? field - 2 : 0;
+                        const float inv = __uint_as_float((uint32_t)(254 - sx) << 23);   // 2^(127 - sx)
+                        const uint32_t nib = f32x2_to_e2m1x2(__fmul_rn(h, inv), 0.0f) & 0xFu;
+                        const uint32_t b = nib | (__shfl_down_sync(0xffffffffu, nib, 1) << 4);   // even lanes
+                        const uint32_t w = b | (__shfl_down_sync(0xffffffffu, b, 2) << 8) |
+                                           (__shfl_down_sync(0xffffffffu, b, 4) << 16) |
+                                           (__shfl_down_sync(0xffffffffu, b, 6) << 24);   // lanes 8 q: word q
+                        const int r = it.row0 + col0 + j, rr = r & 127;
+                        if ((lane & 7) == 0)
+                            *reinterpret_cast<uint32_t *>(a.hq + (size_t)r * (a.hstride / 2) + (fb >> 1) + (lane >> 1)) = w;
+                        if (lane == 0)
+                            a.hq_atoms[((size_t)(r >> 7) * (a.hstride / 128) + (blk >> 2)) * 512 + (rr & 31) * 16 +
+                                       (rr >> 5) * 4 + (blk & 3)] = (uint8_t)sx;
+                    }
+                }
+            } else if (EPI == kSwiGLU) {
                 // activation tensor scale (MXFP4 activations have none)
                 const float xts = MX ? 1.0f : __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
                 const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
@@ -2029,6 +2070,12 @@ cudaError_t launch_ffn_tc(const Plan &p, const void *x, int T, const ExpertPtrs 
     a.b_ts = p.hts;
     const bool mx = c.weight_format == MOE_WEIGHTS_MXFP4;
     const int sbk = mx ? 32 : 16;   // K values a scale byte covers
+    if (mx) {   // the gate/up epilogue quantises the SwiGLU output itself
+        a.hq = p.hq;
+        a.hq_atoms = p.hq_atoms;
+        a.hts_out = p.hts;
+        a.keep_h = p.keep_h;
+    }
     bool ok = true;
     if (part == 0) {
         // permute x codes/scales into the padded rows first

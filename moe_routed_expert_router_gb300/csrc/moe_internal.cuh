@@ -49,6 +49,7 @@ struct Plan {
     moe_config cfg;
     int device = 0;
     int num_sms = 0;
+    int keep_h = 0;             // also store the fp32 SwiGLU output where the gate/up launch quantises it
     int64_t pairs_max = 0;      // max_tokens * k
     int64_t rows_pad_max = 0;   // padded permuted rows (routed + shared)
     int64_t chunks_max = 0;

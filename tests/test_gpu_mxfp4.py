@@ -134,6 +134,7 @@ def test_mx_w4a4_on_the_tcgen05_mmas_end_to_end_and_by_stage(T):
     case = Case(w, T + 3, mx=True)
     plan = plan_for(w, mx=True)
     plan.set_path(moe.PATH_TENSOR_CORE)
+    plan.keep_h(True)   # the gate/up launch quantises h itself; keep the fp32 h to check it
     out, st, _ = case.gpu_forward(plan)
     assert st == moe.OK, moe.STATUS[st]
     ref = _mx_stages(case, out, plan, tc=True)
@@ -142,11 +143,34 @@ def test_mx_w4a4_on_the_tcgen05_mmas_end_to_end_and_by_stage(T):
     assert ok, stats
 
 
+def test_mx_w4a4_tensor_cores_quantise_h_in_the_gate_up_launch():
+    """MXFP4 needs no batch amax for h, so the gate/up epilogue quantises it in
+    the same pass: no separate quantiser launch, and the same codes and scales
+    whether or not the fp32 h is also stored."""
+    w = _mx("verify16_w4a4", tokens=64, hidden=1024, experts=16, inter=512, shared_inter=512)
+    case = Case(w, 2, mx=True)
+    plan = plan_for(w, mx=True)
+    plan.set_path(moe.PATH_TENSOR_CORE)
+    plan.set_profiling(True)
+    bufs = {}
+    for keep in (False, True):
+        plan.keep_h(keep)
+        _, st, _ = case.gpu_forward(plan)
+        assert st == moe.OK, moe.STATUS[st]
+        prof = plan.read_profile()
+        assert prof["quant_h"][1] == 0 and prof["quant_h"][2] == 0, prof["quant_h"]
+        bufs[keep] = [moe.device_view(*plan.debug_buffer(n)).clone() for n in ("h_codes", "h_scale_atoms")]
+    plan.close()
+    for a, b in zip(bufs[False], bufs[True]):
+        assert torch.equal(a, b)
+
+
 def test_mx_w4a4_full_size_verify_batch_on_the_tcgen05_mmas():
     """The 16-token verification batch at full size (H 7168, 256 experts, I
     2048, top-8, shared expert) with MXFP4 weights; AUTO takes the tcgen05 GEMMs."""
     case = Case(_mx("verify16_w4a4"), 0, mx=True)
     plan = plan_for(case.w, mx=True)
+    plan.keep_h(True)
     out, st, _ = case.gpu_forward(plan)
     assert st == moe.OK, moe.STATUS[st]
     ref = _mx_stages(case, out, plan, tc=True)
