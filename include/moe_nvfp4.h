@@ -226,8 +226,9 @@ moe_status moe_plan_sync_status(moe_plan plan, void *stream);
  * step in isolation.  name: "h_codes", "h_scales", "h_scale_atoms" (W4A4 on
  * the tensor cores: the SwiGLU scales in 512-byte atoms of 128 rows x 4
  * blocks, byte (r % 32) * 16 + (r % 128 / 32) * 4 + b % 4 of atom
- * (r / 128, b / 4)), "h_ts", "x_ts", "acc", "counts", "padded_offsets",
- * "offsets", "sorted", "pad_pair", "tiles", "h".
+ * (r / 128, b / 4)), "h_ts", "x_ts", "acc", "counts" (pairs an expert, where
+ * the grouping runs as a launch of its own), "padded_offsets", "offsets",
+ * "sorted", "pad_pair", "tiles", "h".
  * Returns MOE_ERR_INVALID_ARG for an unknown name. */
 moe_status moe_plan_debug_buffer(moe_plan plan, const char *name, void **ptr, size_t *bytes);
 

@@ -189,7 +189,7 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
 template <int NPL>
 __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int t, int E, int k, int kind, int renorm,
                                            int32_t *__restrict__ ids, float *__restrict__ wts,
-                                           int32_t *__restrict__ counts, int *err) {
+                                           int32_t *__restrict__ counts, int *err, int *s_ids_out = nullptr) {
     const int lane = threadIdx.x & 31;
     const float NEG = -__int_as_float(0x7f800000);
     float v[NPL];
@@ -229,6 +229,7 @@ __device__ __forceinline__ void topk_token(const float *__restrict__ logits, int
     if (nan_left && lane == 0) atomicOr(err, kErrDevice);
     if (lane < k) {
         ids[(size_t)t * k + lane] = mine_id;
+        if (s_ids_out) s_ids_out[t * k + lane] = mine_id;   // the same block groups the pairs next
         if (counts) atomicAdd(counts + mine_id, 1);
     }
     float num = 0.0f, den;
@@ -286,6 +287,9 @@ __host__ __device__ __forceinline__ size_t group_small_smem(int E, int P) {
 // rank of t's pair inside the expert (the stable order, increasing p). Every
 // step is then one thread a pair or an expert. The padding rows of the map
 // were set to -1 by every block of the launch before this one started.
+__device__ __forceinline__ int *group_small_ids(int *sm, int E) { return sm + 5 * (E + 2); }
+
+// ids == nullptr: the pairs' experts are already in group_small_ids(sm, E).
 __device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids, int P, int E, int T, int k,
                             int *sm, CallScratch *sc, int *err) {
     unsigned *s_mask = reinterpret_cast<unsigned *>(sm);
@@ -300,7 +304,7 @@ __device__ void group_small(const GroupArgs &g, const int32_t *__restrict__ ids,
     for (int i = tid; i < E; i += nthr) s_mask[i] = 0u;
     __syncthreads();
     for (int q = tid; q < P; q += nthr) {
-        int e = ids[q];
+        int e = ids ? ids[q] : s_ids[q];
         if (e < 0 || e >= E) { atomicOr(err, kErrDevice); e = -1; }
         s_ids[q] = e;
         if (e >= 0) atomicOr(&s_mask[e], 1u << (q / k));
@@ -558,18 +562,23 @@ __global__ void __launch_bounds__(kDecodeRouterThreads) k_router_decode(
         const int r0 = (int)blockIdx.x * per, r1 = min(grp.rows_cap, r0 + per);
         for (int r = r0 + tid; r < r1; r += kDecodeRouterThreads) grp.pad_pair[r] = -1;
     }
-    __threadfence();
+    // release this block's logits and padding rows before its ticket; the last
+    // block's acquire makes every block's visible to it
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
     __syncthreads();
     if (tid == 0) s_last = (atomicAdd(&sc->route_done, 1) == (int)gridDim.x - 1);
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    // with the grouping in this block, the pairs' experts go to its shared
+    // memory too (and no expert counts: the grouping counts from bit masks)
+    int *gsm = reinterpret_cast<int *>(dsmem + decode_router_smem(H, T, E, (int)sizeof(W)));
     for (int t = warp; t < T; t += kDecodeRouterThreads / 32)
-        topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, counts, err);
+        topk_token<NPL>(logits, t, E, k, kind, renorm, ids, wts, grp.active ? nullptr : counts, err,
+                        grp.active ? group_small_ids(gsm, E) : nullptr);
     if (grp.active) {
         __syncthreads();   // the block's ids are visible to all its threads
-        int *gsm = reinterpret_cast<int *>(dsmem + decode_router_smem(H, T, E, (int)sizeof(W)));
-        group_small(grp, ids, T * k, E, T, k, gsm, sc, err);
+        group_small(grp, nullptr, T * k, E, T, k, gsm, sc, err);
     }
 }
 
