@@ -581,8 +581,8 @@ __global__ void __launch_bounds__(fp4_threads(EPI), 1) k_gemm_fp4(const __grid_c
                     }
                 }
             } else if (EPI == kSwiGLU) {
-                // activation tensor scale (MXFP4 activations have none)
-                const float xts = MX ? 1.0f : __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
+                // NVFP4: the activation tensor scale from the batch amax
+                const float xts = __fdiv_rn(__uint_as_float(a.scratch->x_amax), 2688.0f);
                 const float sg = a.ts_a0[m][e] * xts, su = a.ts_a1[m][e] * xts;
                 const int feat = it.f * 128 + quad * 32 + lane;
                 float mx = 0.0f;
